@@ -1,0 +1,278 @@
+/*
+ * Plain single-threaded CPU oracle for Invariant Bit Packing (IBP).
+ * TEST INFRASTRUCTURE ONLY (see ibp_oracle.h): nothing in the GPU codec uses it.
+ *
+ * Written for obviousness, not speed: every bit is moved by its own loop
+ * iteration, elements are assembled byte by byte in little-endian order, and the
+ * steps follow the order in which the IBP page ("Reducing the GPU Memory
+ * Bottleneck with Lossless Compression for ML -- Extended", technical summary)
+ * states them: preprocessing -> compression -> decompression.
+ *
+ * Readings of points the page leaves open (also listed in the design notes):
+ *  R1 one w-bit mask/bitval pair applies to every element word;
+ *  R2 all participation bits of a row come first, then the block payloads (the
+ *     page prepends the bit per block and scans block sizes with a prefix scan;
+ *     a header-first layout gives the same bit count and lets the scan start at once);
+ *  R3 LSB-first bit order inside little-endian 32-bit words; a field holds the
+ *     element's non-invariant bits in ascending position order;
+ *  R4 bit j is invariant iff count(majority value) >= T*N in IEEE double;
+ *  R5 majority value on a tie is 0;
+ *  R6 with an empty mask every block "matches" and costs B*w bits anyway;
+ *  R7 a row is kept compressed only when its stream needs fewer whole 32-bit
+ *     words than the raw row has bytes / 4.
+ */
+#include "ibp_oracle.h"
+
+#include <string.h>
+
+namespace {
+
+/* read element e of a little-endian array of w-bit words */
+uint32_t load_elem(const unsigned char *base, int64_t e, int w_bits) {
+  int nbytes = w_bits / 8;
+  uint32_t v = 0;
+  for (int k = 0; k < nbytes; ++k) v |= (uint32_t)base[e * nbytes + k] << (8 * k);
+  return v;
+}
+
+void store_elem(unsigned char *base, int64_t e, int w_bits, uint32_t v) {
+  int nbytes = w_bits / 8;
+  for (int k = 0; k < nbytes; ++k) base[e * nbytes + k] = (unsigned char)((v >> (8 * k)) & 0xFFu);
+}
+
+int bit_of(uint32_t x, int j) { return (int)((x >> j) & 1u); }
+
+int popcount_w(uint32_t x, int w_bits) {
+  int c = 0;
+  for (int j = 0; j < w_bits; ++j) c += bit_of(x, j);
+  return c;
+}
+
+/* the non-invariant bits of x, packed in ascending position order */
+uint32_t extract_kept(uint32_t x, uint32_t mask, int w_bits) {
+  uint32_t field = 0;
+  int k = 0;
+  for (int j = 0; j < w_bits; ++j) {
+    if (!bit_of(mask, j)) {
+      field |= (uint32_t)bit_of(x, j) << k;
+      ++k;
+    }
+  }
+  return field;
+}
+
+/* inverse of extract_kept: spread field over the non-invariant positions, then
+   put the invariant values back */
+uint32_t reinsert(uint32_t field, uint32_t mask, uint32_t bitval, int w_bits) {
+  uint32_t x = 0;
+  int k = 0;
+  for (int j = 0; j < w_bits; ++j) {
+    if (bit_of(mask, j)) {
+      x |= (uint32_t)bit_of(bitval, j) << j;
+    } else {
+      x |= (uint32_t)bit_of(field, k) << j;
+      ++k;
+    }
+  }
+  return x;
+}
+
+/* bit stream over little-endian 32-bit words, LSB first */
+void put_bit(unsigned char *stream, int64_t pos, int bit) {
+  int64_t word = pos / 32;
+  int in_word = (int)(pos % 32);
+  int64_t byte = word * 4 + in_word / 8;
+  int in_byte = in_word % 8;
+  if (bit) stream[byte] = (unsigned char)(stream[byte] | (1u << in_byte));
+  else stream[byte] = (unsigned char)(stream[byte] & ~(1u << in_byte));
+}
+
+int get_bit(const unsigned char *stream, int64_t pos) {
+  int64_t word = pos / 32;
+  int in_word = (int)(pos % 32);
+  int64_t byte = word * 4 + in_word / 8;
+  int in_byte = in_word % 8;
+  return (stream[byte] >> in_byte) & 1;
+}
+
+void put_field(unsigned char *stream, int64_t *pos, uint32_t value, int nbits) {
+  for (int i = 0; i < nbits; ++i) {
+    put_bit(stream, *pos, bit_of(value, i));
+    *pos += 1;
+  }
+}
+
+uint32_t get_field(const unsigned char *stream, int64_t *pos, int nbits) {
+  uint32_t v = 0;
+  for (int i = 0; i < nbits; ++i) {
+    v |= (uint32_t)get_bit(stream, *pos) << i;
+    *pos += 1;
+  }
+  return v;
+}
+
+int valid_width(int w_bits) { return w_bits == 16 || w_bits == 32; }
+
+uint32_t width_mask(int w_bits) { return w_bits == 32 ? 0xFFFFFFFFu : ((1u << w_bits) - 1u); }
+
+}  // namespace
+
+extern "C" int64_t ibpo_slot_bytes(int64_t row_elems, int w_bits) {
+  int64_t raw = row_elems * (w_bits / 8);
+  return (raw + 15) / 16 * 16;
+}
+
+/* Preprocessing: count, per bit position, how many sampled elements hold a 1;
+   a position is invariant when its majority value is held by at least a
+   fraction T of the sample. */
+extern "C" int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, double T,
+                               uint32_t *mask_out, uint32_t *bitval_out) {
+  if (!elems || n_elems <= 0 || !valid_width(w_bits) || !(T >= 0.0 && T <= 1.0) || !mask_out ||
+      !bitval_out)
+    return IBPO_BAD_ARG;
+  const unsigned char *base = (const unsigned char *)elems;
+  int64_t ones[32];
+  for (int j = 0; j < 32; ++j) ones[j] = 0;
+  for (int64_t e = 0; e < n_elems; ++e) {
+    uint32_t x = load_elem(base, e, w_bits);
+    for (int j = 0; j < w_bits; ++j) ones[j] += bit_of(x, j);
+  }
+  uint32_t mask = 0, bitval = 0;
+  for (int j = 0; j < w_bits; ++j) {
+    int64_t c1 = ones[j];
+    int64_t c0 = n_elems - c1;
+    int v = c1 > c0 ? 1 : 0;               /* R5: a tie picks 0 */
+    int64_t cv = v ? c1 : c0;
+    if ((double)cv >= T * (double)n_elems) { /* R4 */
+      mask |= 1u << j;
+      bitval |= (uint32_t)v << j;
+    }
+  }
+  *mask_out = mask;
+  *bitval_out = bitval;
+  return IBPO_OK;
+}
+
+/* Compression: test each block against mask/bitval, record a participation bit
+   per block, strip the invariant bits of matching blocks and close the gaps,
+   keep failing blocks as they are; store the row in its fixed-size slot and flag
+   it in the bitmask when that saves space. */
+extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                             int64_t block_elems, uint32_t mask, uint32_t bitval, void *slots,
+                             int64_t slot_bytes, uint32_t *bitmask, uint32_t *row_bits) {
+  if (!rows || !slots || !bitmask || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) ||
+      block_elems <= 0 || row_elems % block_elems != 0 ||
+      slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+    return IBPO_BAD_ARG;
+  mask &= width_mask(w_bits);
+  bitval &= mask;
+  const unsigned char *in = (const unsigned char *)rows;
+  unsigned char *out = (unsigned char *)slots;
+  const int64_t raw_bytes = row_elems * (w_bits / 8);
+  const int64_t nb = row_elems / block_elems;
+  const int m = w_bits - popcount_w(mask, w_bits);
+
+  for (int64_t q = 0; q < (n_rows + 31) / 32; ++q) bitmask[q] = 0;
+
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const unsigned char *row = in + r * raw_bytes;
+    unsigned char *slot = out + r * slot_bytes;
+
+    /* participation bit per block */
+    int64_t bits = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+      int match = 1;
+      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+        uint32_t x = load_elem(row, e, w_bits);
+        if ((x & mask) != bitval) match = 0;
+      }
+      bits += 1 + block_elems * (match ? m : w_bits);
+    }
+    if (row_bits) row_bits[r] = (uint32_t)bits;
+
+    int64_t stored_words = (bits + 31) / 32;
+    int compressed = 4 * stored_words < raw_bytes; /* R7 */
+    if (!compressed) {
+      for (int64_t k = 0; k < raw_bytes; ++k) slot[k] = row[k];
+      continue;
+    }
+    for (int64_t k = 0; k < 4 * stored_words; ++k) slot[k] = 0;
+    int64_t pos = 0;
+    /* header: all participation bits first (R2) */
+    for (int64_t b = 0; b < nb; ++b) {
+      int match = 1;
+      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e)
+        if ((load_elem(row, e, w_bits) & mask) != bitval) match = 0;
+      put_bit(slot, pos, match);
+      pos += 1;
+    }
+    /* payloads, block by block */
+    for (int64_t b = 0; b < nb; ++b) {
+      int match = get_bit(slot, b);
+      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+        uint32_t x = load_elem(row, e, w_bits);
+        if (match) put_field(slot, &pos, extract_kept(x, mask, w_bits), m);
+        else put_field(slot, &pos, x, w_bits);
+      }
+    }
+    bitmask[r / 32] |= 1u << (r % 32);
+  }
+  return IBPO_OK;
+}
+
+/* Decompression-gather: for each requested row read the participation bits,
+   walk the blocks in order (each block's start is the sum of the sizes of the
+   blocks before it), and rebuild every element by putting the invariant bits
+   back in place. */
+extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                      int64_t row_elems, int w_bits, int64_t block_elems,
+                                      const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
+                                      const int64_t *idx, int64_t n_idx, void *out) {
+  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
+      row_elems % block_elems != 0 || slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+    return IBPO_BAD_ARG;
+  if (n_idx == 0) return IBPO_OK;
+  if (!slots || !bitmask || !idx || !out) return IBPO_BAD_ARG;
+  mask &= width_mask(w_bits);
+  bitval &= mask;
+  const unsigned char *in = (const unsigned char *)slots;
+  unsigned char *dst = (unsigned char *)out;
+  const int64_t raw_bytes = row_elems * (w_bits / 8);
+  const int64_t nb = row_elems / block_elems;
+  const int m = w_bits - popcount_w(mask, w_bits);
+  int status = IBPO_OK;
+
+  for (int64_t i = 0; i < n_idx; ++i) {
+    int64_t r = idx[i];
+    unsigned char *orow = dst + i * raw_bytes;
+    if (r < 0 || r >= n_rows) {
+      if (status == IBPO_OK) status = IBPO_BAD_INDEX;
+      continue;
+    }
+    const unsigned char *slot = in + r * slot_bytes;
+    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);
+    if (!compressed) {
+      for (int64_t k = 0; k < raw_bytes; ++k) orow[k] = slot[k];
+      continue;
+    }
+    /* the stream length the participation bits describe must fit the rule the
+       compressor used, else the slot is corrupt */
+    int64_t bits = 0;
+    for (int64_t b = 0; b < nb; ++b) bits += 1 + block_elems * (get_bit(slot, b) ? m : w_bits);
+    if (4 * ((bits + 31) / 32) >= raw_bytes) {
+      if (status == IBPO_OK) status = IBPO_CORRUPT;
+      continue;
+    }
+    int64_t pos = nb; /* first payload bit */
+    for (int64_t b = 0; b < nb; ++b) {
+      int match = get_bit(slot, b);
+      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+        uint32_t x;
+        if (match) x = reinsert(get_field(slot, &pos, m), mask, bitval, w_bits);
+        else x = get_field(slot, &pos, w_bits);
+        store_elem(orow, e, w_bits, x);
+      }
+    }
+  }
+  return status;
+}

@@ -1,0 +1,84 @@
+/*
+ * Plain single-threaded CPU oracle for Invariant Bit Packing (IBP).
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check of the package
+ * entry file and the CPU-baseline leg of the benchmark may load this library.
+ * The GPU codec never links, calls or includes anything from this directory,
+ * and this directory includes nothing from the GPU codec.
+ *
+ * Source of the method: "Reducing the GPU Memory Bottleneck with Lossless
+ * Compression for ML -- Extended" (Kamath, Krishnamurthy, Canini, Peter),
+ * technical summary, sections "Core algorithm" (preprocessing / compression /
+ * decompression) and "System integration" (PCIe transfer compression with
+ * fixed-size buffers and a GPU-resident bitmask).
+ *
+ * Every routine works on bit patterns only: elements are w-bit little-endian
+ * words (w = 32 for FP32, 16 for FP16/BF16); no floating-point value is ever
+ * interpreted, so +-0, denormals, Inf and NaN payloads are ordinary words.
+ *
+ * Stream format (the pages leave it open; the readings are listed in the design
+ * notes and repeated in the .cpp):
+ *   - a row of L elements is cut into nb = L/B blocks of B elements;
+ *   - participation bit p_b = 1 iff every element x of block b satisfies
+ *     (x & mask) == bitval;
+ *   - the row's bit stream is: nb participation bits (bit b = p_b), then for each
+ *     block in order either B fields of m = w - popcount(mask) bits (the element's
+ *     non-invariant bits in ascending position order) when p_b = 1, or B raw
+ *     w-bit words when p_b = 0;
+ *   - stream bit i is bit (i mod 32) of little-endian 32-bit word i/32;
+ *   - the row is stored compressed iff 4*ceil(bits/32) < L*w/8; then its slot
+ *     holds the stream (zero padded to the end of the last used word) and row
+ *     bit r of the bitmask is 1; otherwise the slot holds the raw row and the
+ *     bitmask bit is 0.
+ */
+#ifndef IBP_ORACLE_H
+#define IBP_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes of the oracle (its own numbering) */
+#define IBPO_OK 0
+#define IBPO_BAD_ARG (-1)
+#define IBPO_BAD_INDEX (-5)
+#define IBPO_CORRUPT (-6)
+
+/* Metadata (technical summary, core algorithm: preprocessing).
+ * elems: n_elems little-endian words of w_bits (16 or 32) bits.
+ * For each bit position j < w: c1 = number of elements whose bit j is 1,
+ * c0 = n_elems - c1; the majority value v = (c1 > c0); bit j is invariant iff
+ * (double)count_of_v >= T * (double)n_elems. Writes mask (invariant positions)
+ * and bitval (their values; zero outside mask). Returns IBPO_OK or IBPO_BAD_ARG. */
+int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, double T,
+                    uint32_t *mask_out, uint32_t *bitval_out);
+
+/* Slot size for a row: raw bytes L*w/8 rounded up to a multiple of 16. */
+int64_t ibpo_slot_bytes(int64_t row_elems, int w_bits);
+
+/* Compression (technical summary, core algorithm: compression; system
+ * integration: fixed-size buffers + bitmask). rows: n_rows x row_elems words.
+ * slots: n_rows x slot_bytes bytes (every byte of a used slot prefix is written;
+ * for compressed rows bytes past the last used word are left untouched).
+ * bitmask: ceil(n_rows/32) words, fully rewritten (bits past n_rows = 0).
+ * row_bits (nullable): per-row sum over blocks of (1 + B*m) or (1 + B*w). */
+int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                  int64_t block_elems, uint32_t mask, uint32_t bitval, void *slots,
+                  int64_t slot_bytes, uint32_t *bitmask, uint32_t *row_bits);
+
+/* Decompress-gather (technical summary, core algorithm: decompression).
+ * out[i] = original row idx[i], for i < n_idx. An index outside [0, n_rows)
+ * leaves out[i] untouched and makes the call return IBPO_BAD_INDEX; a compressed
+ * slot whose participation bits describe a stream of at least the raw size leaves
+ * out[i] untouched and makes the call return IBPO_CORRUPT (first error wins). */
+int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                           int64_t row_elems, int w_bits, int64_t block_elems,
+                           const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
+                           const int64_t *idx, int64_t n_idx, void *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,284 @@
+"""Checks that pin the oracle to facts other than itself.
+
+Each check takes an ``oracle.Oracle`` instance and raises AssertionError on a
+mismatch, so the same checks run against the real oracle and against copies of it
+with a mistake planted on purpose (tests/test_oracle_pins.py).
+
+What pins what (method: "Reducing the GPU Memory Bottleneck with Lossless
+Compression for ML -- Extended", technical summary, core algorithm):
+  * hand-worked example (tests/golden/hand_example_fp16.txt): exact mask, bitval,
+    sizes, bitmask and stream words worked out by hand;
+  * brute-force meta: per-bit counts taken with numpy.unpackbits over every input
+    of a small alphabet, against the preprocessing rule (majority value held by at
+    least a fraction T of the sample);
+  * closed forms of the preprocessing rule: T = 1 gives mask = ~(OR ^ AND),
+    bitval = AND & mask; identical elements give a full mask; a tie picks 0;
+  * the size formula sum_b (1 + B*(w - popcount(mask))) for matching blocks and
+    (1 + B*w) otherwise, with matches found by a vectorised numpy comparison, and
+    the store-compressed rule 4*ceil(bits/32) < raw bytes;
+  * the stream layout rebuilt as a Python string of '0'/'1' characters;
+  * lossless round trip (the decoded row equals the original word for word) on
+    +-0, denormals, +-Inf, NaN payloads and all-ones words;
+  * decode of the hand-worked stream words (typed in from the golden file, not
+    produced by the oracle).
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_hand_example():
+    rows, streams = [], []
+    d = {}
+    with open(os.path.join(GOLDEN, "hand_example_fp16.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "row":
+                rows.append([int(v, 16) for v in vals])
+            elif key == "stream":
+                streams.append([int(v, 16) for v in vals])
+            elif key in ("mask", "bitval", "bitmask"):
+                d[key] = int(vals[0], 16)
+            elif key == "row_bits":
+                d[key] = [int(v) for v in vals]
+            elif key == "T":
+                d[key] = float(vals[0])
+            elif key == "block":
+                d[key] = int(vals[0])
+    d["rows"] = np.array(rows, dtype=np.uint16)
+    d["streams"] = streams
+    return d
+
+
+def wmask(w):
+    return (1 << w) - 1
+
+
+def bits_of(words: np.ndarray) -> np.ndarray:
+    """[..., w] array of bits (bit j of each little-endian word) via unpackbits."""
+    a = np.ascontiguousarray(words)
+    w = 8 * a.dtype.itemsize
+    b = np.unpackbits(a.view(np.uint8).reshape(a.shape + (w // 8,)), axis=-1, bitorder="little")
+    return b.reshape(a.shape + (w,))
+
+
+def brute_meta(words: np.ndarray, T: float):
+    flat = np.ascontiguousarray(words).reshape(-1)
+    w = 8 * flat.dtype.itemsize
+    n = flat.size
+    ones = bits_of(flat).sum(axis=0).astype(np.int64)
+    mask = bitval = 0
+    for j in range(w):
+        c1 = int(ones[j])
+        c0 = n - c1
+        v = 1 if c1 > c0 else 0
+        if float(c1 if v else c0) >= T * float(n):
+            mask |= 1 << j
+            bitval |= v << j
+    return mask, bitval
+
+
+def check_hand_example(o):
+    d = load_hand_example()
+    mask, bitval = o.build_meta(d["rows"], d["T"])
+    assert (mask, bitval) == (d["mask"], d["bitval"]), (hex(mask), hex(bitval))
+    slots, bitmask, row_bits = o.compress(d["rows"], d["block"], mask, bitval)
+    assert list(row_bits) == d["row_bits"], list(row_bits)
+    assert int(bitmask[0]) == d["bitmask"], hex(int(bitmask[0]))
+    for r, words in enumerate(d["streams"]):
+        got = slots[r, : 4 * len(words)].view("<u4").tolist()
+        assert got == words, (r, [hex(x) for x in got])
+
+
+def check_hand_decode(o):
+    """Decode slots typed in from the golden file (not produced by the oracle)."""
+    d = load_hand_example()
+    n, L = d["rows"].shape
+    slots = np.zeros((n, 16), dtype=np.uint8)
+    for r, words in enumerate(d["streams"]):
+        slots[r, : 4 * len(words)] = np.array(words, dtype="<u4").view(np.uint8)
+    bitmask = np.array([d["bitmask"]], dtype=np.uint32)
+    idx = np.array([1, 0, 1], dtype=np.int64)
+    out, rc = o.decompress_gather(slots, n, L, np.uint16, d["block"], bitmask, d["mask"],
+                                  d["bitval"], idx)
+    assert rc == 0
+    assert np.array_equal(out, d["rows"][idx])
+
+
+FP16_ALPHABET = [0x0000, 0x8000, 0x3C00, 0xFFFF, 0x0001, 0x7C00, 0x7E01, 0x03FF]
+
+
+def check_meta_exhaustive(o):
+    """Every 2x2 FP16 input over an 8-word alphabet (+-0, 1.0, all-ones, smallest
+    denormal, +Inf, a NaN with payload, largest denormal), at several T."""
+    combos = np.array(list(itertools.product(FP16_ALPHABET, repeat=4)), dtype=np.uint16)
+    for T in (0.0, 0.5, 0.75, 0.9, 1.0):
+        for c in combos:
+            got = o.build_meta(c.reshape(2, 2), T)
+            exp = brute_meta(c, T)
+            assert got == exp, (c, T, got, exp)
+
+
+def check_meta_closed_forms(o):
+    g = np.random.default_rng(12345)
+    for dt, w in ((np.uint32, 32), (np.uint16, 16)):
+        for trial in range(20):
+            n = int(g.integers(1, 200))
+            x = g.integers(0, 1 << w, size=n, dtype=np.uint64).astype(dt)
+            # force some bits constant so T = 1 has something to find
+            keep = int(g.integers(0, 1 << w))
+            fixed = int(g.integers(0, 1 << w))
+            x = ((x.astype(np.uint64) & ~np.uint64(keep)) | np.uint64(fixed & keep)).astype(dt)
+            OR = int(np.bitwise_or.reduce(x.astype(np.uint64)))
+            AND = int(np.bitwise_and.reduce(x.astype(np.uint64)))
+            mask, bitval = o.build_meta(x, 1.0)
+            exp_mask = ~(OR ^ AND) & wmask(w)
+            assert mask == exp_mask, (hex(mask), hex(exp_mask))
+            assert bitval == AND & exp_mask
+            # identical elements: every position is invariant
+            y = np.full(n, x[0], dtype=dt)
+            assert o.build_meta(y, float(g.random())) == (wmask(w), int(x[0]))
+        # a tie (one element with all bits 0, one with all bits 1) picks value 0
+        t = np.array([0, wmask(w)], dtype=dt)
+        assert o.build_meta(t, 0.5) == (wmask(w), 0)
+        assert o.build_meta(t, 0.51) == (0, 0)
+    # threshold boundary: 9 of 10 elements share bit 0 -> invariant at T = 0.9,
+    # 8 of 10 -> not
+    a = np.array([1] * 9 + [0], dtype=np.uint32)
+    m, b = o.build_meta(a, 0.9)
+    assert m & 1 and b & 1
+    a = np.array([1] * 8 + [0] * 2, dtype=np.uint32)
+    m, _ = o.build_meta(a, 0.9)
+    assert not (m & 1)
+
+
+def block_matches(rows: np.ndarray, B: int, mask: int, bitval: int) -> np.ndarray:
+    n, L = rows.shape
+    wide = rows.astype(np.uint64)
+    ok = (wide & np.uint64(mask)) == np.uint64(bitval)
+    return ok.reshape(n, L // B, B).all(axis=2)
+
+
+def check_size_formula(o):
+    g = np.random.default_rng(777)
+    cases = [(np.uint32, 32, 32, 128), (np.uint32, 32, 64, 256), (np.uint16, 16, 64, 256),
+             (np.uint16, 16, 32, 96), (np.uint32, 32, 4, 12), (np.uint16, 16, 1, 5)]
+    for dt, w, B, L in cases:
+        n = 64
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        # high bits mostly constant so that most blocks match
+        hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 2)) - 1))
+        flip = g.random(size=(n, L)) < 0.01
+        x = np.where(flip, base, (base & ~hi) | (np.uint64(0x5A5A5A5A) & hi)).astype(dt)
+        mask, bitval = o.build_meta(x, 0.9)
+        slots, bitmask, row_bits = o.compress(x, B, mask, bitval)
+        m = w - bin(mask).count("1")
+        match = block_matches(x, B, mask, bitval)
+        exp_bits = (1 + np.where(match, B * m, B * w)).sum(axis=1)
+        assert np.array_equal(row_bits.astype(np.int64), exp_bits)
+        raw = L * w // 8
+        exp_flag = 4 * ((exp_bits + 31) // 32) < raw
+        got_flag = ((bitmask[np.arange(n) // 32] >> (np.arange(n) % 32).astype(np.uint32)) & 1)
+        assert np.array_equal(got_flag.astype(bool), exp_flag)
+    # equality case of the store rule: FP32, B = L = 32, only the sign bit
+    # invariant -> 1 + 32*31 = 993 bits = 32 words = 128 B = raw -> stored raw
+    x = g.integers(0, 1 << 31, size=(8, 32), dtype=np.uint64).astype(np.uint32)
+    x[:, 0] = 0x7FFFFFFF
+    x[:, 1] = 0x00000000
+    mask, bitval = o.build_meta(x, 1.0)
+    assert mask == 0x80000000 and bitval == 0
+    slots, bitmask, row_bits = o.compress(x, 32, mask, bitval)
+    assert np.all(row_bits == 993)
+    assert int(bitmask[0]) == 0
+    assert np.array_equal(slots[:, :128].view("<u4"), x)
+
+
+def expected_slot_bits(row: np.ndarray, B: int, mask: int, bitval: int) -> str:
+    """The row's stream as a string of '0'/'1' characters, stream bit i at index i."""
+    w = 8 * row.dtype.itemsize
+    L = row.size
+    kept = [j for j in range(w) if not (mask >> j) & 1]
+    blocks = [row[b * B:(b + 1) * B] for b in range(L // B)]
+    parts = []
+    flags = [all((int(x) & mask) == bitval for x in blk) for blk in blocks]
+    parts.append("".join("1" if f else "0" for f in flags))
+    for f, blk in zip(flags, blocks):
+        for x in blk:
+            x = int(x)
+            if f:
+                parts.append("".join(str((x >> j) & 1) for j in kept))
+            else:
+                parts.append("".join(str((x >> j) & 1) for j in range(w)))
+    return "".join(parts)
+
+
+def words_from_bitstring(s: str) -> list[int]:
+    s = s + "0" * (-len(s) % 32)
+    return [int(s[i:i + 32][::-1], 2) for i in range(0, len(s), 32)]
+
+
+def check_stream_layout(o):
+    g = np.random.default_rng(4242)
+    for dt, w, B, L in ((np.uint16, 16, 4, 16), (np.uint32, 32, 8, 24), (np.uint16, 16, 2, 6),
+                        (np.uint32, 32, 32, 64)):
+        n = 12
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        keep_hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 2 - 3)) - 1))
+        flip = g.random(size=(n, L)) < 0.05
+        x = np.where(flip, base, (base & ~keep_hi) | (np.uint64(0x3C3C3C3C) & keep_hi)).astype(dt)
+        mask, bitval = o.build_meta(x, 0.8)
+        slots, bitmask, row_bits = o.compress(x, B, mask, bitval)
+        raw = L * w // 8
+        for r in range(n):
+            s = expected_slot_bits(x[r], B, mask, bitval)
+            assert len(s) == int(row_bits[r])
+            compressed = (int(bitmask[r // 32]) >> (r % 32)) & 1
+            if compressed:
+                words = words_from_bitstring(s)
+                assert slots[r, : 4 * len(words)].view("<u4").tolist() == words
+            else:
+                assert bytes(slots[r, :raw]) == x[r].tobytes()
+
+
+def special_words(w: int) -> list[int]:
+    if w == 32:
+        return [0x00000000, 0x80000000, 0x00000001, 0x007FFFFF, 0x80000001, 0x7F800000,
+                0xFF800000, 0x7FC00000, 0x7FC12345, 0x7F800001, 0xFFFFFFFF, 0x3F800000,
+                0xBF800000, 0x00800000]
+    return [0x0000, 0x8000, 0x0001, 0x03FF, 0x8001, 0x7C00, 0xFC00, 0x7E00, 0x7E5A, 0x7C01,
+            0xFFFF, 0x3C00, 0xBC00, 0x7F80, 0xFF80, 0x7FC1, 0x0400]
+
+
+def check_round_trip_specials(o):
+    g = np.random.default_rng(99)
+    for dt, w in ((np.uint32, 32), (np.uint16, 16)):
+        sp = np.array(special_words(w), dtype=dt)
+        for B in (1, 2, 4, 8, 32):
+            L = B * 4
+            n = 40
+            x = sp[g.integers(0, sp.size, size=(n, L))]
+            # rows that are mostly one special word, so that blocks also match
+            x[: n // 2] = np.where(g.random(size=(n // 2, L)) < 0.9, sp[g.integers(0, sp.size)],
+                                   x[: n // 2])
+            for T in (0.0, 0.6, 0.9, 1.0):
+                mask, bitval = o.build_meta(x, T)
+                for mk, bv in ((mask, bitval), (0, 0), (wmask(w), int(x[0, 0])),
+                               (0x7F80 if w == 16 else 0x7F800000, 0)):
+                    slots, bitmask, _ = o.compress(x, B, mk, bv & mk)
+                    idx = g.integers(0, n, size=64)
+                    out, rc = o.decompress_gather(slots, n, L, dt, B, bitmask, mk, bv & mk, idx)
+                    assert rc == 0
+                    assert np.array_equal(out, x[idx]), (w, B, T, hex(mk))
+
+
+ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
+              check_meta_closed_forms, check_size_formula, check_stream_layout,
+              check_round_trip_specials]

@@ -1,0 +1,108 @@
+"""The oracle against what the method and mathematics fix (no GPU needed)."""
+import numpy as np
+import pytest
+
+import ibp_inputs as gen
+import oracle
+import pins
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.default()
+
+
+@pytest.mark.parametrize("check", pins.ALL_CHECKS, ids=lambda c: c.__name__)
+def test_pin(o, check):
+    check(o)
+
+
+def test_brute_meta_on_workload_prefixes(o):
+    cases = [(gen.tiny_fp32(512), 0.9), (gen.gnn_dense(300), 0.9), (gen.gnn_sparse(40), 0.9),
+             (gen.dlrm_table(3, 300), 0.95), (gen.llm_weight(0, "q", 16), 0.9),
+             (gen.llm_kv(1, 1, n_rows=8), 0.9)]
+    for x, T in cases:
+        words = x.view(np.uint32) if x.dtype == np.float32 else x
+        assert o.build_meta(words, T) == pins.brute_meta(words, T)
+
+
+@pytest.mark.parametrize("name,B,T", [("tiny", 32, 0.9), ("dense", 32, 0.9), ("sparse", 32, 0.9),
+                                      ("dlrm", 32, 0.95), ("w_down", 64, 0.9), ("kv", 64, 0.9)])
+def test_round_trip_workload_prefixes(o, name, B, T):
+    x = {"tiny": lambda: gen.tiny_fp32(1024), "dense": lambda: gen.gnn_dense(1000),
+         "sparse": lambda: gen.gnn_sparse(200), "dlrm": lambda: gen.dlrm_table(0, 1000),
+         "w_down": lambda: gen.llm_weight(2, "down", 24),
+         "kv": lambda: gen.llm_kv(0, 0, n_rows=64)}[name]()
+    words = x.view(np.uint32) if x.dtype == np.float32 else x
+    mask, bitval = o.build_meta(words, T)
+    slots, bitmask, row_bits = o.compress(words, B, mask, bitval)
+    n, L = words.shape
+    g = np.random.default_rng(5)
+    idx = np.concatenate([g.integers(0, n, size=300), [0, n - 1, n - 1, 0]]).astype(np.int64)
+    out, rc = o.decompress_gather(slots, n, L, words.dtype, B, bitmask, mask, bitval, idx)
+    assert rc == 0
+    assert np.array_equal(out, words[idx])
+    match = pins.block_matches(words, B, mask, bitval)
+    m = 8 * words.dtype.itemsize - bin(mask).count("1")
+    exp = (1 + np.where(match, B * m, B * 8 * words.dtype.itemsize)).sum(axis=1)
+    assert np.array_equal(row_bits.astype(np.int64), exp)
+
+
+def test_error_paths(o):
+    x = gen.tiny_fp32(64).view(np.uint32)
+    mask, bitval = o.build_meta(x, 0.9)
+    slots, bitmask, _ = o.compress(x, 32, mask, bitval)
+    n, L = x.shape
+    sentinel = np.full((3, L), 0xDEADBEEF, dtype=np.uint32)
+    out, rc = o.decompress_gather(slots, n, L, np.uint32, 32, bitmask, mask, bitval,
+                                  np.array([1, n, -1], dtype=np.int64), out=sentinel.copy())
+    assert rc == oracle.BAD_INDEX
+    assert np.array_equal(out[0], x[1])
+    assert np.all(out[1:] == 0xDEADBEEF)
+    # corrupt a compressed row: participation bits all 0 describe a raw-sized stream
+    r = next(r for r in range(n) if (bitmask[r // 32] >> (r % 32)) & 1)
+    bad = slots.copy()
+    bad[r, 0] &= 0xF0
+    out, rc = o.decompress_gather(bad, n, L, np.uint32, 32, bitmask, mask, bitval,
+                                  np.array([r], dtype=np.int64), out=sentinel[:1].copy())
+    assert rc == oracle.CORRUPT
+    assert np.all(out == 0xDEADBEEF)
+    # empty gather is a no-op
+    out, rc = o.decompress_gather(slots, n, L, np.uint32, 32, bitmask, mask, bitval,
+                                  np.zeros(0, dtype=np.int64))
+    assert rc == 0 and out.shape == (0, L)
+
+
+# Mistakes planted in a copy of the oracle source; each must break at least one pin.
+PLANTED = [
+    ("threshold > instead of >=", "(double)cv >= T * (double)n_elems",
+     "(double)cv > T * (double)n_elems"),
+    ("tie picks 1", "int v = c1 > c0 ? 1 : 0;", "int v = c1 >= c0 ? 1 : 0;"),
+    ("participation bit dropped from size", "bits += 1 + block_elems * (match ? m : w_bits);",
+     "bits += block_elems * (match ? m : w_bits);"),
+    ("kept bits taken from the mask", "    if (!bit_of(mask, j)) {\n      field",
+     "    if (bit_of(mask, j)) {\n      field"),
+    ("MSB-first bit order", "  int in_word = (int)(pos % 32);\n  int64_t byte = word * 4 + in_word / 8;\n  int in_byte = in_word % 8;\n  if (bit)",
+     "  int in_word = 31 - (int)(pos % 32);\n  int64_t byte = word * 4 + in_word / 8;\n  int in_byte = in_word % 8;\n  if (bit)"),
+    ("store rule <= instead of <", "int compressed = 4 * stored_words < raw_bytes;",
+     "int compressed = 4 * stored_words <= raw_bytes;"),
+    ("payload read starts one bit late", "int64_t pos = nb; /* first payload bit */",
+     "int64_t pos = nb + 1; /* first payload bit */"),
+    ("bitval not reinserted", "x |= (uint32_t)bit_of(bitval, j) << j;", "x |= 0;"),
+    ("bitval stores the minority value", "bitval |= (uint32_t)v << j;",
+     "bitval |= (uint32_t)(1 - v) << j;"),
+]
+
+
+@pytest.mark.parametrize("label,old,new", PLANTED, ids=[p[0] for p in PLANTED])
+def test_planted_mistake_is_caught(tmp_path, label, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation anchor not found once: {label}"
+    bad = oracle.compile_variant(src.replace(old, new), str(tmp_path))
+    failures = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(bad)
+        except AssertionError:
+            failures.append(check.__name__)
+    assert failures, f"planted mistake '{label}' passed every pin"
