@@ -1,0 +1,151 @@
+/*
+ * ibp.h -- C ABI of the GB300 (sm_103a) Invariant Bit Packing codec.
+ *
+ * Method: "Reducing the GPU Memory Bottleneck with Lossless Compression for ML --
+ * Extended" (Kamath, Krishnamurthy, Canini, Peter), technical summary:
+ *   - "Core algorithm", preprocessing: find the bit positions of the element word
+ *     that hold one value in at least a fraction T of a sample, keep them as a
+ *     fixed-size mask + bitval in GPU memory, reuse them for the whole dataset;
+ *   - "Core algorithm", compression: per fixed-size block, test the invariant
+ *     positions against bitval; on a match strip them and close the gaps; mark
+ *     each block with a participation bit; run on the GPU over zero-copy memory;
+ *   - "Core algorithm", decompression: a warp stages a contiguous compressed
+ *     segment in shared memory, prefix-scans block sizes with warp primitives to
+ *     find each block's bit offset, and reinserts the invariant bits;
+ *   - "System integration", PCIe transfer compression: one fixed-size buffer per
+ *     tensor of which only the compressed part is read, plus a GPU-resident
+ *     bitmask of which tensors are compressed.
+ *
+ * Conventions shared by every call
+ *   - A "row" is the unit stored in one slot (a feature vector, an embedding
+ *     row, a weight row, a token's K or V). Rows are row_elems little-endian
+ *     element words of w bits: w = 32 (IBP_FP32) or 16 (IBP_FP16, IBP_BF16).
+ *     Only bit patterns are handled: +-0, denormals, Inf and NaN payloads are
+ *     ordinary words and always round-trip exactly.
+ *   - block_elems B must be 32 or 64 and divide row_elems; 1 <= row_elems <= 2^20.
+ *   - Slot r of a store starts at slots + r*slot_bytes; slot_bytes is at least
+ *     ibp_slot_bytes() (the raw row rounded up to 16 bytes) and a multiple of 16.
+ *   - Stream format of a compressed row (bit i = bit i%32 of little-endian 32-bit
+ *     word i/32): nb = row_elems/B participation bits, then each block in order,
+ *     either B fields of m = w - popcount(mask) bits (the element's non-invariant
+ *     bits, ascending) or B raw words. A row is stored compressed iff
+ *     4*ceil(bits/32) < raw bytes, where bits = sum_b (1 + B*m) or (1 + B*w).
+ *   - Bitmask: bit r of a store is bit r%32 of 32-bit word r/32.
+ *   - Ownership: the caller owns and allocates every buffer; the library
+ *     allocates nothing, keeps no per-call state and never synchronises a stream
+ *     except where stated. Pointers named d_* must be device memory. rows and
+ *     slots may be device memory or page-locked host memory registered with CUDA
+ *     (read and written zero-copy by the kernels); pageable host memory is
+ *     rejected. rows, slots and out must be 16-byte aligned.
+ *   - Every compute call is asynchronous on stream s (0 = legacy default stream)
+ *     and may be captured in a CUDA graph once the argument checks pass.
+ *
+ * Return codes: IBP_OK (0) or a negative code found before anything is launched.
+ * Errors a kernel detects are written to *d_status (when it is non-null) with an
+ * atomic compare-and-swap from 0, so the first error wins; the caller zeroes
+ * *d_status before the call. No kernel traps, asserts or waits without bound.
+ */
+#ifndef IBP_H
+#define IBP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ibp_stream_t; /* same object as cudaStream_t */
+
+typedef enum { IBP_FP32 = 0, IBP_FP16 = 1, IBP_BF16 = 2 } ibp_dtype;
+
+enum {
+  IBP_OK = 0,
+  IBP_ERR_ARG = -1,         /* null/misaligned/pageable pointer, bad size, T outside [0,1] */
+  IBP_ERR_DTYPE = -2,       /* dtype not one of ibp_dtype */
+  IBP_ERR_UNSUPPORTED = -3, /* block size or row length the kernels do not handle */
+  IBP_ERR_CUDA = -4,        /* a CUDA call or launch failed */
+  IBP_ERR_INDEX = -5,       /* (device) gather index outside [0, n_rows) */
+  IBP_ERR_CORRUPT = -6,     /* (device) participation bits describe an impossible stream */
+  IBP_ERR_META = -7         /* (device) *d_meta disagrees with the dtype/block_elems passed */
+};
+
+/* Metadata: the fixed-size mask/bitval pair of the preprocessing stage.
+ * Plain data (16 bytes); the caller may copy or serialise it. mask has a 1 at
+ * every invariant bit position; bitval holds their values and is 0 elsewhere. */
+typedef struct {
+  uint32_t mask;
+  uint32_t bitval;
+  uint32_t dtype;       /* ibp_dtype */
+  uint32_t block_elems; /* B */
+} ibp_meta;
+
+/* Store statistics written by ibp_query. */
+typedef struct {
+  int64_t n_rows;
+  int64_t n_compressed; /* rows whose bitmask bit is 1 */
+  int64_t raw_bytes;    /* n_rows * row_elems * w/8 */
+  int64_t stored_bytes; /* sum over rows: 4*ceil(bits/32) if compressed, else raw row bytes */
+  int64_t total_bits;   /* sum over rows of the size formula, compressed or not */
+} ibp_stats;
+
+/* Human-readable name of a return/status code (static string). */
+const char *ibp_status_string(int code);
+
+/* Bytes of one slot: row_elems * w/8 rounded up to 16. */
+int ibp_slot_bytes(int64_t row_elems, int dtype, int64_t *slot_bytes);
+
+/* Bytes of device scratch ibp_build_meta needs (the per-bit-position counters). */
+int ibp_meta_scratch_bytes(size_t *bytes);
+
+/* Preprocessing ("Core algorithm", preprocessing).
+ * rows: n_rows x row_elems element words (device or registered host memory).
+ * For every bit position j < w, counts the sampled elements whose bit j is 1; j is
+ * invariant iff the majority value's count c satisfies (double)c >= T*(double)N in
+ * IEEE double (N = n_rows*row_elems; a tie counts as majority value 0).
+ * Writes *d_meta = {mask, bitval, dtype, block_elems}. d_scratch: device memory of
+ * ibp_meta_scratch_bytes(), overwritten (no initial contents needed). */
+int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtype, double T,
+                   uint32_t block_elems, ibp_meta *d_meta, void *d_scratch, ibp_stream_t s);
+
+/* Compression ("Core algorithm", compression; "System integration").
+ * Encodes rows [0, n_rows) into their slots with the mask/bitval in *d_meta, whose
+ * dtype and block_elems must equal the ones passed. Compressed rows hold their
+ * stream in the first 4*ceil(bits/32) bytes of the slot (the rest of the slot up
+ * to the next 16-byte boundary is written with zeros, later bytes are untouched);
+ * other rows hold their raw bytes. d_row_bitmask (ceil(n_rows/32) words) is fully
+ * rewritten, bits past n_rows set to 0. d_row_bits (nullable, n_rows words)
+ * receives each row's size-formula bit count. rows and slots must not overlap. */
+int ibp_compress(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                 uint32_t block_elems, const ibp_meta *d_meta, void *slots, int64_t slot_bytes,
+                 uint32_t *d_row_bitmask, uint32_t *d_row_bits, int32_t *d_status,
+                 ibp_stream_t s);
+
+/* Decompress-gather ("Core algorithm", decompression; "System integration").
+ * out[i] (row_elems words, device memory, rows packed back to back) receives the
+ * original row d_idx[i] for i < n_idx; indices may repeat. Only the used prefix of
+ * each slot is read. n_idx == 0 is a no-op. A row whose index is outside
+ * [0, n_rows) or whose participation bits describe a stream that would not have
+ * been stored compressed is skipped (out[i] untouched) and IBP_ERR_INDEX or
+ * IBP_ERR_CORRUPT is recorded in *d_status. */
+int ibp_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                          int64_t row_elems, int dtype, uint32_t block_elems,
+                          const uint32_t *d_row_bitmask, const ibp_meta *d_meta,
+                          const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
+                          ibp_stream_t s);
+
+/* Statistics of a store: reduces the bitmask and the per-row bit counts written
+ * by ibp_compress into *d_stats (device memory), asynchronously on s. */
+int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+              int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s);
+
+/* Measurement helper, not part of the codec: streams `bytes` (a multiple of 16)
+ * from src (device or registered host memory) with 16-byte loads across the whole
+ * GPU and writes one XOR checksum word to *d_sink, so a caller can time the plain
+ * read bandwidth of the memory the codec reads zero-copy. */
+int ibp_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, ibp_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,181 @@
+"""Python binding of the GB300 Invariant Bit Packing codec (``include/ibp.h``).
+
+Argument marshalling only: every step of the codec runs in the CUDA kernels of
+``_build/libibp_gb300.so``. Tensors are torch tensors used as plain memory
+(device memory, or page-locked host memory for rows and slots read or written
+zero-copy); calls are enqueued on the current CUDA stream unless one is given.
+There is no CPU fallback: importing works without the library, but every call
+raises if the shared library has not been built (``build_lib.build()``).
+
+Method: "Reducing the GPU Memory Bottleneck with Lossless Compression for ML --
+Extended", technical summary, "Core algorithm" and "System integration".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build_lib
+
+FP32, FP16, BF16 = 0, 1, 2
+OK = 0
+ERR_ARG, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_INDEX, ERR_CORRUPT, ERR_META = (
+    -1, -2, -3, -4, -5, -6, -7)
+
+_TORCH_DTYPES = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
+WIDTH = {FP32: 32, FP16: 16, BF16: 16}
+
+_lib = None
+
+
+class IBPError(RuntimeError):
+    def __init__(self, code: int, call: str):
+        self.code = code
+        super().__init__(f"{call}: {status_string(code)} ({code})")
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int64), ("n_compressed", ctypes.c_int64),
+                ("raw_bytes", ctypes.c_int64), ("stored_bytes", ctypes.c_int64),
+                ("total_bits", ctypes.c_int64)]
+
+
+SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp_build_meta",
+           "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read")
+
+
+def library_path() -> str:
+    return build_lib.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load the built library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = build_lib.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"IBP CUDA library not built ({path}); run "
+                           "lossless_bit_level_gb300.build_lib.build() first")
+    lib = ctypes.CDLL(path)
+    i64, i32, u32, dbl, vp = (ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_double,
+                              ctypes.c_void_p)
+    lib.ibp_status_string.argtypes = [i32]
+    lib.ibp_status_string.restype = ctypes.c_char_p
+    lib.ibp_slot_bytes.argtypes = [i64, i32, ctypes.POINTER(i64)]
+    lib.ibp_meta_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ibp_build_meta.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp]
+    lib.ibp_compress.argtypes = [vp, i64, i64, i32, u32, vp, vp, i64, vp, vp, vp, vp]
+    lib.ibp_decompress_gather.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
+    lib.ibp_query.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.ibp_probe_read.argtypes = [vp, i64, vp, vp]
+    for name in SYMBOLS[1:]:
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().ibp_status_string(int(code)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(rc: int, call: str) -> None:
+    if rc != OK:
+        raise IBPError(rc, call)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dtype_code(t: torch.Tensor, dtype: int | None = None) -> int:
+    if dtype is not None:
+        return int(dtype)
+    if t.dtype not in _TORCH_DTYPES:
+        raise ValueError(f"pass dtype= for element tensors of {t.dtype}")
+    return _TORCH_DTYPES[t.dtype]
+
+
+def slot_bytes(row_elems: int, dtype: int) -> int:
+    out = ctypes.c_int64(0)
+    _check(load().ibp_slot_bytes(int(row_elems), int(dtype), ctypes.byref(out)), "ibp_slot_bytes")
+    return out.value
+
+
+def meta_scratch_bytes() -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().ibp_meta_scratch_bytes(ctypes.byref(out)), "ibp_meta_scratch_bytes")
+    return out.value
+
+
+def _rows_shape(rows: torch.Tensor) -> tuple[int, int]:
+    if rows.dim() != 2 or not rows.is_contiguous():
+        raise ValueError("rows must be a contiguous 2-D tensor [n_rows, row_elems]")
+    return rows.shape[0], rows.shape[1]
+
+
+def build_meta(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Tensor,
+               scratch: torch.Tensor, dtype: int | None = None, stream=None) -> None:
+    """ibp_build_meta: mask/bitval of ``rows`` into ``meta`` (16 device bytes)."""
+    n, L = _rows_shape(rows)
+    _check(load().ibp_build_meta(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
+                                 int(block_elems), _ptr(meta), _ptr(scratch), _stream(stream)),
+           "ibp_build_meta")
+
+
+def compress(rows: torch.Tensor, block_elems: int, meta: torch.Tensor, slots: torch.Tensor,
+             bitmask: torch.Tensor, row_bits: torch.Tensor | None = None,
+             status: torch.Tensor | None = None, dtype: int | None = None,
+             stream=None) -> None:
+    """ibp_compress: encode ``rows`` into ``slots`` ([n_rows, slot_bytes] bytes)."""
+    n, L = _rows_shape(rows)
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(n, 1)
+    _check(load().ibp_compress(_ptr(rows), n, L, dtype_code(rows, dtype), int(block_elems),
+                               _ptr(meta), _ptr(slots), sb, _ptr(bitmask), _ptr(row_bits),
+                               _ptr(status), _stream(stream)), "ibp_compress")
+
+
+def decompress_gather(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
+                      block_elems: int, bitmask: torch.Tensor, meta: torch.Tensor,
+                      idx: torch.Tensor, out: torch.Tensor, status: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """ibp_decompress_gather: rows ``idx`` rebuilt into ``out`` [n_idx, row_elems]."""
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(int(n_rows), 1)
+    if idx.dtype != torch.int64:
+        raise ValueError("idx must be int64")
+    _check(load().ibp_decompress_gather(_ptr(slots), sb, int(n_rows), int(row_elems), int(dtype),
+                                        int(block_elems), _ptr(bitmask), _ptr(meta), _ptr(idx),
+                                        idx.numel(), _ptr(out), _ptr(status), _stream(stream)),
+           "ibp_decompress_gather")
+
+
+def query(bitmask: torch.Tensor, row_bits: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
+          stats: torch.Tensor, stream=None) -> None:
+    """ibp_query: store statistics into ``stats`` (40 device bytes, see Stats)."""
+    _check(load().ibp_query(_ptr(bitmask), _ptr(row_bits), int(n_rows), int(row_elems),
+                            int(dtype), _ptr(stats), _stream(stream)), "ibp_query")
+
+
+def read_stats(stats: torch.Tensor) -> Stats:
+    host = stats.detach().to("cpu").contiguous().view(torch.uint8).numpy().tobytes()
+    return Stats.from_buffer_copy(host[:ctypes.sizeof(Stats)])
+
+
+def probe_read(src: torch.Tensor, sink: torch.Tensor, nbytes: int | None = None,
+               stream=None) -> None:
+    """ibp_probe_read: stream ``nbytes`` of ``src`` through the GPU (bandwidth probe)."""
+    n = src.numel() * src.element_size() if nbytes is None else int(nbytes)
+    _check(load().ibp_probe_read(_ptr(src), n, _ptr(sink), _stream(stream)), "ibp_probe_read")

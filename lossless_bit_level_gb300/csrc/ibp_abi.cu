@@ -1,0 +1,255 @@
+// C ABI of the IBP codec: argument checks, geometry, launches (declared in include/ibp.h).
+// Also holds the two small auxiliary kernels: store statistics and the read probe.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "ibp_device.cuh"
+#include "ibp_internal.h"
+
+namespace ibp {
+
+namespace {
+
+constexpr int64_t MAX_ROW_ELEMS = int64_t(1) << 20;
+
+enum class Where { device_only, device_or_host };
+
+// Device memory, managed memory, or (when allowed) page-locked host memory that
+// CUDA has mapped; anything else is rejected before a kernel could fault on it.
+bool pointer_ok(const void *p, Where where, size_t align) {
+  if (!p || (reinterpret_cast<uintptr_t>(p) % align) != 0) return false;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (attr.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return where == Where::device_or_host && attr.devicePointer == p;
+    default: return false;
+  }
+}
+
+bool dtype_ok(int dtype) { return dtype == IBP_FP32 || dtype == IBP_FP16 || dtype == IBP_BF16; }
+
+int make_geom(int64_t row_elems, int dtype, uint32_t block_elems, RowGeom *g) {
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (row_elems <= 0 || block_elems == 0) return IBP_ERR_ARG;
+  if (row_elems % block_elems != 0) return IBP_ERR_ARG;
+  if (block_elems != 32 && block_elems != 64) return IBP_ERR_UNSUPPORTED;
+  if (row_elems > MAX_ROW_ELEMS) return IBP_ERR_UNSUPPORTED;
+  g->w = width_of(dtype);
+  g->epw = 32 / g->w;
+  g->B = (int)block_elems;
+  g->lwb = (int)block_elems * g->w / 32;
+  g->nb = (int)(row_elems / block_elems);
+  g->raw_words = (int)(row_elems * g->w / 32);
+  g->row_elems = row_elems;
+  g->raw_bytes = row_elems * g->w / 8;
+  return IBP_OK;
+}
+
+int64_t slot_bytes_of(const RowGeom &g) { return (g.raw_bytes + 15) / 16 * 16; }
+
+__global__ void query_kernel(const uint32_t *bitmask, const uint32_t *row_bits, int64_t n_rows,
+                             int64_t raw_bytes, ibp_stats *stats) {
+  unsigned long long comp = 0, stored = 0, bits = 0;
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n_rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    const bool c = (bitmask[r >> 5] >> (r & 31)) & 1u;
+    const uint32_t b = row_bits[r];
+    comp += c;
+    stored += c ? 4ull * ((b + 31u) >> 5) : (unsigned long long)raw_bytes;
+    bits += b;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    comp += __shfl_xor_sync(FULL, comp, o);
+    stored += __shfl_xor_sync(FULL, stored, o);
+    bits += __shfl_xor_sync(FULL, bits, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(reinterpret_cast<unsigned long long *>(&stats->n_compressed), comp);
+    atomicAdd(reinterpret_cast<unsigned long long *>(&stats->stored_bytes), stored);
+    atomicAdd(reinterpret_cast<unsigned long long *>(&stats->total_bits), bits);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    stats->n_rows = n_rows;
+    stats->raw_bytes = n_rows * raw_bytes;
+  }
+}
+
+__global__ void probe_read_kernel(const uint4 *__restrict__ src, int64_t nvec,
+                                  unsigned long long *sink) {
+  uint32_t acc = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; k + 3 * stride < nvec; k += 4 * stride) {
+    const uint4 a = src[k], b = src[k + stride], c = src[k + 2 * stride], d = src[k + 3 * stride];
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^
+           d.z ^ d.w;
+  }
+  for (; k < nvec; k += stride) {
+    const uint4 a = src[k];
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(FULL, acc, o);
+  if ((threadIdx.x & 31) == 0 && acc) atomicXor(sink, (unsigned long long)acc);
+}
+
+}  // namespace
+
+int device_info(DeviceInfo *out) {
+  static DeviceInfo cache[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IBP_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && have[dev]) {
+    *out = cache[dev];
+    return IBP_OK;
+  }
+  DeviceInfo d;
+  d.device = dev;
+  if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess)
+    return IBP_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = d;
+  return IBP_OK;
+}
+
+int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                 int64_t raw_bytes, ibp_stats *d_stats, cudaStream_t s) {
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  if (cudaMemsetAsync(d_stats, 0, sizeof(ibp_stats), s) != cudaSuccess) return IBP_ERR_CUDA;
+  const int64_t want = std::max<int64_t>(1, (n_rows + 255) / 256);
+  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * 4);
+  query_kernel<<<grid, 256, 0, s>>>(d_bitmask, d_row_bits, n_rows, raw_bytes, d_stats);
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+}
+
+int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s) {
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  if (cudaMemsetAsync(d_sink, 0, sizeof(uint64_t), s) != cudaSuccess) return IBP_ERR_CUDA;
+  const int64_t nvec = bytes / 16;
+  if (nvec == 0) return IBP_OK;
+  const int grid = (int)std::min<int64_t>((nvec + 255) / 256, (int64_t)dev.sm_count * 8);
+  probe_read_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), nvec,
+                                         reinterpret_cast<unsigned long long *>(d_sink));
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+}
+
+}  // namespace ibp
+
+using namespace ibp;
+
+extern "C" {
+
+const char *ibp_status_string(int code) {
+  switch (code) {
+    case IBP_OK: return "ok";
+    case IBP_ERR_ARG: return "invalid argument";
+    case IBP_ERR_DTYPE: return "unknown dtype";
+    case IBP_ERR_UNSUPPORTED: return "unsupported block size or row length";
+    case IBP_ERR_CUDA: return "CUDA call or launch failed";
+    case IBP_ERR_INDEX: return "gather index out of range";
+    case IBP_ERR_CORRUPT: return "corrupt slot header";
+    case IBP_ERR_META: return "metadata does not match dtype/block size";
+    default: return "unknown status";
+  }
+}
+
+int ibp_slot_bytes(int64_t row_elems, int dtype, int64_t *slot_bytes) {
+  if (!slot_bytes) return IBP_ERR_ARG;
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (row_elems <= 0) return IBP_ERR_ARG;
+  *slot_bytes = (row_elems * width_of(dtype) / 8 + 15) / 16 * 16;
+  return IBP_OK;
+}
+
+int ibp_meta_scratch_bytes(size_t *bytes) {
+  if (!bytes) return IBP_ERR_ARG;
+  *bytes = 32 * sizeof(unsigned long long);
+  return IBP_OK;
+}
+
+int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtype, double T,
+                   uint32_t block_elems, ibp_meta *d_meta, void *d_scratch, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_rows <= 0 || !(T >= 0.0 && T <= 1.0)) return IBP_ERR_ARG;
+  if (!pointer_ok(rows, Where::device_or_host, 16) || !pointer_ok(d_meta, Where::device_only, 16) ||
+      !pointer_ok(d_scratch, Where::device_only, 8))
+    return IBP_ERR_ARG;
+  const int64_t n_elems = n_rows * row_elems;
+  const int64_t n_words = n_elems * g.w / 32;
+  return launch_build_meta(rows, n_words, dtype, T, block_elems, n_elems, d_meta, d_scratch,
+                           reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_compress(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                 uint32_t block_elems, const ibp_meta *d_meta, void *slots, int64_t slot_bytes,
+                 uint32_t *d_row_bitmask, uint32_t *d_row_bits, int32_t *d_status,
+                 ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_rows < 0 || slot_bytes < slot_bytes_of(g) || slot_bytes % 16 != 0) return IBP_ERR_ARG;
+  if (n_rows == 0) return IBP_OK;
+  if (!pointer_ok(rows, Where::device_or_host, 16) || !pointer_ok(slots, Where::device_or_host, 16) ||
+      !pointer_ok(d_meta, Where::device_only, 16) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      (d_row_bits && !pointer_ok(d_row_bits, Where::device_only, 4)) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_compress(rows, n_rows, g, (uint32_t)dtype, d_meta, slots, slot_bytes,
+                         d_row_bitmask, d_row_bits, d_status, reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                          int64_t row_elems, int dtype, uint32_t block_elems,
+                          const uint32_t *d_row_bitmask, const ibp_meta *d_meta,
+                          const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
+                          ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_rows < 0 || n_idx < 0 || slot_bytes < slot_bytes_of(g) || slot_bytes % 16 != 0)
+    return IBP_ERR_ARG;
+  if (n_idx == 0) return IBP_OK;
+  if (!pointer_ok(slots, Where::device_or_host, 16) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      !pointer_ok(d_meta, Where::device_only, 16) || !pointer_ok(d_idx, Where::device_only, 8) ||
+      !pointer_ok(out, Where::device_only, 16) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_gather(slots, slot_bytes, n_rows, g, (uint32_t)dtype, d_row_bitmask, d_meta, d_idx,
+                       n_idx, out, d_status, reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+              int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s) {
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (n_rows < 0 || row_elems <= 0) return IBP_ERR_ARG;
+  if (!pointer_ok(d_stats, Where::device_only, 8)) return IBP_ERR_ARG;
+  if (n_rows > 0 && (!pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+                     !pointer_ok(d_row_bits, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_query(d_row_bitmask, d_row_bits, n_rows, row_elems * width_of(dtype) / 8, d_stats,
+                      reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, ibp_stream_t s) {
+  if (bytes < 0 || bytes % 16 != 0) return IBP_ERR_ARG;
+  if (!pointer_ok(src, Where::device_or_host, 16) || !pointer_ok(d_sink, Where::device_only, 8))
+    return IBP_ERR_ARG;
+  return launch_probe_read(src, bytes, d_sink, reinterpret_cast<cudaStream_t>(s));
+}
+
+}  // extern "C"

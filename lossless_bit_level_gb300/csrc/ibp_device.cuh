@@ -1,0 +1,159 @@
+// Device-side helpers shared by the IBP kernels.
+//
+// All kernels view a row as 32-bit "lane words": an FP32 element, or two 16-bit
+// elements (element 2k in the low half). With the 16-bit mask and bitval copied
+// into both halves, the packed form of a lane word's non-invariant bits is the
+// concatenation of the two elements' fields, low element first -- which is
+// exactly what the stream holds for two consecutive elements of one block. So one
+// code path serves FP32, FP16 and BF16.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ibp.h"
+
+namespace ibp {
+
+constexpr unsigned FULL = 0xFFFFFFFFu;
+constexpr int MAX_RUNS = 16;  // a 32-bit word has at most 16 runs of ones
+
+// Contiguous runs of non-invariant ("kept") bit positions of a lane word:
+// run r covers lane-word bits [dst, dst+len) and field bits [src, src+len).
+// Built once per CTA in shared memory, then copied into registers by the
+// templated bodies (NR = number of runs, known after the switch).
+struct SharedRuns {
+  uint32_t n;
+  uint32_t dst[MAX_RUNS], len[MAX_RUNS], src[MAX_RUNS];
+};
+
+template <int NR>
+struct RegRuns {
+  uint32_t dst[NR > 0 ? NR : 1], len[NR > 0 ? NR : 1], src[NR > 0 ? NR : 1];
+};
+
+// Per-call code parameters derived from the metadata in device memory.
+struct Code {
+  uint32_t mask32;    // invariant positions, replicated to both halves for 16-bit
+  uint32_t bitval32;  // their values, replicated likewise
+  int fc;             // bits a lane word takes in a matching block (epw * m)
+};
+
+__device__ __forceinline__ uint32_t low_mask(uint32_t n) {  // n in [0, 32]
+  return n >= 32 ? FULL : ((1u << n) - 1u);
+}
+
+__device__ __forceinline__ uint32_t bfe(uint32_t x, uint32_t pos, uint32_t len) {
+  uint32_t r;
+  asm("bfe.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(pos), "r"(len));
+  return r;
+}
+
+// insert the low `len` bits of a into b at `pos`
+__device__ __forceinline__ uint32_t bfi(uint32_t a, uint32_t b, uint32_t pos, uint32_t len) {
+  uint32_t r;
+  asm("bfi.b32 %0, %1, %2, %3, %4;" : "=r"(r) : "r"(a), "r"(b), "r"(pos), "r"(len));
+  return r;
+}
+
+// 32 bits of the 64-bit value (hi:lo) starting at bit sh (sh in [0, 31])
+__device__ __forceinline__ uint32_t window(uint32_t lo, uint32_t hi, uint32_t sh) {
+  return __funnelshift_r(lo, hi, sh);
+}
+
+__device__ __forceinline__ Code make_code(const ibp_meta &m) {
+  Code c;
+  const bool w16 = m.dtype != IBP_FP32;
+  uint32_t mask = w16 ? (m.mask & 0xFFFFu) : m.mask;
+  uint32_t bitval = (w16 ? (m.bitval & 0xFFFFu) : m.bitval) & mask;
+  c.mask32 = w16 ? (mask | (mask << 16)) : mask;
+  c.bitval32 = w16 ? (bitval | (bitval << 16)) : bitval;
+  c.fc = 32 - __popc(c.mask32);
+  return c;
+}
+
+// Fill the run table of `kept` (one thread).
+__device__ __forceinline__ void make_runs(uint32_t kept, SharedRuns &r) {
+  uint32_t n = 0, acc = 0;
+  while (kept) {
+    const uint32_t start = __ffs(kept) - 1;
+    const uint32_t rest = kept >> start;
+    const uint32_t len = (~rest == 0u) ? (32u - start) : (uint32_t)(__ffs(~rest) - 1);
+    r.dst[n] = start;
+    r.len[n] = len;
+    r.src[n] = acc;
+    ++n;
+    acc += len;
+    kept &= ~(low_mask(len) << start);
+  }
+  r.n = n;
+}
+
+template <int NR>
+__device__ __forceinline__ RegRuns<NR> load_runs(const SharedRuns &s) {
+  RegRuns<NR> r;
+#pragma unroll
+  for (int k = 0; k < NR; ++k) {
+    r.dst[k] = s.dst[k];
+    r.len[k] = s.len[k];
+    r.src[k] = s.src[k];
+  }
+  return r;
+}
+
+// Spread a packed field over the kept positions (parallel bit deposit).
+// NR < 0: run count only known at run time, table read from shared memory.
+template <int NR>
+__device__ __forceinline__ uint32_t deposit(uint32_t field, const RegRuns<NR> &r,
+                                            const SharedRuns &s) {
+  uint32_t x = 0;
+  if constexpr (NR >= 0) {
+#pragma unroll
+    for (int k = 0; k < NR; ++k) x = bfi(bfe(field, r.src[k], r.len[k]), x, r.dst[k], r.len[k]);
+  } else {
+    for (uint32_t k = 0; k < s.n; ++k) x = bfi(bfe(field, s.src[k], s.len[k]), x, s.dst[k], s.len[k]);
+  }
+  return x;
+}
+
+// Gather the kept positions of x into a packed field (parallel bit extract).
+template <int NR>
+__device__ __forceinline__ uint32_t extract(uint32_t x, const RegRuns<NR> &r, const SharedRuns &s) {
+  uint32_t f = 0;
+  if constexpr (NR >= 0) {
+#pragma unroll
+    for (int k = 0; k < NR; ++k) f = bfi(bfe(x, r.dst[k], r.len[k]), f, r.src[k], r.len[k]);
+  } else {
+    for (uint32_t k = 0; k < s.n; ++k) f = bfi(bfe(x, s.dst[k], s.len[k]), f, s.src[k], s.len[k]);
+  }
+  return f;
+}
+
+// First error wins; nothing is written when status is null.
+__device__ __forceinline__ void report(int32_t *status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ ibp_meta load_meta(const ibp_meta *m) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4 *>(m));
+  ibp_meta r;
+  r.mask = v.x;
+  r.bitval = v.y;
+  r.dtype = v.z;
+  r.block_elems = v.w;
+  return r;
+}
+
+// Asynchronous 16-byte global -> shared copy (bypasses L1); works for device
+// memory and for registered host memory reached zero-copy.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace ibp

@@ -1,0 +1,47 @@
+// Internal declarations shared by the codec's CUDA translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ibp.h"
+
+namespace ibp {
+
+// Row geometry, computed on the host from (row_elems, dtype, block_elems).
+// Kernels work on 32-bit "lane words": one FP32 element or two 16-bit elements.
+struct RowGeom {
+  int w;             // element width in bits (16 or 32)
+  int epw;           // elements per lane word (32 / w)
+  int B;             // block size in elements
+  int lwb;           // lane words per block (B * w / 32): 16, 32 or 64
+  int nb;            // blocks per row
+  int raw_words;     // lane words per row
+  int64_t row_elems; // elements per row
+  int64_t raw_bytes; // bytes per raw row
+};
+
+inline int width_of(int dtype) { return dtype == IBP_FP32 ? 32 : 16; }
+
+// Device properties the launchers size their grids with (cached per device).
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int max_smem_optin;
+};
+int device_info(DeviceInfo *out);
+
+int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, uint32_t block_elems,
+                      int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s);
+int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
+                    const ibp_meta *d_meta, void *slots, int64_t slot_bytes, uint32_t *d_bitmask,
+                    uint32_t *d_row_bits, int32_t *d_status, cudaStream_t s);
+int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
+                  uint32_t dtype, const uint32_t *d_bitmask, const ibp_meta *d_meta,
+                  const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
+                  cudaStream_t s);
+int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                 int64_t raw_bytes, ibp_stats *d_stats, cudaStream_t s);
+int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s);
+
+}  // namespace ibp

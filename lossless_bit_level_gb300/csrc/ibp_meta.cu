@@ -1,0 +1,157 @@
+// Metadata (preprocessing) kernels of Invariant Bit Packing for sm_103a.
+//
+// "Reducing the GPU Memory Bottleneck with Lossless Compression for ML --
+// Extended", technical summary, "Core algorithm" (preprocessing): find the bit
+// positions that hold the same value in at least a fraction T of the sampled
+// elements; emit a fixed-size mask and bitval kept in GPU memory.
+//
+// meta_count_kernel: a positional population count over the sample's 32-bit
+// words. Each thread adds 8 words per step into bit-sliced carry-save counters
+// (Harley-Seal: ones/twos/fours planes and a ripple counter of "eights"), so a
+// word costs a handful of bitwise operations instead of 32 bit tests; the planes
+// are flushed into 32 per-position totals every 255 steps, then reduced over the
+// warp and added into 32 64-bit global counters. 16-bit elements are counted as
+// halves of 32-bit words and folded in the finalize step.
+// meta_finalize_kernel: one warp applies the threshold in IEEE double and writes
+// the 16-byte ibp_meta.
+#include <algorithm>
+
+#include "ibp_device.cuh"
+#include "ibp_internal.h"
+
+namespace ibp {
+namespace {
+
+constexpr int META_THREADS = 256;
+
+__device__ __forceinline__ void csa(uint32_t &h, uint32_t &l, uint32_t a, uint32_t b, uint32_t c) {
+  const uint32_t u = a ^ b;
+  h = (a & b) | (u & c);
+  l = u ^ c;
+}
+
+struct Planes {
+  uint32_t ones = 0, twos = 0, fours = 0;
+  uint32_t eights[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // ripple counter of eights, bit-sliced
+  uint32_t tot[32];
+};
+
+__device__ __forceinline__ void add8(Planes &P, const uint4 &a, const uint4 &b) {
+  uint32_t twosA, twosB, foursA, foursB, eights;
+  csa(twosA, P.ones, P.ones, a.x, a.y);
+  csa(twosB, P.ones, P.ones, a.z, a.w);
+  csa(foursA, P.twos, P.twos, twosA, twosB);
+  csa(twosA, P.ones, P.ones, b.x, b.y);
+  csa(twosB, P.ones, P.ones, b.z, b.w);
+  csa(foursB, P.twos, P.twos, twosA, twosB);
+  csa(eights, P.fours, P.fours, foursA, foursB);
+  uint32_t carry = eights;
+#pragma unroll
+  for (int l = 0; l < 8; ++l) {
+    const uint32_t t = P.eights[l] & carry;
+    P.eights[l] ^= carry;
+    carry = t;
+  }
+}
+
+__device__ __forceinline__ void flush_eights(Planes &P) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int l = 0; l < 8; ++l) c |= ((P.eights[l] >> j) & 1u) << l;
+    P.tot[j] += 8u * c;
+  }
+#pragma unroll
+  for (int l = 0; l < 8; ++l) P.eights[l] = 0;
+}
+
+__global__ void __launch_bounds__(META_THREADS)
+    meta_count_kernel(const uint4 *__restrict__ v, int64_t nvec, const uint32_t *tail, int ntail,
+                      unsigned long long *counters) {
+  Planes P;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) P.tot[j] = 0;
+  const int64_t npairs = (nvec + 1) / 2;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int steps = 0;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < npairs; k += stride) {
+    const uint4 a = v[2 * k];
+    const uint4 b = (2 * k + 1 < nvec) ? v[2 * k + 1] : make_uint4(0, 0, 0, 0);
+    add8(P, a, b);
+    if (++steps == 255) {
+      flush_eights(P);
+      steps = 0;
+    }
+  }
+  flush_eights(P);
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    P.tot[j] += ((P.ones >> j) & 1u) + 2u * ((P.twos >> j) & 1u) + 4u * ((P.fours >> j) & 1u);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int i = 0; i < ntail; ++i) {
+      const uint32_t x = tail[i];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) P.tot[j] += (x >> j) & 1u;
+    }
+  }
+  // warp reduction, then one 64-bit atomic per position per warp
+  const int lane = threadIdx.x & 31;
+  unsigned long long mine = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    unsigned long long s = P.tot[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    if (lane == j) mine = s;
+  }
+  if (mine) atomicAdd(&counters[lane], mine);
+}
+
+__global__ void meta_finalize_kernel(const unsigned long long *counters, int64_t n_elems, int w,
+                                     double T, uint32_t dtype, uint32_t block_elems,
+                                     ibp_meta *meta) {
+  const int j = threadIdx.x;  // one warp
+  unsigned long long c1 = 0;
+  if (j < w) c1 = (w == 32) ? counters[j] : counters[j] + counters[j + 16];
+  const unsigned long long N = (unsigned long long)n_elems;
+  const unsigned long long c0 = N - c1;
+  const bool v = c1 > c0;  // a tie keeps 0
+  const unsigned long long cv = v ? c1 : c0;
+  const bool inv = j < w && (double)cv >= T * (double)N;
+  const uint32_t mask = __ballot_sync(FULL, inv);
+  const uint32_t bitval = __ballot_sync(FULL, inv && v);
+  if (j == 0) {
+    ibp_meta m;
+    m.mask = mask;
+    m.bitval = bitval;
+    m.dtype = dtype;
+    m.block_elems = block_elems;
+    *meta = m;
+  }
+}
+
+}  // namespace
+
+int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, uint32_t block_elems,
+                      int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s) {
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  unsigned long long *counters = static_cast<unsigned long long *>(d_scratch);
+  if (cudaMemsetAsync(counters, 0, 32 * sizeof(unsigned long long), s) != cudaSuccess)
+    return IBP_ERR_CUDA;
+  const int64_t nvec = n_words / 4;
+  const int ntail = (int)(n_words - 4 * nvec);
+  const uint32_t *tail = static_cast<const uint32_t *>(rows) + 4 * nvec;
+  const int64_t npairs = (nvec + 1) / 2;
+  const int64_t want = std::max<int64_t>(1, (npairs + META_THREADS - 1) / META_THREADS);
+  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * 8);
+  meta_count_kernel<<<grid, META_THREADS, 0, s>>>(static_cast<const uint4 *>(rows), nvec, tail,
+                                                  ntail, counters);
+  if (cudaGetLastError() != cudaSuccess) return IBP_ERR_CUDA;
+  meta_finalize_kernel<<<1, 32, 0, s>>>(counters, n_elems, width_of(dtype), T, (uint32_t)dtype,
+                                        block_elems, d_meta);
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+}
+
+}  // namespace ibp

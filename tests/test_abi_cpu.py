@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks answer before any CUDA work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lossless_bit_level_gb300 as ibp
+from lossless_bit_level_gb300 import build_lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "ibp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return ibp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ibp_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(ibp.SYMBOLS)
+
+
+def test_size_queries(lib):
+    assert ibp.slot_bytes(128, ibp.FP32) == 512
+    assert ibp.slot_bytes(4096, ibp.BF16) == 8192
+    assert ibp.slot_bytes(11008, ibp.BF16) == 22016
+    assert ibp.slot_bytes(33, ibp.FP16) == 80
+    assert ibp.meta_scratch_bytes() == 256
+    with pytest.raises(ibp.IBPError):
+        ibp.slot_bytes(0, ibp.FP32)
+    with pytest.raises(ibp.IBPError) as e:
+        ibp.slot_bytes(128, 7)
+    assert e.value.code == ibp.ERR_DTYPE
+
+
+def test_argument_errors_before_cuda(lib):
+    vp = ctypes.c_void_p
+    # null pointers, bad T, bad dtype, unsupported block size, ragged row
+    assert lib.ibp_build_meta(None, 10, 128, ibp.FP32, 0.9, 32, None, None, None) == ibp.ERR_ARG
+    assert lib.ibp_build_meta(vp(16), 10, 128, ibp.FP32, 1.5, 32, vp(16), vp(16), None) == \
+        ibp.ERR_ARG
+    assert lib.ibp_build_meta(vp(16), 10, 128, 9, 0.9, 32, vp(16), vp(16), None) == ibp.ERR_DTYPE
+    assert lib.ibp_compress(None, 10, 128, ibp.FP32, 48, None, None, 512, None, None, None,
+                            None) == ibp.ERR_ARG  # 128 % 48 != 0
+    assert lib.ibp_compress(None, 10, 128, ibp.FP32, 16, None, None, 512, None, None, None,
+                            None) == ibp.ERR_UNSUPPORTED
+    assert lib.ibp_compress(None, 10, 128, ibp.FP32, 32, None, None, 496, None, None, None,
+                            None) == ibp.ERR_ARG  # slot too small
+    assert lib.ibp_compress(None, 10, 1 << 21, ibp.FP32, 32, None, None, 1 << 23, None, None,
+                            None, None) == ibp.ERR_UNSUPPORTED
+    assert lib.ibp_decompress_gather(None, 512, 10, 128, ibp.FP32, 32, None, None, None, 0, None,
+                                     None, None) == ibp.OK  # empty gather is a no-op
+    assert lib.ibp_decompress_gather(None, 512, 10, 128, ibp.FP32, 32, None, None, None, -1, None,
+                                     None, None) == ibp.ERR_ARG
+    assert lib.ibp_decompress_gather(None, 512, 10, 128, ibp.FP32, 32, None, None, None, 4, None,
+                                     None, None) == ibp.ERR_ARG
+    assert lib.ibp_probe_read(None, 17, None, None) == ibp.ERR_ARG
+    assert ibp.status_string(ibp.ERR_CORRUPT) == "corrupt slot header"

@@ -1,0 +1,265 @@
+"""GPU codec vs the oracle, element by element, on seeded inputs (needs a GPU)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import ibp_inputs as gen
+import lossless_bit_level_gb300 as ibp
+import oracle
+import pins
+from codec_harness import (GpuStore, bitmask_np, compare_slots, from_torch, gpu_compress,
+                           gpu_gather, gpu_meta, meta_tensor, meta_values, oracle_store,
+                           row_bits_np, slots_np, to_torch, words_of)
+
+pytestmark = pytest.mark.gpu
+
+FP32, FP16, BF16 = ibp.FP32, ibp.FP16, ibp.BF16
+
+
+def full_check(words: np.ndarray, dtype_code: int, T: float, B: int, idx: np.ndarray,
+               where: str = "device", rows_where: str = "device"):
+    """Meta, bitmask, row bits, slots and gathered rows against the oracle."""
+    n, L = words.shape
+    mask, bitval, o_slots, o_bitmask, o_row_bits = oracle_store(words, T, B)
+    rows_t = to_torch(words, rows_where)
+    meta = gpu_meta(rows_t, dtype_code, T, B)
+    assert meta_values(meta) == (mask, bitval, dtype_code, B)
+    store = GpuStore(n, L, dtype_code, B, where)
+    gpu_compress(rows_t, meta, store)
+    torch.cuda.synchronize()
+    assert int(store.status.item()) == 0
+    assert np.array_equal(bitmask_np(store), o_bitmask)
+    assert np.array_equal(row_bits_np(store), o_row_bits)
+    raw = L * words.dtype.itemsize
+    compare_slots(slots_np(store), o_slots, o_bitmask, o_row_bits, raw)
+    out, st = gpu_gather(store, meta, idx)
+    assert st == 0
+    o_out, rc = oracle.decompress_gather(o_slots, n, L, words.dtype, B, o_bitmask, mask, bitval, idx)
+    assert rc == 0
+    got = from_torch(out, words.dtype)
+    assert np.array_equal(got, o_out)
+    assert np.array_equal(got, words[idx])
+    return store, meta, (mask, bitval, o_slots, o_bitmask, o_row_bits)
+
+
+def test_tiny_fp32_full_config():
+    """4096 x 128 FP32 N(0, 0.05), T = 0.9, B = 32, 1024 uniform indices, HBM."""
+    words = words_of(gen.tiny_fp32())
+    idx = gen.uniform_indices(words.shape[0], 1024, workload=gen.TINY)
+    full_check(words, FP32, 0.9, 32, idx)
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_gnn_dense_prefix(where):
+    words = words_of(gen.gnn_dense(20_000))
+    idx = gen.zipf_indices(words.shape[0], 5000, 1.0, workload=gen.GNN_DENSE)
+    full_check(words, FP32, 0.9, 32, idx, where=where, rows_where=where)
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_gnn_sparse_prefix(where):
+    words = words_of(gen.gnn_sparse(4000))
+    idx = gen.uniform_indices(words.shape[0], 3000, workload=gen.GNN_SPARSE)
+    full_check(words, FP32, 0.9, 32, idx, where=where)
+
+
+def test_dlrm_prefix():
+    words = words_of(gen.dlrm_table(5, 20_000))
+    idx = gen.zipf_indices(words.shape[0], 4096, 1.05, workload=gen.DLRM)
+    full_check(words, FP32, 0.95, 32, idx, where="host")
+
+
+@pytest.mark.parametrize("name", ["q", "down"])
+def test_llm_weight_rows(name):
+    words = gen.llm_weight(3, name, n_rows=300)
+    idx = np.arange(words.shape[0], dtype=np.int64)
+    full_check(words, BF16, 0.9, 64, idx, where="host")
+
+
+def test_llm_kv_rows():
+    words = gen.llm_kv(2, 1, n_rows=1000)
+    idx = np.arange(words.shape[0], dtype=np.int64)[::-1].copy()
+    full_check(words, BF16, 0.9, 64, idx)
+
+
+@pytest.mark.parametrize("dtype_code,np_dt,B,L", [
+    (FP32, np.uint32, 32, 96), (FP32, np.uint32, 64, 192), (FP32, np.uint32, 32, 1056),
+    (FP16, np.uint16, 32, 32), (FP16, np.uint16, 32, 224), (BF16, np.uint16, 64, 64),
+    (BF16, np.uint16, 32, 11008), (FP16, np.uint16, 64, 4160)])
+def test_shapes_and_ragged_tails(dtype_code, np_dt, B, L):
+    """Several tiles, odd block counts (half-used last chunk for 16-bit B=32),
+    multi-segment rows, rows not a multiple of 32 blocks."""
+    g = np.random.default_rng(L * 7 + B)
+    w = 8 * np.dtype(np_dt).itemsize
+    n = 333
+    base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+    hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 2 + 1)) - 1))
+    flip = g.random(size=(n, L)) < 0.002
+    words = np.where(flip, base, (base & ~hi) | (np.uint64(0x3F1E3F1E) & hi)).astype(np_dt)
+    idx = np.concatenate([g.integers(0, n, size=500), [0, n - 1, 0, 0]]).astype(np.int64)
+    full_check(words, dtype_code, 0.9, B, idx)
+
+
+@pytest.mark.parametrize("mask,bitval", [
+    (0x00000000, 0x00000000),          # empty mask: every row raw
+    (0xFFFFFFFF, 0x00000000),          # full mask: matching blocks are 0 bits
+    (0x55555555, 0x41041041 & 0x55555555),  # 16 runs: generic deposit path
+    (0x0F0F0F0F, 0x0A0B0C0D & 0x0F0F0F0F),  # 4 runs
+    (0x7F800000, 0x3F800000),
+])
+def test_forced_masks_fp32(mask, bitval):
+    """Meta written directly (any mask is a valid code): compress + gather vs oracle."""
+    g = np.random.default_rng(mask & 0xFFFF)
+    n, L, B = 200, 128, 32
+    rnd = g.integers(0, 1 << 32, size=(n, L), dtype=np.uint64).astype(np.uint32)
+    keep = g.random(size=(n, L)) < 0.995
+    words = np.where(keep, (rnd & ~np.uint32(mask)) | np.uint32(bitval), rnd).astype(np.uint32)
+    words[: n // 4] = rnd[: n // 4]  # some rows with no match at all
+    o_slots, o_bitmask, o_row_bits = oracle.compress(words, B, mask, bitval)
+    meta = meta_tensor(mask, bitval, FP32, B)
+    store = GpuStore(n, L, FP32, B, "device")
+    gpu_compress(to_torch(words, "device"), meta, store)
+    torch.cuda.synchronize()
+    assert np.array_equal(bitmask_np(store), o_bitmask)
+    assert np.array_equal(row_bits_np(store), o_row_bits)
+    compare_slots(slots_np(store), o_slots, o_bitmask, o_row_bits, L * 4)
+    idx = g.integers(0, n, size=400)
+    out, st = gpu_gather(store, meta, idx)
+    assert st == 0
+    assert np.array_equal(from_torch(out, np.uint32), words[idx])
+
+
+@pytest.mark.parametrize("mask16", [0x7F80, 0xFFFF, 0x0000, 0x5555, 0x8001])
+def test_forced_masks_bf16(mask16):
+    g = np.random.default_rng(mask16)
+    n, L, B = 150, 256, 64
+    bitval = 0x3F80 & mask16
+    rnd = g.integers(0, 1 << 16, size=(n, L), dtype=np.uint64).astype(np.uint16)
+    keep = g.random(size=(n, L)) < 0.998
+    words = np.where(keep, (rnd & ~np.uint16(mask16)) | np.uint16(bitval), rnd).astype(np.uint16)
+    o_slots, o_bitmask, o_row_bits = oracle.compress(words, B, mask16, bitval)
+    meta = meta_tensor(mask16, bitval, BF16, B)
+    store = GpuStore(n, L, BF16, B, "host")
+    gpu_compress(to_torch(words, "host"), meta, store)
+    torch.cuda.synchronize()
+    assert np.array_equal(bitmask_np(store), o_bitmask)
+    assert np.array_equal(row_bits_np(store), o_row_bits)
+    compare_slots(slots_np(store), o_slots, o_bitmask, o_row_bits, L * 2)
+    idx = g.integers(0, n, size=300)
+    out, st = gpu_gather(store, meta, idx)
+    assert st == 0
+    assert np.array_equal(from_torch(out, np.uint16), words[idx])
+
+
+@pytest.mark.parametrize("w", [32, 16])
+def test_special_values_round_trip(w):
+    g = np.random.default_rng(w)
+    sp = np.array(pins.special_words(w), dtype=np.uint32 if w == 32 else np.uint16)
+    n, L = 256, 128
+    words = sp[g.integers(0, sp.size, size=(n, L))]
+    words[: n // 2] = np.where(g.random(size=(n // 2, L)) < 0.97, sp[3], words[: n // 2])
+    dtype_code = FP32 if w == 32 else FP16
+    for T in (0.0, 0.6, 0.95, 1.0):
+        idx = g.integers(0, n, size=512)
+        full_check(words, dtype_code, T, 32, idx)
+
+
+def test_gpu_decodes_oracle_slots():
+    """The decoder alone: slots written by the oracle, gathered by the GPU."""
+    words = words_of(gen.gnn_sparse(2000))
+    mask, bitval, o_slots, o_bitmask, o_row_bits = oracle_store(words, 0.9, 32)
+    n, L = words.shape
+    store = GpuStore(n, L, FP32, 32, "host")
+    store.slots.copy_(torch.from_numpy(o_slots))
+    store.bitmask.copy_(torch.from_numpy(o_bitmask.view(np.int32)))
+    meta = meta_tensor(mask, bitval, FP32, 32)
+    idx = gen.uniform_indices(n, 2500, workload=gen.GNN_SPARSE)
+    out, st = gpu_gather(store, meta, idx)
+    assert st == 0
+    assert np.array_equal(from_torch(out, np.uint32), words[idx])
+
+
+def test_error_status_and_edge_cases():
+    words = words_of(gen.tiny_fp32(256))
+    n, L = words.shape
+    mask, bitval, o_slots, o_bitmask, o_row_bits = oracle_store(words, 0.9, 32)
+    rows_t = to_torch(words, "device")
+    meta = gpu_meta(rows_t, FP32, 0.9, 32)
+    store = GpuStore(n, L, FP32, 32, "device")
+    gpu_compress(rows_t, meta, store)
+    # out-of-range index: row skipped, status INDEX, other rows still decoded
+    sentinel = torch.full((3, L), -7, dtype=torch.int32, device="cuda")
+    out, st = gpu_gather(store, meta, np.array([5, n, -1], dtype=np.int64), out=sentinel)
+    assert st == ibp.ERR_INDEX
+    got = from_torch(out, np.uint32)
+    assert np.array_equal(got[0], words[5])
+    assert np.all(got[1:] == np.uint32(0xFFFFFFF9))
+    # corrupt header: clear the participation bits of a compressed row
+    bm = bitmask_np(store)
+    r = next(r for r in range(n) if (bm[r // 32] >> (r % 32)) & 1)
+    store.slots[r, 0] = store.slots[r, 0] & 0xF0
+    sentinel = torch.full((1, L), -7, dtype=torch.int32, device="cuda")
+    out, st = gpu_gather(store, meta, np.array([r], dtype=np.int64), out=sentinel)
+    assert st == ibp.ERR_CORRUPT
+    assert np.all(from_torch(out, np.uint32) == np.uint32(0xFFFFFFF9))
+    # empty gather: no-op, no launch
+    out, st = gpu_gather(store, meta, np.zeros(0, dtype=np.int64))
+    assert st == 0 and out.shape == (0, L)
+    # metadata that disagrees with the call: status META, nothing written
+    wrong = meta_tensor(mask, bitval, BF16, 32)
+    sentinel = torch.full((1, L), -7, dtype=torch.int32, device="cuda")
+    out, st = gpu_gather(store, wrong, np.array([0], dtype=np.int64), out=sentinel)
+    assert st == ibp.ERR_META
+    # argument errors are returned before any launch
+    with pytest.raises(ibp.IBPError) as e:
+        ibp.decompress_gather(store.slots, n, L, FP32, 48, store.bitmask, meta,
+                              torch.zeros(1, dtype=torch.int64, device="cuda"),
+                              torch.zeros((1, L), dtype=torch.int32, device="cuda"))
+    assert e.value.code in (ibp.ERR_ARG, ibp.ERR_UNSUPPORTED)
+    pageable = torch.zeros((n, store.slot_bytes), dtype=torch.uint8)
+    with pytest.raises(ibp.IBPError) as e:
+        ibp.decompress_gather(pageable, n, L, FP32, 32, store.bitmask, meta,
+                              torch.zeros(1, dtype=torch.int64, device="cuda"),
+                              torch.zeros((1, L), dtype=torch.int32, device="cuda"))
+    assert e.value.code == ibp.ERR_ARG
+
+
+def test_query_stats():
+    words = words_of(gen.gnn_dense(5000))
+    n, L = words.shape
+    mask, bitval, o_slots, o_bitmask, o_row_bits = oracle_store(words, 0.9, 32)
+    rows_t = to_torch(words, "device")
+    meta = gpu_meta(rows_t, FP32, 0.9, 32)
+    store = GpuStore(n, L, FP32, 32, "device")
+    gpu_compress(rows_t, meta, store)
+    stats_t = torch.zeros((10,), dtype=torch.int32, device="cuda")
+    ibp.query(store.bitmask, store.row_bits, n, L, FP32, stats_t)
+    st = ibp.read_stats(stats_t)
+    stored = oracle.stored_bytes(o_row_bits, o_bitmask, L * 4)
+    flags = (o_bitmask[np.arange(n) // 32] >> (np.arange(n) % 32).astype(np.uint32)) & 1
+    assert st.n_rows == n
+    assert st.n_compressed == int(flags.sum())
+    assert st.raw_bytes == n * L * 4
+    assert st.stored_bytes == int(stored.sum())
+    assert st.total_bits == int(o_row_bits.astype(np.int64).sum())
+
+
+def test_meta_from_host_rows_matches():
+    words = gen.llm_kv(4, 0, n_rows=2048)
+    mask, bitval = oracle.build_meta(words, 0.9)
+    meta = gpu_meta(to_torch(words, "host"), BF16, 0.9, 64)
+    assert meta_values(meta) == (mask, bitval, BF16, 64)
+
+
+def test_probe_read_checksum():
+    g = np.random.default_rng(3)
+    a = g.integers(0, 1 << 32, size=1 << 16, dtype=np.uint64).astype(np.uint32)
+    exp = int(np.bitwise_xor.reduce(a))
+    sink = torch.zeros((2,), dtype=torch.int32, device="cuda")
+    for where in ("device", "host"):
+        ibp.probe_read(to_torch(a, where), sink)
+        torch.cuda.synchronize()
+        got = int(sink.cpu().numpy().view(np.uint64)[0])
+        assert got == exp
