@@ -1,0 +1,618 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Invariant Bit Packing codec.
+
+Headline: decompress-gather throughput in GB/s of uncompressed output rows on the
+dense GNN-feature workload (2,000,000 x 128 FP32, column c ~ N(mu_c, sigma_c),
+rows L2-normalised; T = 0.9, B = 32), one step = one gather of 100,000
+Zipf(1.0) row indices from slots held in page-locked host memory and read
+zero-copy by the kernel. The same run also reports, each with its roofline:
+  * the HBM-resident gather of the same store (slots in device memory);
+  * metadata build and compression throughput (the preprocessing stages);
+  * space saving of the store (bitmask + row sizes from ibp_query);
+  * the end-to-end figure through the C ABI with host buffers (index upload,
+    gather, download of the gathered rows inside the timed region);
+  * the oracle (plain single-threaded C++) timed on the host cores on a bounded
+    sample, as a CPU baseline.
+
+python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload W]
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(no collective on the data path); rank 0 prints one JSON line with the
+whole-job throughput over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ibp_inputs as gen  # noqa: E402
+import lossless_bit_level_gb300 as ibp  # noqa: E402
+
+METRIC = "IBP decompress-gather GB/s (uncompressed out) & space saving %, vs roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+WORKLOADS = {
+    # name: rows factory, dtype code, T, B, batch size, index sampler, residency, description
+    "gnn_dense": dict(
+        rows=lambda: gen.gnn_dense(), dtype=ibp.FP32, T=0.9, B=32, batch=100_000,
+        index=lambda n, k, part: gen.zipf_indices(n, k, 1.0, part=part, workload=gen.GNN_DENSE),
+        residency="host",
+        desc="dense GNN features 2,000,000 x 128 FP32 (col N(mu_c,sigma_c), rows L2-normalised), "
+             "T=0.9, B=32; gather 100,000 Zipf(1.0) indices per step from pinned host slots "
+             "(zero-copy)"),
+    "gnn_sparse": dict(
+        rows=lambda: gen.gnn_sparse(), dtype=ibp.FP32, T=0.9, B=32, batch=100_000,
+        index=lambda n, k, part: gen.uniform_indices(n, k, part=part, workload=gen.GNN_SPARSE),
+        residency="host",
+        desc="sparse GNN features 500,000 x 512 FP32 (1.0 w.p. 0.01), T=0.9, B=32; gather "
+             "100,000 uniform indices per step from pinned host slots (zero-copy)"),
+    "tiny": dict(
+        rows=lambda: gen.tiny_fp32(), dtype=ibp.FP32, T=0.9, B=32, batch=1024,
+        index=lambda n, k, part: gen.uniform_indices(n, k, part=part, workload=gen.TINY),
+        residency="device",
+        desc="tiny FP32 4096 x 128 N(0,0.05), T=0.9, B=32; gather 1024 uniform indices, HBM"),
+    "dlrm_table": dict(
+        rows=lambda: gen.dlrm_table(0), dtype=ibp.FP32, T=0.95, B=32, batch=65_536,
+        index=lambda n, k, part: gen.zipf_indices(n, k, 1.05, part=part, workload=gen.DLRM),
+        residency="host",
+        desc="one DLRM embedding table 1,000,000 x 128 FP32 U(-1e-3,1e-3), T=0.95, B=32; "
+             "gather 65,536 Zipf(1.05) lookups per step from pinned host slots (zero-copy)"),
+}
+
+
+# ----------------------------------------------------------------------------- utilities
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="ibp_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        smax = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        reasons = set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names[1:], r[3][1:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": smax,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def clocks_rejected(clk) -> bool:
+    if not clk:
+        return False
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(clk["reasons"]):
+        return True
+    return clk["sm_mhz"] < 0.5 * clk["sm_max_mhz"] and "sw_power_cap" not in clk["reasons"]
+
+
+def event_pair(stream):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    return a, b
+
+
+def measure_link(dev, nbytes=1 << 30, reps=10):
+    """Pinned host -> device copy bandwidth (cudaMemcpyAsync through torch), device ->
+    pinned host, and the zero-copy read probe kernel over the same pinned buffer."""
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    best_h2d = best_d2h = best_probe = 0.0
+    sink = torch.zeros(2, dtype=torch.int32, device=dev)
+    for _ in range(reps):
+        a, b = event_pair(s)
+        a.record(s)
+        d.copy_(host, non_blocking=True)
+        b.record(s)
+        b.synchronize()
+        best_h2d = max(best_h2d, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+        a.record(s)
+        host.copy_(d, non_blocking=True)
+        b.record(s)
+        b.synchronize()
+        best_d2h = max(best_d2h, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+        a.record(s)
+        ibp.probe_read(host, sink)
+        b.record(s)
+        b.synchronize()
+        best_probe = max(best_probe, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del host, d
+    return {"h2d_memcpy_gbs": best_h2d, "d2h_memcpy_gbs": best_d2h,
+            "zero_copy_read_gbs": best_probe, "bytes": nbytes, "reps": reps}
+
+
+def measure_hbm_copy(dev, nbytes=1 << 30, reps=10):
+    a_t = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).fill_(1)
+    b_t = torch.empty_like(a_t)
+    s = torch.cuda.current_stream()
+    best = 0.0
+    for _ in range(reps):
+        a, b = event_pair(s)
+        a.record(s)
+        b_t.copy_(a_t)
+        b.record(s)
+        b.synchronize()
+        best = max(best, 2 * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return best
+
+
+# ----------------------------------------------------------------------------- the codec
+
+class Store:
+    def __init__(self, words_np, dtype, T, B, residency, dev):
+        self.n, self.L = words_np.shape
+        self.dtype, self.T, self.B, self.residency, self.dev = dtype, T, B, residency, dev
+        self.raw_bytes = self.L * words_np.dtype.itemsize
+        self.slot_bytes = ibp.slot_bytes(self.L, dtype)
+        tdt = torch.int32 if words_np.dtype.itemsize == 4 else torch.int16
+        npv = np.int32 if words_np.dtype.itemsize == 4 else np.int16
+        src = torch.from_numpy(words_np.view(npv))
+        if residency == "host":
+            self.rows = torch.empty(src.shape, dtype=tdt, pin_memory=True)
+            self.rows.copy_(src)
+            self.slots = torch.empty((self.n, self.slot_bytes), dtype=torch.uint8,
+                                     pin_memory=True)
+        else:
+            self.rows = src.to(dev)
+            self.slots = torch.empty((self.n, self.slot_bytes), dtype=torch.uint8, device=dev)
+        self.word_dtype = tdt
+        self.meta = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.scratch = torch.empty(ibp.meta_scratch_bytes() // 4, dtype=torch.int32, device=dev)
+        self.bitmask = torch.zeros(((self.n + 31) // 32,), dtype=torch.int32, device=dev)
+        self.row_bits = torch.zeros((self.n,), dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stats_t = torch.zeros(10, dtype=torch.int32, device=dev)
+
+    def build_meta(self):
+        ibp.build_meta(self.rows, self.T, self.B, self.meta, self.scratch, dtype=self.dtype)
+
+    def compress(self):
+        ibp.compress(self.rows, self.B, self.meta, self.slots, self.bitmask, self.row_bits,
+                     self.status, dtype=self.dtype)
+
+    def gather(self, idx, out, status=None):
+        ibp.decompress_gather(self.slots, self.n, self.L, self.dtype, self.B, self.bitmask,
+                              self.meta, idx, out, status)
+
+    def stats(self):
+        ibp.query(self.bitmask, self.row_bits, self.n, self.L, self.dtype, self.stats_t)
+        return ibp.read_stats(self.stats_t)
+
+    def stored_per_row(self):
+        bits = self.row_bits.cpu().numpy().view(np.uint32).astype(np.int64)
+        bm = self.bitmask.cpu().numpy().view(np.uint32)
+        r = np.arange(self.n)
+        flags = (bm[r // 32] >> (r % 32).astype(np.uint32)) & 1
+        return np.where(flags == 1, 4 * ((bits + 31) // 32), self.raw_bytes)
+
+
+def time_stage(fn, reps, flush=None):
+    s = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a, b = event_pair(s)
+        a.record(s)
+        fn()
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    return min(ts), statistics.median(ts)
+
+
+def timed_gather(store, batches, out, steps, warmup, flush, barrier):
+    """W warm-up steps, then K timed steps; per-step CUDA events on the launch stream
+    (the L2 flush between steps sits outside the events). Returns seconds per step
+    list and the clock summary."""
+    s = torch.cuda.current_stream()
+    for k in range(warmup):
+        store.gather(batches[k % len(batches)], out)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for k in range(steps):
+            flush()
+            starts[k].record(s)
+            store.gather(batches[k % len(batches)], out)
+            ends[k].record(s)
+        torch.cuda.synchronize()
+        barrier()
+    per_step = [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
+    return per_step, clk.summary()
+
+
+def run_e2e(store, host_batches, steps, warmup, dev):
+    """Through the public API with host buffers: pinned index batch -> device, gather,
+    gathered rows -> pinned host, all inside the timed region of each step."""
+    n_idx = host_batches[0].numel()
+    idx_d = torch.empty(n_idx, dtype=torch.int64, device=dev)
+    out_d = torch.empty((n_idx, store.L), dtype=store.word_dtype, device=dev)
+    out_h = torch.empty((n_idx, store.L), dtype=store.word_dtype, pin_memory=True)
+    s = torch.cuda.current_stream()
+
+    def step(k):
+        idx_d.copy_(host_batches[k % len(host_batches)], non_blocking=True)
+        store.gather(idx_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for k in range(warmup):
+        step(k)
+    torch.cuda.synchronize()
+    a, b = event_pair(s)
+    a.record(s)
+    for k in range(steps):
+        step(k)
+    b.record(s)
+    b.synchronize()
+    t = a.elapsed_time(b) * 1e-3 / steps
+    return {"value": n_idx * store.raw_bytes / t / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": n_idx * 8, "d2h_bytes_per_step": n_idx * store.raw_bytes,
+            "ms_per_step": t * 1e3}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_sample(wl, seconds_budget=10.0, sample_rows=200_000):
+    """The oracle (as written) on a bounded sample of the workload: a prefix table of
+    sample_rows rows is built once (meta + compress by the oracle), then batches of
+    the workload's batch size, drawn with the workload's index distribution over the
+    prefix, are gathered until the time budget is spent."""
+    import oracle
+
+    rows = wl["rows_prefix"](sample_rows)
+    words = rows.view(np.uint32) if rows.dtype == np.float32 else rows
+    n, L = words.shape
+    mask, bitval = oracle.build_meta(words, wl["T"])
+    slots, bitmask, _ = oracle.compress(words, wl["B"], mask, bitval)
+    total_bytes = 0
+    total_t = 0.0
+    k = 0
+    out = np.empty((wl["batch"], L), dtype=words.dtype)
+    while total_t < seconds_budget and k < 64:
+        idx = wl["index"](n, wl["batch"], 1000 + k)
+        t0 = time.perf_counter()
+        _, rc = oracle.decompress_gather(slots, n, L, words.dtype, wl["B"], bitmask, mask,
+                                         bitval, idx, out=out)
+        total_t += time.perf_counter() - t0
+        assert rc == 0
+        total_bytes += idx.size * L * words.dtype.itemsize
+        k += 1
+    return {"value": total_bytes / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{k} gathers of {wl['batch']} indices ({wl['index_desc']}) over a "
+                      f"{n}-row prefix table compressed by the oracle; single thread",
+            "seconds": total_t, "batches": k}
+
+
+# ----------------------------------------------------------------------------- main
+
+def workload_table(name):
+    wl = dict(WORKLOADS[name])
+    wl["name"] = name
+    if name == "gnn_dense":
+        wl["rows_prefix"] = lambda n: gen.gnn_dense(n)
+        wl["index_desc"] = "Zipf(1.0)"
+    elif name == "gnn_sparse":
+        wl["rows_prefix"] = lambda n: gen.gnn_sparse(min(n, 500_000))
+        wl["index_desc"] = "uniform"
+    elif name == "tiny":
+        wl["rows_prefix"] = lambda n: gen.tiny_fp32(min(n, 4096))
+        wl["index_desc"] = "uniform"
+    else:
+        wl["rows_prefix"] = lambda n: gen.dlrm_table(0, min(n, 1_000_000))
+        wl["index_desc"] = "Zipf(1.05)"
+    return wl
+
+
+def run_reference(args, wl):
+    """The oracle arm: the plain C++ oracle, as written, on the host cores. Each step
+    gathers a bounded sample of one batch (a prefix of the batch's indices, sized so
+    that the whole run stays within a few minutes) from a prefix table that the
+    oracle itself built; the value is GB/s of rebuilt rows, as for the GPU arm."""
+    rank, _, world = env_rank()
+    if rank != 0:
+        return 0
+    import oracle
+
+    steps, warmup = max(1, args.steps), max(0, args.warmup)
+    prefix_rows = 200_000
+    rows = wl["rows_prefix"](prefix_rows)
+    words = rows.view(np.uint32) if rows.dtype == np.float32 else rows
+    n, L = words.shape
+    mask, bitval = oracle.build_meta(words, wl["T"])
+    slots, bitmask, _ = oracle.compress(words, wl["B"], mask, bitval)
+    out = np.empty((wl["batch"], L), dtype=words.dtype)
+    # calibrate: seconds per index of the oracle gather on this host
+    probe = wl["index"](n, min(wl["batch"], 20_000), 999)
+    t0 = time.perf_counter()
+    oracle.decompress_gather(slots, n, L, words.dtype, wl["B"], bitmask, mask, bitval, probe,
+                             out=out)
+    per_index = (time.perf_counter() - t0) / probe.size
+    budget = 120.0 / (steps + warmup)
+    per_step = int(max(256, min(wl["batch"], budget / max(per_index, 1e-9))))
+    batches = [wl["index"](n, wl["batch"], 2000 + (k % 20))[:per_step] for k in range(20)]
+    for k in range(warmup):
+        oracle.decompress_gather(slots, n, L, words.dtype, wl["B"], bitmask, mask, bitval,
+                                 batches[k % 20], out=out)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        oracle.decompress_gather(slots, n, L, words.dtype, wl["B"], bitmask, mask, bitval,
+                                 batches[k % 20], out=out)
+    t = (time.perf_counter() - t0) / steps
+    value = per_step * L * words.dtype.itemsize / t / 1e9
+    sample = (f"each step gathers the first {per_step} of a {wl['batch']}-index "
+              f"{wl['index_desc']} batch over a {n}-row prefix table built by the oracle; "
+              "single thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": wl["desc"]},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ibp", "reference"], default="ibp")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gnn_dense")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip the HBM-resident and e2e legs")
+    ap.add_argument("--residency", choices=["host", "device"], default=None,
+                    help="override where slots and rows live (default: the workload's)")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="use only the first ROWS rows of the table (smaller profiling cases)")
+    args = ap.parse_args()
+    steps = args.steps if args.steps is not None else 2000
+    warmup = args.warmup if args.warmup is not None else 20
+    args.steps, args.warmup = steps, warmup
+    if warmup < 3 and args.impl == "ibp":
+        raise SystemExit("at least 3 warm-up steps are required")
+    wl = workload_table(args.workload)
+    if args.residency:
+        wl["residency"] = args.residency
+    if args.rows:
+        k = args.rows
+        wl["rows"] = lambda: wl["rows_prefix"](k)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    rank, local_rank, world = env_rank()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    from lossless_bit_level_gb300 import build_lib
+    build_lib.build()
+    ibp.load()
+
+    peaks = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    hbm_peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    # inputs: generated on the host (seeded), resident where the workload says
+    rows_np = wl["rows"]()
+    words = rows_np.view(np.uint32) if rows_np.dtype == np.float32 else rows_np
+    del rows_np
+    store = Store(words, wl["dtype"], wl["T"], wl["B"], wl["residency"], dev)
+    n, L = store.n, store.L
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush():
+        flush_buf.fill_(0)
+
+    link = measure_link(dev)
+    hbm_copy_now = measure_hbm_copy(dev)
+    torch.cuda.empty_cache()
+
+    # preprocessing stages (timed with CUDA events; raw input bytes per second)
+    reps = 5
+    meta_t, _ = time_stage(store.build_meta, reps, flush)
+    comp_t, _ = time_stage(store.compress, reps, flush)
+    torch.cuda.synchronize()
+    assert int(store.status.item()) == 0
+    st = store.stats()
+    stored = store.stored_per_row()
+    table_raw = n * store.raw_bytes
+
+    # index batches (distinct per step, cycled)
+    nb = 20
+    host_batches = [torch.from_numpy(wl["index"](n, wl["batch"], k)).pin_memory()
+                    for k in range(nb)]
+    batches = [b.to(dev) for b in host_batches]
+    out = torch.empty((wl["batch"], L), dtype=store.word_dtype, device=dev)
+    gathered_stored = np.array([stored[b.numpy()].sum() for b in host_batches], dtype=np.int64)
+
+    attempt = 0
+    while True:
+        per_step, clk = timed_gather(store, batches, out, steps, warmup, flush, barrier)
+        attempt += 1
+        if not clocks_rejected(clk) or attempt >= 2:
+            break
+    t_step = float(np.mean(per_step))
+    if dist is not None:
+        tt = torch.tensor([t_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+    out_bytes = wl["batch"] * store.raw_bytes
+    value = world * out_bytes / t_step / 1e9
+    stored_per_step = float(np.mean([gathered_stored[k % nb] for k in range(steps)]))
+    link_bytes = stored_per_step  # compressed bytes crossing the link per launch
+    residency = wl["residency"]
+    if residency == "host":
+        achieved = link_bytes / t_step / 1e9
+        peak = link["h2d_memcpy_gbs"]
+        roofline = {"bound": "host_link", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": None,
+                    "peak_source": "pinned host->device cudaMemcpyAsync, 1 GiB, best of 10, "
+                                   "measured in this run",
+                    "algorithmic_bytes_per_launch": link_bytes}
+    else:
+        alg = wl["batch"] * 8 + stored_per_step + out_bytes
+        achieved = alg / t_step / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": None,
+                    "peak_source": f"{hbm_peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                    "algorithmic_bytes_per_launch": alg}
+
+    extra = {}
+    if not args.quick:
+        # HBM-resident gather of the same store
+        if residency == "host":
+            dstore = Store.__new__(Store)
+            dstore.__dict__.update(store.__dict__)
+            dstore.slots = store.slots.to(dev)
+            dstore.residency = "device"
+            per_step_h, clk_h = timed_gather(dstore, batches, out, max(50, steps // 4), warmup,
+                                             flush, barrier)
+            th = float(np.mean(per_step_h))
+            alg = wl["batch"] * 8 + stored_per_step + out_bytes
+            extra["hbm_resident"] = {
+                "value": out_bytes / th / 1e9, "unit": "GB/s", "ms_per_step": th * 1e3,
+                "roofline": {"bound": "hbm", "achieved": alg / th / 1e9, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": alg / th / 1e9 / hbm_peak,
+                             "traffic": None, "peak_source": f"{hbm_peak_src} hbm_gbs",
+                             "algorithmic_bytes_per_launch": alg},
+                "clocks": clk_h}
+            del dstore
+        extra["e2e"] = run_e2e(store, host_batches, max(20, steps // 10), warmup, dev)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": wl["desc"], "rows": n, "row_elems": L, "T": wl["T"],
+                   "block_elems": wl["B"], "batch": wl["batch"], "residency": residency,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"{world} independent replica(s)"},
+        "space_saving_pct": 100.0 * (1.0 - st.stored_bytes / st.raw_bytes),
+        "space_saving_gathered_pct": 100.0 * (1.0 - stored_per_step / out_bytes),
+        "bit_saving_pct": 100.0 * (1.0 - st.total_bits / (8.0 * st.raw_bytes)),
+        "rows_compressed_pct": 100.0 * st.n_compressed / st.n_rows,
+        "metadata_bytes": 16, "bitmask_bytes": 4 * ((n + 31) // 32),
+        "meta": {"mask": f"{int(store.meta[0].item()) & 0xFFFFFFFF:#010x}",
+                 "bitval": f"{int(store.meta[1].item()) & 0xFFFFFFFF:#010x}"},
+        "roofline": roofline,
+        "clocks": clk,
+        "gpu_launches": steps,
+        "stages": {
+            "build_meta": {"gbs_raw_in": table_raw / meta_t / 1e9, "ms": meta_t * 1e3,
+                           "residency": residency},
+            "compress": {"gbs_raw_in": table_raw / comp_t / 1e9, "ms": comp_t * 1e3,
+                         "residency": residency},
+        },
+        "link": link, "hbm_copy_gbs_this_run": hbm_copy_now,
+        "e2e": extra.pop("e2e", None),
+    }
+    line.update(extra)
+    if residency == "host":
+        line["stages"]["build_meta"]["frac_of_link"] = table_raw / meta_t / 1e9 / link[
+            "h2d_memcpy_gbs"]
+        line["stages"]["compress"]["link_bytes_gbs"] = (table_raw + float(stored.sum())) / \
+            comp_t / 1e9
+    else:
+        line["stages"]["build_meta"]["frac_of_hbm"] = table_raw / meta_t / 1e9 / hbm_peak
+        line["stages"]["compress"]["frac_of_hbm"] = (table_raw + float(stored.sum())) / \
+            comp_t / 1e9 / hbm_peak
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = oracle_sample(wl)
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

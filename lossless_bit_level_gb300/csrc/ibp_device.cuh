@@ -101,6 +101,21 @@ __device__ __forceinline__ RegRuns<NR> load_runs(const SharedRuns &s) {
   return r;
 }
 
+// Spread a packed field over the kept positions of `base` (parallel bit deposit;
+// base supplies the invariant bits, e.g. bitval).
+template <int NR>
+__device__ __forceinline__ uint32_t deposit_into(uint32_t field, uint32_t base,
+                                                 const RegRuns<NR> &r, const SharedRuns &s) {
+  uint32_t x = base;
+  if constexpr (NR >= 0) {
+#pragma unroll
+    for (int k = 0; k < NR; ++k) x = bfi(bfe(field, r.src[k], r.len[k]), x, r.dst[k], r.len[k]);
+  } else {
+    for (uint32_t k = 0; k < s.n; ++k) x = bfi(bfe(field, s.src[k], s.len[k]), x, s.dst[k], s.len[k]);
+  }
+  return x;
+}
+
 // Spread a packed field over the kept positions (parallel bit deposit).
 // NR < 0: run count only known at run time, table read from shared memory.
 template <int NR>
@@ -146,9 +161,13 @@ __device__ __forceinline__ ibp_meta load_meta(const ibp_meta *m) {
 
 // Asynchronous 16-byte global -> shared copy (bypasses L1); works for device
 // memory and for registered host memory reached zero-copy.
+// .ca: the request goes through L1, whose coalescer merges a warp's 16-byte pieces
+// into whole 128-byte lines (the .cg form sends one 32-byte sector request per
+// 16-byte piece, which doubles the bytes read from memory that L2 does not cache,
+// such as host memory read zero-copy).
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
