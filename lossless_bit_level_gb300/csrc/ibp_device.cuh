@@ -18,18 +18,22 @@ namespace ibp {
 constexpr unsigned FULL = 0xFFFFFFFFu;
 constexpr int MAX_RUNS = 16;  // a 32-bit word has at most 16 runs of ones
 
-// Contiguous runs of non-invariant ("kept") bit positions of a lane word:
-// run r covers lane-word bits [dst, dst+len) and field bits [src, src+len).
+// Contiguous runs of non-invariant ("kept") bit positions of a lane word. Run k
+// covers lane-word bits [dst, dst+len) and field bits [src, src+len), where src
+// (the count of kept bits below dst) never exceeds dst. Stored as the left shift
+// sh = dst - src that moves field bits to their place, the run's mask in
+// lane-word space (mdst) and in field space (msrc = mdst >> sh), so one run costs
+// a shift and one AND-OR to deposit or to extract.
 // Built once per CTA in shared memory, then copied into registers by the
 // templated bodies (NR = number of runs, known after the switch).
 struct SharedRuns {
   uint32_t n;
-  uint32_t dst[MAX_RUNS], len[MAX_RUNS], src[MAX_RUNS];
+  uint32_t sh[MAX_RUNS], mdst[MAX_RUNS], msrc[MAX_RUNS];
 };
 
 template <int NR>
 struct RegRuns {
-  uint32_t dst[NR > 0 ? NR : 1], len[NR > 0 ? NR : 1], src[NR > 0 ? NR : 1];
+  uint32_t sh[NR > 0 ? NR : 1], mdst[NR > 0 ? NR : 1], msrc[NR > 0 ? NR : 1];
 };
 
 // Per-call code parameters derived from the metadata in device memory.
@@ -41,19 +45,6 @@ struct Code {
 
 __device__ __forceinline__ uint32_t low_mask(uint32_t n) {  // n in [0, 32]
   return n >= 32 ? FULL : ((1u << n) - 1u);
-}
-
-__device__ __forceinline__ uint32_t bfe(uint32_t x, uint32_t pos, uint32_t len) {
-  uint32_t r;
-  asm("bfe.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(pos), "r"(len));
-  return r;
-}
-
-// insert the low `len` bits of a into b at `pos`
-__device__ __forceinline__ uint32_t bfi(uint32_t a, uint32_t b, uint32_t pos, uint32_t len) {
-  uint32_t r;
-  asm("bfi.b32 %0, %1, %2, %3, %4;" : "=r"(r) : "r"(a), "r"(b), "r"(pos), "r"(len));
-  return r;
 }
 
 // 32 bits of the 64-bit value (hi:lo) starting at bit sh (sh in [0, 31])
@@ -79,12 +70,13 @@ __device__ __forceinline__ void make_runs(uint32_t kept, SharedRuns &r) {
     const uint32_t start = __ffs(kept) - 1;
     const uint32_t rest = kept >> start;
     const uint32_t len = (~rest == 0u) ? (32u - start) : (uint32_t)(__ffs(~rest) - 1);
-    r.dst[n] = start;
-    r.len[n] = len;
-    r.src[n] = acc;
+    const uint32_t m = low_mask(len) << start;
+    r.sh[n] = start - acc;
+    r.mdst[n] = m;
+    r.msrc[n] = m >> (start - acc);
     ++n;
     acc += len;
-    kept &= ~(low_mask(len) << start);
+    kept &= ~m;
   }
   r.n = n;
 }
@@ -94,39 +86,26 @@ __device__ __forceinline__ RegRuns<NR> load_runs(const SharedRuns &s) {
   RegRuns<NR> r;
 #pragma unroll
   for (int k = 0; k < NR; ++k) {
-    r.dst[k] = s.dst[k];
-    r.len[k] = s.len[k];
-    r.src[k] = s.src[k];
+    r.sh[k] = s.sh[k];
+    r.mdst[k] = s.mdst[k];
+    r.msrc[k] = s.msrc[k];
   }
   return r;
 }
 
 // Spread a packed field over the kept positions of `base` (parallel bit deposit;
-// base supplies the invariant bits, e.g. bitval).
+// base supplies the invariant bits, e.g. bitval). Field bits past the last run
+// are ignored, so the field needs no masking. NR < 0: run count known only at
+// run time, table read from shared memory.
 template <int NR>
 __device__ __forceinline__ uint32_t deposit_into(uint32_t field, uint32_t base,
                                                  const RegRuns<NR> &r, const SharedRuns &s) {
   uint32_t x = base;
   if constexpr (NR >= 0) {
 #pragma unroll
-    for (int k = 0; k < NR; ++k) x = bfi(bfe(field, r.src[k], r.len[k]), x, r.dst[k], r.len[k]);
+    for (int k = 0; k < NR; ++k) x |= (field << r.sh[k]) & r.mdst[k];
   } else {
-    for (uint32_t k = 0; k < s.n; ++k) x = bfi(bfe(field, s.src[k], s.len[k]), x, s.dst[k], s.len[k]);
-  }
-  return x;
-}
-
-// Spread a packed field over the kept positions (parallel bit deposit).
-// NR < 0: run count only known at run time, table read from shared memory.
-template <int NR>
-__device__ __forceinline__ uint32_t deposit(uint32_t field, const RegRuns<NR> &r,
-                                            const SharedRuns &s) {
-  uint32_t x = 0;
-  if constexpr (NR >= 0) {
-#pragma unroll
-    for (int k = 0; k < NR; ++k) x = bfi(bfe(field, r.src[k], r.len[k]), x, r.dst[k], r.len[k]);
-  } else {
-    for (uint32_t k = 0; k < s.n; ++k) x = bfi(bfe(field, s.src[k], s.len[k]), x, s.dst[k], s.len[k]);
+    for (uint32_t k = 0; k < s.n; ++k) x |= (field << s.sh[k]) & s.mdst[k];
   }
   return x;
 }
@@ -137,9 +116,9 @@ __device__ __forceinline__ uint32_t extract(uint32_t x, const RegRuns<NR> &r, co
   uint32_t f = 0;
   if constexpr (NR >= 0) {
 #pragma unroll
-    for (int k = 0; k < NR; ++k) f = bfi(bfe(x, r.dst[k], r.len[k]), f, r.src[k], r.len[k]);
+    for (int k = 0; k < NR; ++k) f |= (x >> r.sh[k]) & r.msrc[k];
   } else {
-    for (uint32_t k = 0; k < s.n; ++k) f = bfi(bfe(x, s.dst[k], s.len[k]), f, s.src[k], s.len[k]);
+    for (uint32_t k = 0; k < s.n; ++k) f |= (x >> s.sh[k]) & s.msrc[k];
   }
   return f;
 }

@@ -146,29 +146,38 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
                                             const RegRuns<NR> &runs, const SharedRuns &sruns,
                                             const Unit &un, const uint8_t *buf, int tl) {
   const uint32_t fc = (uint32_t)code.fc;
-  const uint32_t fc_mask = low_mask(fc);
   const uint32_t shrink = 32u - fc;
   const uint32_t *S = reinterpret_cast<const uint32_t *>(buf);
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + un.out_word);
   for (uint32_t v = tl; v < un.nvec; v += TL) {
     const uint32_t lw = 4 * v;
     const uint32_t lb = lw >> a.lwb_shift;
-    const bool p = (un.segp >> lb) & 1u;
+    const uint32_t j = lw - (lb << a.lwb_shift);  // lane word within its block
     const uint32_t cnt = __popc(un.segp & low_mask(lb));
-    const uint32_t f = p ? fc : 32u;
-    const uint32_t fm = p ? fc_mask : FULL;
-    uint32_t pos = un.lsb + (uint32_t)a.lwb * (32u * lb - shrink * cnt) +
-                   (lw - (lb << a.lwb_shift)) * f;
-    uint32_t y[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    const uint32_t blk = un.lsb + (uint32_t)a.lwb * (32u * lb - shrink * cnt);  // block start bit
+    uint4 y;
+    if (!((un.segp >> lb) & 1u)) {
+      // block kept raw: four whole words behind one constant bit shift
+      const uint32_t pos = blk + 32u * j;
       const uint32_t *w = S + (pos >> 5);
-      const uint32_t x = window(w[0], w[1], pos) & fm;
-      const uint32_t d = deposit_into<NR>(x, code.bitval32, runs, sruns);
-      y[t] = p ? d : x;
-      pos += f;
+      const uint32_t sh = pos & 31u;
+      y.x = window(w[0], w[1], sh);
+      y.y = window(w[1], w[2], sh);
+      y.z = window(w[2], w[3], sh);
+      y.w = window(w[3], w[4], sh);
+    } else {
+      // matching block: fields of fc bits, invariant bits put back from bitval
+      uint32_t pos = blk + j * fc;
+      uint32_t f[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t *w = S + (pos >> 5);
+        f[t] = deposit_into<NR>(window(w[0], w[1], pos & 31u), code.bitval32, runs, sruns);
+        pos += fc;
+      }
+      y = make_uint4(f[0], f[1], f[2], f[3]);
     }
-    dst[v] = make_uint4(y[0], y[1], y[2], y[3]);
+    dst[v] = y;
   }
 }
 
