@@ -165,6 +165,25 @@ def event_pair(stream):
     return a, b
 
 
+def recorded_traffic(key):
+    """DRAM / host-link bytes per gather launch from the committed ncu summary
+    (profiles/gather_traffic.json), or None when the gather kernel source changed
+    since those counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gather_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for p in ("ibp_gather.cu", "ibp_device.cuh"):
+        with open(os.path.join(ROOT, "lossless_bit_level_gb300", "csrc", p), "rb") as f:
+            h.update(f.read())
+    if rec.get("kernel_source_sha256") != h.hexdigest():
+        return None
+    return rec.get("captures", {}).get(key)
+
+
 def measure_link(dev, nbytes=1 << 30, reps=10):
     """Pinned host -> device copy bandwidth (cudaMemcpyAsync through torch), device ->
     pinned host, and the zero-copy read probe kernel over the same pinned buffer."""
@@ -540,19 +559,26 @@ def main():
     stored_per_step = float(np.mean([gathered_stored[k % nb] for k in range(steps)]))
     link_bytes = stored_per_step  # compressed bytes crossing the link per launch
     residency = wl["residency"]
+    idx_key = "/uniform" if args.indices == "uniform" else ""
+    rec = recorded_traffic(f"{args.workload}/{residency}{idx_key}") if not args.rows else None
     if residency == "host":
         achieved = link_bytes / t_step / 1e9
         peak = link["h2d_memcpy_gbs"]
+        traffic = rec["sysmem_read_bytes"] if rec else None
         roofline = {"bound": "host_link", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": None,
+                    "frac": achieved / peak, "traffic": traffic,
+                    "traffic_kind": "ncu sysmem read bytes per launch (bytes that crossed the link; "
+                                    "duplicate rows served from L1/L2 do not)",
+                    "traffic_frac": (traffic / t_step / 1e9 / peak) if traffic else None,
                     "peak_source": "pinned host->device cudaMemcpyAsync, 1 GiB, best of 10, "
                                    "measured in this run",
                     "algorithmic_bytes_per_launch": link_bytes}
     else:
         alg = wl["batch"] * 8 + stored_per_step + out_bytes
         achieved = alg / t_step / 1e9
+        traffic = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) if rec else None
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None,
+                    "frac": achieved / hbm_peak, "traffic": traffic,
                     "peak_source": f"{hbm_peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg}
 
@@ -568,11 +594,14 @@ def main():
                                              flush, barrier)
             th = float(np.mean(per_step_h))
             alg = wl["batch"] * 8 + stored_per_step + out_bytes
+            rec_d = recorded_traffic(f"{args.workload}/device{idx_key}") if not args.rows else None
             extra["hbm_resident"] = {
                 "value": out_bytes / th / 1e9, "unit": "GB/s", "ms_per_step": th * 1e3,
                 "roofline": {"bound": "hbm", "achieved": alg / th / 1e9, "peak": hbm_peak,
                              "unit": "GB/s", "frac": alg / th / 1e9 / hbm_peak,
-                             "traffic": None, "peak_source": f"{hbm_peak_src} hbm_gbs",
+                             "traffic": (rec_d["dram_read_bytes"] + rec_d["dram_write_bytes"])
+                             if rec_d else None,
+                             "peak_source": f"{hbm_peak_src} hbm_gbs",
                              "algorithmic_bytes_per_launch": alg},
                 "clocks": clk_h}
             del dstore
