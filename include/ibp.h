@@ -108,6 +108,27 @@ int ibp_meta_scratch_bytes(size_t *bytes);
 int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtype, double T,
                    uint32_t block_elems, ibp_meta *d_meta, void *d_scratch, ibp_stream_t s);
 
+/* ibp_build_meta for callers that cannot allocate device memory (the paper has no
+ * counterpart; this is a library convenience). Same arguments, checks and result
+ * as ibp_build_meta, except that the counters live in a 256-byte array built into
+ * the library (kept by every GPU that loads it until the process exits) instead of
+ * caller-provided scratch. Meant for code that must not call cudaMalloc when it
+ * needs the metadata: a plug-in inside a framework whose allocator owns all device
+ * memory, a latency-critical loop where an allocation's implicit synchronisation is
+ * not allowed, a system that forbids allocation after start-up.
+ * - Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - The counters are cleared on stream s at the start of every call, so results
+ *   never depend on an earlier call; but every call shares the one array, so calls
+ *   whose kernels overlap on the GPU (e.g. on unordered streams) race and give
+ *   undefined results. Order them on one stream or with events.
+ * - Returns IBP_ERR_UNSUPPORTED if the counters ever needed more than the 256 bytes
+ *   built in (ibp_meta_scratch_bytes() is 256 for every input size today). */
+int ibp_build_meta_noalloc(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                           double T, uint32_t block_elems, ibp_meta *d_meta, ibp_stream_t s);
+
 /* Compression ("Core algorithm", compression; "System integration").
  * Encodes rows [0, n_rows) into their slots with the mask/bitval in *d_meta, whose
  * dtype and block_elems must equal the ones passed. Compressed rows hold their

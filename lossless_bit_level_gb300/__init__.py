@@ -43,7 +43,8 @@ class Stats(ctypes.Structure):
 
 
 SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp_build_meta",
-           "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read")
+           "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read",
+           "ibp_build_meta_noalloc")
 
 
 def library_path() -> str:
@@ -71,6 +72,7 @@ def load() -> ctypes.CDLL:
     lib.ibp_decompress_gather.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
     lib.ibp_query.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.ibp_probe_read.argtypes = [vp, i64, vp, vp]
+    lib.ibp_build_meta_noalloc.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp]
     for name in SYMBOLS[1:]:
         getattr(lib, name).restype = i32
     _lib = lib
@@ -132,6 +134,16 @@ def build_meta(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Tenso
     _check(load().ibp_build_meta(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
                                  int(block_elems), _ptr(meta), _ptr(scratch), _stream(stream)),
            "ibp_build_meta")
+
+
+def build_meta_noalloc(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Tensor,
+                       dtype: int | None = None, stream=None) -> None:
+    """ibp_build_meta_noalloc: as build_meta, with the library's built-in counter
+    array instead of caller scratch (for callers that cannot allocate)."""
+    n, L = _rows_shape(rows)
+    _check(load().ibp_build_meta_noalloc(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
+                                         int(block_elems), _ptr(meta), _stream(stream)),
+           "ibp_build_meta_noalloc")
 
 
 def compress(rows: torch.Tensor, block_elems: int, meta: torch.Tensor, slots: torch.Tensor,

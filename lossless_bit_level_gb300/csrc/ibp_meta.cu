@@ -155,3 +155,64 @@ int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, ui
 }
 
 }  // namespace ibp
+
+// ---------------------------------------------------------------------------
+// Metadata build without any device allocation.
+//
+// Some callers cannot allocate device memory at the moment they need the
+// metadata: a plug-in running inside a framework whose allocator owns all device
+// memory and hands none of it out; a latency-critical loop in which a cudaMalloc
+// (which may synchronise the device) must never happen; a system that forbids
+// allocation once it has started. For them, the 256 bytes of bit-position
+// counters live in the file-scope array below, which every GPU that loads this
+// library keeps until the process exits.
+//
+// The counters are cleared on the stream at the start of every call, so a call
+// never sees the previous call's counts, but all calls share this one array:
+// two calls whose kernels overlap on the GPU (different streams, no ordering
+// between them) race on it and both results are then undefined.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr int NOALLOC_COUNTER_WORDS = 32;  // one 64-bit counter per bit position of a 32-bit word
+static __device__ __align__(256) unsigned long long g_noalloc_meta_counters[NOALLOC_COUNTER_WORDS];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {nullptr};
+
+// Device address of the counter array on the current device. The array's name is
+// only a host-side stand-in in host code, so the address is looked up once per
+// device (with that device current) and reused.
+int noalloc_counters(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IBP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (dev >= 0 && dev < NOALLOC_MAX_DEVICES && g_noalloc_ptr[dev]) {
+    *out = g_noalloc_ptr[dev];
+    return IBP_OK;
+  }
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_meta_counters) != cudaSuccess || !ptr) {
+    cudaGetLastError();
+    return IBP_ERR_CUDA;
+  }
+  if (dev >= 0 && dev < NOALLOC_MAX_DEVICES) g_noalloc_ptr[dev] = ptr;
+  *out = ptr;
+  return IBP_OK;
+}
+
+}  // namespace
+
+extern "C" int ibp_build_meta_noalloc(const void *rows, int64_t n_rows, int64_t row_elems,
+                                      int dtype, double T, uint32_t block_elems, ibp_meta *d_meta,
+                                      ibp_stream_t s) {
+  size_t need = 0;
+  if (int rc = ibp_meta_scratch_bytes(&need)) return rc;
+  if (need > sizeof(g_noalloc_meta_counters)) return IBP_ERR_UNSUPPORTED;
+  void *counters = nullptr;
+  if (int rc = noalloc_counters(&counters)) return rc;
+  return ibp_build_meta(rows, n_rows, row_elems, dtype, T, block_elems, d_meta, counters, s);
+}
