@@ -1,0 +1,130 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+Per workload:
+  * metadata: GPU vs oracle over the whole table or tensor;
+  * compression: the slots, bitmask bits and per-row sizes of a random sample of rows
+    against the oracle's own compression of the same rows with the same metadata;
+  * decompress-gather: full index batches, every gathered row against the original
+    row (exact; the codec is lossless) and against the oracle's gather of the sampled
+    rows from the oracle's slots.
+Tables are generated, checked and freed one at a time.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import ibp_inputs as gen
+import lossless_bit_level_gb300 as ibp
+import oracle
+from codec_harness import GpuStore, gpu_compress, gpu_gather, gpu_meta, meta_values, to_torch
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def check_table(words: np.ndarray, dtype: int, T: float, B: int, batches, residencies,
+                sample_rows: int = 4096, oracle_meta: bool = True, seed: int = 0):
+    n, L = words.shape
+    raw = L * words.dtype.itemsize
+    rows_host = to_torch(words, "host")
+    meta = gpu_meta(rows_host, dtype, T, B)
+    mask, bitval, mdt, mb = meta_values(meta)
+    assert (mdt, mb) == (dtype, B)
+    if oracle_meta:
+        assert (mask, bitval) == oracle.build_meta(words, T)
+    # compress zero-copy from host rows into host slots (the bench's configuration)
+    store = GpuStore(n, L, dtype, B, "host")
+    gpu_compress(rows_host, meta, store)
+    torch.cuda.synchronize()
+    assert int(store.status.item()) == 0
+    g = np.random.default_rng(seed)
+    sample = np.unique(np.concatenate([g.integers(0, n, size=sample_rows), [0, n - 1]]))
+    o_slots, o_bitmask, o_row_bits = oracle.compress(words[sample], B, mask, bitval)
+    bm = store.bitmask.cpu().numpy().view(np.uint32)
+    flags = (bm[sample // 32] >> (sample % 32).astype(np.uint32)) & 1
+    o_flags = (o_bitmask[np.arange(sample.size) // 32] >>
+               (np.arange(sample.size) % 32).astype(np.uint32)) & 1
+    assert np.array_equal(flags, o_flags)
+    rb = store.row_bits.cpu().numpy().view(np.uint32)[:n]
+    assert np.array_equal(rb[sample], o_row_bits)
+    gslots = store.slots[torch.from_numpy(sample)].numpy()
+    used = np.where(o_flags == 1, 4 * ((o_row_bits.astype(np.int64) + 31) // 32), raw)
+    for k in range(sample.size):
+        assert np.array_equal(gslots[k, :used[k]], o_slots[k, :used[k]]), int(sample[k])
+    # the last bitmask word has no bits past n_rows
+    if n % 32:
+        assert int(bm[-1]) >> (n % 32) == 0
+    for where in residencies:
+        if where == "device":
+            dstore = GpuStore.__new__(GpuStore)
+            dstore.__dict__.update(store.__dict__)
+            dstore.slots = store.slots.to("cuda")
+            use = dstore
+        else:
+            use = store
+        for idx in batches:
+            out, st = gpu_gather(use, meta, idx)
+            assert st == 0
+            got = out.cpu().numpy().view(words.dtype)
+            assert np.array_equal(got, words[idx]), where
+            # the oracle's gather of the sampled rows from the oracle's own slots
+            pick = np.nonzero(np.isin(idx, sample))[0][:2048]
+            if pick.size:
+                pos = np.searchsorted(sample, idx[pick])
+                o_out, rc = oracle.decompress_gather(o_slots, sample.size, L, words.dtype, B,
+                                                     o_bitmask, mask, bitval, pos)
+                assert rc == 0
+                assert np.array_equal(got[pick], o_out)
+            del out
+        if where == "device":
+            del dstore
+        torch.cuda.empty_cache()
+    return store
+
+
+def test_gnn_dense_full():
+    """2,000,000 x 128 FP32, T = 0.9, B = 32; 100,000 Zipf(1.0) indices, host and HBM."""
+    words = gen.gnn_dense().view(np.uint32)
+    batches = [gen.zipf_indices(words.shape[0], 100_000, 1.0, part=k, workload=gen.GNN_DENSE)
+               for k in range(2)]
+    check_table(words, ibp.FP32, 0.9, 32, batches, ("host", "device"))
+
+
+def test_gnn_sparse_full():
+    """500,000 x 512 FP32 binary, T = 0.9, B = 32; 100,000 uniform indices, host and HBM."""
+    words = gen.gnn_sparse().view(np.uint32)
+    batches = [gen.uniform_indices(words.shape[0], 100_000, part=k, workload=gen.GNN_SPARSE)
+               for k in range(2)]
+    check_table(words, ibp.FP32, 0.9, 32, batches, ("host", "device"))
+
+
+def test_dlrm_all_tables_full():
+    """26 tables x 1,000,000 x 128 FP32, per-table meta T = 0.95, B = 32; 65,536 Zipf(1.05)
+    lookups per table, host and HBM. The oracle builds the metadata of every fourth
+    table over the whole table (its slowest step); every table is checked otherwise."""
+    for t in range(26):
+        words = gen.dlrm_table(t).view(np.uint32)
+        batches = [gen.zipf_indices(words.shape[0], 65_536, 1.05, part=t, workload=gen.DLRM)]
+        check_table(words, ibp.FP32, 0.95, 32, batches, ("host", "device") if t < 2 else ("host",),
+                    sample_rows=1024, oracle_meta=(t % 4 == 0), seed=t)
+        del words
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("layer", [0, 31])
+def test_llm_layer_full(layer):
+    """One decoder layer at full size: the seven weight matrices and K, V caches
+    (8 x 4096 tokens x 4096 channels), per tensor T = 0.9, B = 64; every row streamed
+    in order from host slots."""
+    for name in gen.LLM_MATRICES:
+        words = gen.llm_weight(layer, name)
+        idx = np.arange(words.shape[0], dtype=np.int64)
+        check_table(words, ibp.BF16, 0.9, 64, [idx], ("host",), sample_rows=512, seed=layer)
+    for kv in (0, 1):
+        words = gen.llm_kv(layer, kv)
+        idx = np.arange(words.shape[0], dtype=np.int64)
+        check_table(words, ibp.BF16, 0.9, 64, [idx], ("host", "device"), sample_rows=1024,
+                    seed=layer + kv)
+        del words
+        torch.cuda.empty_cache()
