@@ -67,7 +67,8 @@ enum {
   IBP_ERR_CUDA = -4,        /* a CUDA call or launch failed */
   IBP_ERR_INDEX = -5,       /* (device) gather index outside [0, n_rows) */
   IBP_ERR_CORRUPT = -6,     /* (device) participation bits describe an impossible stream */
-  IBP_ERR_META = -7         /* (device) *d_meta disagrees with the dtype/block_elems passed */
+  IBP_ERR_META = -7,        /* (device) *d_meta disagrees with the dtype/block_elems passed */
+  IBP_ERR_TIMEOUT = -8      /* (device) a bounded wait inside a kernel ran out; output incomplete */
 };
 
 /* Metadata: the fixed-size mask/bitval pair of the preprocessing stage.

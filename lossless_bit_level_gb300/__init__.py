@@ -21,8 +21,8 @@ from . import build_lib
 
 FP32, FP16, BF16 = 0, 1, 2
 OK = 0
-ERR_ARG, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_INDEX, ERR_CORRUPT, ERR_META = (
-    -1, -2, -3, -4, -5, -6, -7)
+ERR_ARG, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_INDEX, ERR_CORRUPT, ERR_META, ERR_TIMEOUT = (
+    -1, -2, -3, -4, -5, -6, -7, -8)
 
 _TORCH_DTYPES = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
 WIDTH = {FP32: 32, FP16: 16, BF16: 16}

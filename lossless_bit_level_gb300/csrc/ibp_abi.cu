@@ -33,6 +33,15 @@ bool pointer_ok(const void *p, Where where, size_t align) {
   }
 }
 
+bool in_device_memory(const void *p) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeDevice;
+}
+
 bool dtype_ok(int dtype) { return dtype == IBP_FP32 || dtype == IBP_FP16 || dtype == IBP_BF16; }
 
 int make_geom(int64_t row_elems, int dtype, uint32_t block_elems, RowGeom *g) {
@@ -163,6 +172,7 @@ const char *ibp_status_string(int code) {
     case IBP_ERR_INDEX: return "gather index out of range";
     case IBP_ERR_CORRUPT: return "corrupt slot header";
     case IBP_ERR_META: return "metadata does not match dtype/block size";
+    case IBP_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
     default: return "unknown status";
   }
 }
@@ -230,7 +240,8 @@ int ibp_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
       (d_status && !pointer_ok(d_status, Where::device_only, 4)))
     return IBP_ERR_ARG;
   return launch_gather(slots, slot_bytes, n_rows, g, (uint32_t)dtype, d_row_bitmask, d_meta, d_idx,
-                       n_idx, out, d_status, reinterpret_cast<cudaStream_t>(s));
+                       n_idx, out, d_status, in_device_memory(slots),
+                       reinterpret_cast<cudaStream_t>(s));
 }
 
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,

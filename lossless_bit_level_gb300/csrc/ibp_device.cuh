@@ -154,4 +154,77 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ---- mbarrier helpers ------------------------------------------------------------
+// Waits are bounded: each poll asks the hardware to suspend the warp for up to
+// WAIT_SUSPEND_NS (it wakes as soon as the phase completes, so a waiting warp takes
+// no issue slots); a wait gives up after WAIT_TIMEOUT_NS of global time or
+// WAIT_POLLS polls, whichever comes first, and the caller then records
+// IBP_ERR_TIMEOUT instead of waiting forever.
+constexpr uint32_t WAIT_SUSPEND_NS = 1u << 16;
+constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
+constexpr uint32_t WAIT_POLLS = 1u << 26;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(WAIT_SUSPEND_NS)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete; gives up when the
+// time or poll bound runs out, or as soon as *abort (nullable) is set. Returns true
+// when the phase completed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < WAIT_POLLS; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((abort && *abort) || global_ns() - t0 > WAIT_TIMEOUT_NS) return false;
+  }
+  return false;
+}
+
+// Make `bar` track this thread's cp.async copies issued so far: the pending count
+// of the current phase is raised by one now and lowered when those copies have
+// landed, so the phase cannot complete before them.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 }  // namespace ibp

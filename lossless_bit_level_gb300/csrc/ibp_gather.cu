@@ -35,6 +35,7 @@ namespace ibp {
 namespace {
 
 constexpr int GATHER_WARPS = 8;         // warps per CTA
+constexpr int GATHER_NBUF = 4;          // staging buffers per team (units in flight + 1)
 constexpr int SEG_TARGET_BYTES = 4096;  // raw bytes per segment (at most 32 blocks)
 
 struct GatherArgs {
@@ -62,8 +63,24 @@ struct Unit {
   uint32_t nchunk;     // 16-byte chunks to stage (0: nothing to do)
   uint32_t nvec;       // 16-byte output vectors (0: nothing to do)
   uint32_t lsb;        // bit offset of the segment's first block in the staged bytes
-  uint32_t segp;       // participation bits of the segment's blocks (0 for raw rows)
+  uint32_t segp;       // participation bits of the segment's blocks (0 for raw rows);
+                       // the row index when lsb == PARSE_HEADER
+  uint32_t bmw;        // bitmask word of the row (only when lsb == PARSE_HEADER)
 };
+
+// Unit.lsb value telling the decoder to take the participation bits from the
+// staged bytes (the whole slot prefix was staged).
+constexpr uint32_t PARSE_HEADER = 0xFFFFFFFFu;
+
+// Stage whole slots (one round trip less per compressed row) when compression can
+// save at most a fifth of a row: even a row whose blocks all match then stores at
+// least 80% of its raw bytes, so reading the raw-size prefix costs little extra.
+// Rows of one segment only (the participation bits then fit one word).
+__device__ __forceinline__ bool whole_slot(const GatherArgs &a, uint32_t shrink) {
+  const uint32_t fc = 32u - shrink;
+  const uint32_t min_bits = (uint32_t)a.nb + (uint32_t)a.lwb * (uint32_t)a.nb * fc;
+  return (int64_t)((min_bits + 31) >> 5) * 4 * 5 >= a.raw_bytes * 4;
+}
 
 __device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u) {
   if (u >= a.n_units) return -1;
@@ -80,6 +97,7 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   un.nvec = 0;
   un.lsb = 0;
   un.segp = 0;
+  un.bmw = 0;
   if (u >= a.n_units) return un;
   int64_t i = u;
   int s = 0;
@@ -96,6 +114,16 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   }
   const uint8_t *slot = a.slots + r * a.slot_bytes;
   const uint32_t nvec = (uint32_t)(nblk * a.lwb / 4);
+  if (a.nseg == 1 && a.n_rows <= 0xFFFFFFFFll && whole_slot(a, shrink)) {
+    // stage the slot's whole raw-size prefix at once: the bitmask bit and, for a
+    // compressed row, the participation bits are read later, off the critical path
+    un.src = slot;
+    un.nchunk = nvec;
+    un.nvec = nvec;
+    un.lsb = PARSE_HEADER;
+    un.segp = (uint32_t)r;
+    return un;
+  }
   if (!((__ldg(a.bitmask + (r >> 5)) >> (r & 31)) & 1u)) {  // stored raw
     un.src = slot + (size_t)b0 * a.lwb * 4;
     un.nchunk = nvec;
@@ -136,6 +164,12 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   return un;
 }
 
+// Issue the bitmask load of a whole-slot unit; its value is used one pipeline step
+// later, when the unit is decoded.
+__device__ __forceinline__ void fetch_bitmask(const GatherArgs &a, Unit &un) {
+  if (un.lsb == PARSE_HEADER) un.bmw = __ldg(a.bitmask + (un.segp >> 5));
+}
+
 template <int TL>
 __device__ __forceinline__ void stage_unit(const Unit &un, uint8_t *buf, int tl) {
   for (uint32_t c = tl; c < un.nchunk; c += TL) cp_async16(buf + 16 * c, un.src + 16 * c);
@@ -149,14 +183,35 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
   const uint32_t shrink = 32u - fc;
   const uint32_t *S = reinterpret_cast<const uint32_t *>(buf);
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + un.out_word);
-  for (uint32_t v = tl; v < un.nvec; v += TL) {
+  uint32_t segp = un.segp, lsb = un.lsb, nvec = un.nvec;
+  if (lsb == PARSE_HEADER) {  // whole slot staged
+    if (!((un.bmw >> (segp & 31)) & 1u)) {  // stored raw: the slot prefix is the row
+      segp = 0;
+      lsb = 0;
+    } else {  // participation bits are S[0] (one segment, nb <= 32)
+      segp = S[0] & low_mask((uint32_t)a.nb);
+      lsb = (uint32_t)a.nb;
+      const uint32_t total =
+          (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * __popc(segp));
+      if ((int64_t)((total + 31) >> 5) * 4 >= a.raw_bytes) {
+        if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
+        nvec = 0;
+      }
+    }
+  }
+  if (segp == 0 && lsb == 0) {  // row stored raw: the staged bytes are the row
+    const uint4 *S4 = reinterpret_cast<const uint4 *>(buf);
+    for (uint32_t v = tl; v < nvec; v += TL) dst[v] = S4[v];
+    return;
+  }
+  for (uint32_t v = tl; v < nvec; v += TL) {
     const uint32_t lw = 4 * v;
     const uint32_t lb = lw >> a.lwb_shift;
     const uint32_t j = lw - (lb << a.lwb_shift);  // lane word within its block
-    const uint32_t cnt = __popc(un.segp & low_mask(lb));
-    const uint32_t blk = un.lsb + (uint32_t)a.lwb * (32u * lb - shrink * cnt);  // block start bit
+    const uint32_t cnt = __popc(segp & low_mask(lb));
+    const uint32_t blk = lsb + (uint32_t)a.lwb * (32u * lb - shrink * cnt);  // block start bit
     uint4 y;
-    if (!((un.segp >> lb) & 1u)) {
+    if (!((segp >> lb) & 1u)) {
       // block kept raw: four whole words behind one constant bit shift
       const uint32_t pos = blk + 32u * j;
       const uint32_t *w = S + (pos >> 5);
@@ -181,9 +236,15 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
   }
 }
 
+// Decode-time fields of a staged unit, kept in shared memory next to its buffer.
+struct __align__(16) StagedMeta {
+  int64_t out_word;
+  uint32_t lsb, segp, nvec, bmw;
+};
+
 template <int NR, int TL>
 __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedRuns &sruns,
-                            uint8_t *warp_smem) {
+                            uint8_t *warp_smem, StagedMeta *warp_meta) {
   constexpr int TPW = 32 / TL;  // teams per warp
   const RegRuns<NR> runs = load_runs<NR>(sruns);
   const int lane = threadIdx.x & 31;
@@ -192,53 +253,87 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
   const bool leader = tl == 0;
   const uint32_t shrink = 32u - (uint32_t)code.fc;
   const int64_t warp_gid = (int64_t)blockIdx.x * GATHER_WARPS + (threadIdx.x >> 5);
-  const int64_t stride = (int64_t)gridDim.x * GATHER_WARPS * TPW;
-  uint8_t *const buf0 = warp_smem + team * a.unit_bytes;
-  const int buf_step = TPW * a.unit_bytes;  // second buffer of this team
+  const int64_t stride = (int64_t)gridDim.x * GATHER_WARPS * TPW;  // between a team's units
+  uint8_t *const bufs = warp_smem + team * a.unit_bytes;  // buffer k at bufs + k * buf_step
+  const int buf_step = TPW * a.unit_bytes;
+  StagedMeta *const metas = warp_meta + team;  // meta k at metas[k * TPW]
 
   int64_t base = warp_gid * TPW;  // first unit of this warp in the current iteration
   if (base >= a.n_units) return;
-  int64_t u = base + team;
-  Unit cur = plan_unit(a, shrink, u, load_index(a, u), leader);
-  int64_t r_next = load_index(a, u + stride);
-  stage_unit<TL>(cur, buf0, tl);
-  cp_async_commit();
-  int b = 0;  // buffer holding `cur`
-  for (;;) {
-    const int64_t u_next = u + stride;
-    const int64_t r_after = load_index(a, u_next + stride);  // prefetch
-    const Unit nxt = plan_unit(a, shrink, u_next, r_next, leader);
-    stage_unit<TL>(nxt, buf0 + (b ^ 1) * buf_step, tl);
+  int64_t u_plan = base + team;  // next unit this team plans
+  int64_t r_plan = load_index(a, u_plan);
+  int k_plan = 0;                // buffer it goes to
+  uint32_t pend_bmw = 0;         // bitmask word loaded for the last planned unit,
+  int pend_k = -1;               // stored into its meta one step later
+
+  // plan one unit, stage its bytes, record what decoding it will need
+  auto plan_and_stage = [&]() {
+    const int64_t r_after = load_index(a, u_plan + stride);  // prefetch
+    const Unit un = plan_unit(a, shrink, u_plan, r_plan, leader);
+    if (leader && pend_k >= 0) metas[pend_k * TPW].bmw = pend_bmw;
+    pend_bmw = un.lsb == PARSE_HEADER ? __ldg(a.bitmask + (un.segp >> 5)) : 0u;
+    pend_k = k_plan;
+    if (leader) {
+      StagedMeta m;
+      m.out_word = un.out_word;
+      m.lsb = un.lsb;
+      m.segp = un.segp;
+      m.nvec = un.nvec;
+      m.bmw = 0;
+      metas[k_plan * TPW] = m;
+    }
+    stage_unit<TL>(un, bufs + k_plan * buf_step, tl);
     cp_async_commit();
-    cp_async_wait<1>();
+    k_plan = k_plan + 1 == GATHER_NBUF ? 0 : k_plan + 1;
+    u_plan += stride;
+    r_plan = r_after;
+  };
+
+#pragma unroll 1
+  for (int j = 0; j < GATHER_NBUF - 1; ++j) plan_and_stage();
+  int k_dec = 0;
+  for (;;) {
+    plan_and_stage();
+    cp_async_wait<GATHER_NBUF - 1>();
     __syncwarp();
-    decode_unit<NR, TL>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
+    const StagedMeta m = metas[k_dec * TPW];
+    Unit un;
+    un.src = nullptr;
+    un.nchunk = 0;
+    un.out_word = m.out_word;
+    un.lsb = m.lsb;
+    un.segp = m.segp;
+    un.nvec = m.nvec;
+    un.bmw = m.bmw;
+    decode_unit<NR, TL>(a, code, runs, sruns, un, bufs + k_dec * buf_step, tl);
     __syncwarp();
     base += stride;
     if (base >= a.n_units) break;
-    cur = nxt;
-    r_next = r_after;
-    u = u_next;
-    b ^= 1;
+    k_dec = k_dec + 1 == GATHER_NBUF ? 0 : k_dec + 1;
   }
   cp_async_wait<0>();
 }
 
 template <int TL>
 __device__ void dispatch_runs(const GatherArgs &a, const Code &code, const SharedRuns &sruns,
-                              uint8_t *warp_smem) {
+                              uint8_t *warp_smem, StagedMeta *warp_meta) {
   switch (sruns.n) {
-    case 0: gather_body<0, TL>(a, code, sruns, warp_smem); break;
-    case 1: gather_body<1, TL>(a, code, sruns, warp_smem); break;
-    case 2: gather_body<2, TL>(a, code, sruns, warp_smem); break;
-    case 3: gather_body<3, TL>(a, code, sruns, warp_smem); break;
-    case 4: gather_body<4, TL>(a, code, sruns, warp_smem); break;
-    default: gather_body<-1, TL>(a, code, sruns, warp_smem); break;
+    case 0: gather_body<0, TL>(a, code, sruns, warp_smem, warp_meta); break;
+    case 1: gather_body<1, TL>(a, code, sruns, warp_smem, warp_meta); break;
+    case 2: gather_body<2, TL>(a, code, sruns, warp_smem, warp_meta); break;
+    case 3: gather_body<3, TL>(a, code, sruns, warp_smem, warp_meta); break;
+    case 4: gather_body<4, TL>(a, code, sruns, warp_smem, warp_meta); break;
+    default: gather_body<-1, TL>(a, code, sruns, warp_smem, warp_meta); break;
   }
 }
 
+// shared bytes of one warp of the team kernel
+__host__ __device__ inline size_t team_warp_bytes(int tl, int unit_bytes) {
+  return (size_t)GATHER_NBUF * (32 / tl) * (unit_bytes + sizeof(StagedMeta));
+}
+
 template <int TL>
-__global__ void __launch_bounds__(GATHER_WARPS * 32, 3) gather_kernel(GatherArgs a) {
+__global__ void __launch_bounds__(GATHER_WARPS * 32, 2) gather_kernel(GatherArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
   const ibp_meta m = load_meta(a.meta);
@@ -249,8 +344,210 @@ __global__ void __launch_bounds__(GATHER_WARPS * 32, 3) gather_kernel(GatherArgs
   const Code code = make_code(m);
   if (threadIdx.x == 0) make_runs(~code.mask32, sruns);
   __syncthreads();
-  uint8_t *warp_smem = smem + (size_t)(threadIdx.x >> 5) * 2 * (32 / TL) * a.unit_bytes;
-  dispatch_runs<TL>(a, code, sruns, warp_smem);
+  uint8_t *warp_smem = smem + (threadIdx.x >> 5) * team_warp_bytes(TL, a.unit_bytes);
+  StagedMeta *warp_meta = reinterpret_cast<StagedMeta *>(
+      warp_smem + (size_t)GATHER_NBUF * (32 / TL) * a.unit_bytes);
+  dispatch_runs<TL>(a, code, sruns, warp_smem, warp_meta);
+}
+
+// ---------------------------------------------------------------------------
+// Warp-specialised variant: planner warps resolve the dependent loads, decoder
+// warps stream.
+//
+// Planning a unit is a chain of dependent memory round trips (index -> bitmask
+// bit -> header words). In the team kernel above every warp waits through that
+// chain itself. Here planner warps do nothing else: one lane per unit, 32 units
+// per step, each plan (source span, bit offset, participation bits, output
+// position) written into a ring of plan slots in shared memory and published with
+// a release arrive on the slot's "planned" mbarrier. Decoder warps run teams of TL
+// lanes; a team takes its next plan (already resolved), releases the plan slot on
+// its "free" mbarrier, stages the unit's bytes into its own double buffer with
+// cp.async and decodes the previous unit meanwhile, so a decoder never waits on a
+// dependent global load, only on its own data one unit behind.
+//
+// Unit k of the CTA uses plan slot k % PLAN_SLOTS. PLAN_SLOTS is a multiple of the
+// CTA's decoder teams and of 32 * planners, so every use of a slot is written by the
+// same planner lane and read by the same decoder team, in order: a slot's barrier is
+// never more than one phase behind the unit being waited for, which the parity
+// waits rely on. Every wait is bounded (mbar_wait); one that runs out records
+// IBP_ERR_TIMEOUT and raises a CTA-wide abort flag that ends every loop.
+// ---------------------------------------------------------------------------
+constexpr int WS_PLANNERS = 2;
+constexpr int WS_DECODERS = 8;
+constexpr int WS_THREADS = 32 * (WS_PLANNERS + WS_DECODERS);
+constexpr int PLAN_SLOTS = 256;
+
+struct __align__(16) PlanSlot {
+  const uint8_t *src;
+  int64_t out_word;
+  uint32_t nchunk, lsb, segp, nvec;
+};
+
+__device__ __forceinline__ void ws_abort(const GatherArgs &a, volatile int *abort) {
+  if (!*abort) {
+    report(a.status, IBP_ERR_TIMEOUT);
+    *abort = 1;
+  }
+}
+
+__device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64_t count,
+                        int64_t r_first, PlanSlot *plans, uint64_t *planned, uint64_t *freed,
+                        volatile int *abort) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t shrink = 32u - (uint32_t)code.fc;
+  const int64_t step = 32 * WS_PLANNERS;
+  int64_t k = 32 * (int64_t)(threadIdx.x >> 5) + lane;
+  int64_t r_next = r_first;
+  for (; k - lane < count; k += step) {
+    const bool have = k < count;
+    const int64_t r = r_next;
+    r_next = k + step < count ? load_index(a, u0 + k + step) : -1;  // prefetch
+    bool ok = true;
+    if (have) {
+      const Unit un = plan_unit(a, shrink, u0 + k, r, true);
+      const int slot = (int)(k % PLAN_SLOTS);
+      ok = mbar_wait(&freed[slot], (uint32_t)((k / PLAN_SLOTS) & 1) ^ 1u, abort);
+      if (ok) {
+        PlanSlot p;
+        p.src = un.src;
+        p.out_word = un.out_word;
+        p.nchunk = un.nchunk;
+        p.lsb = un.lsb;
+        p.segp = un.segp;
+        p.nvec = un.nvec;
+        plans[slot] = p;
+        mbar_arrive(&planned[slot]);
+      }
+    }
+    if (!ok) ws_abort(a, abort);
+    if (__any_sync(FULL, *abort != 0)) break;
+  }
+}
+
+template <int TL>
+__device__ __forceinline__ Unit ws_take(const GatherArgs &a, int64_t k, int64_t count,
+                                        const PlanSlot *plans, uint64_t *planned,
+                                        uint64_t *freed, int tl, volatile int *abort, bool *ok) {
+  Unit un;
+  un.src = nullptr;
+  un.out_word = 0;
+  un.nchunk = 0;
+  un.nvec = 0;
+  un.lsb = 0;
+  un.segp = 0;
+  un.bmw = 0;
+  *ok = true;
+  if (k >= count) return un;
+  const int slot = (int)(k % PLAN_SLOTS);
+  *ok = mbar_wait(&planned[slot], (uint32_t)((k / PLAN_SLOTS) & 1), abort);
+  if (*ok) {
+    const PlanSlot p = plans[slot];
+    un.src = p.src;
+    un.out_word = p.out_word;
+    un.nchunk = p.nchunk;
+    un.lsb = p.lsb;
+    un.segp = p.segp;
+    un.nvec = p.nvec;
+    fetch_bitmask(a, un);
+  }
+  return un;
+}
+
+template <int TL>
+__device__ __forceinline__ void ws_release(int64_t k, int64_t count, uint64_t *freed, int tl) {
+  if (k < count && tl == 0) mbar_arrive(&freed[(int)(k % PLAN_SLOTS)]);
+}
+
+template <int NR, int TL>
+__device__ void ws_decode(const GatherArgs &a, const Code &code, const SharedRuns &sruns,
+                          int64_t count, const PlanSlot *plans, uint64_t *planned,
+                          uint64_t *freed, uint8_t *warp_smem, volatile int *abort) {
+  constexpr int TPW = 32 / TL;
+  const RegRuns<NR> runs = load_runs<NR>(sruns);
+  const int lane = threadIdx.x & 31;
+  const int team = lane / TL;
+  const int tl = lane % TL;
+  const int64_t stride = (int64_t)WS_DECODERS * TPW;  // decoder teams per CTA
+  const int64_t T = (int64_t)((threadIdx.x >> 5) - WS_PLANNERS) * TPW + team;
+  uint8_t *const buf0 = warp_smem + team * a.unit_bytes;
+  const int buf_step = TPW * a.unit_bytes;
+  int64_t k = T;
+  bool ok;
+  Unit cur = ws_take<TL>(a, k, count, plans, planned, freed, tl, abort, &ok);
+  if (!__all_sync(FULL, ok)) {
+    if (lane == 0) ws_abort(a, abort);
+    return;
+  }
+  __syncwarp();
+  ws_release<TL>(k, count, freed, tl);
+  stage_unit<TL>(cur, buf0, tl);
+  cp_async_commit();
+  int b = 0;
+  for (int64_t base = T - team; base < count; base += stride) {
+    const int64_t kn = k + stride;
+    const Unit nxt = ws_take<TL>(a, kn, count, plans, planned, freed, tl, abort, &ok);
+    if (!__all_sync(FULL, ok)) {
+      if (lane == 0) ws_abort(a, abort);
+      break;
+    }
+    __syncwarp();
+    ws_release<TL>(kn, count, freed, tl);
+    stage_unit<TL>(nxt, buf0 + (b ^ 1) * buf_step, tl);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncwarp();
+    decode_unit<NR, TL>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
+    __syncwarp();
+    cur = nxt;
+    k = kn;
+    b ^= 1;
+  }
+  cp_async_wait<0>();
+}
+
+template <int TL>
+__global__ void __launch_bounds__(WS_THREADS, 2) gather_ws_kernel(GatherArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ SharedRuns sruns;
+  __shared__ int abort_flag;
+  __shared__ PlanSlot plans[PLAN_SLOTS];
+  __shared__ uint64_t planned[PLAN_SLOTS], freed[PLAN_SLOTS];
+  const int64_t u0 = a.n_units * blockIdx.x / gridDim.x;
+  const int64_t count = a.n_units * (blockIdx.x + 1) / gridDim.x - u0;
+  const int warp = threadIdx.x >> 5;
+  // planners fetch their first indices while the metadata load is in flight
+  const int64_t k_first = 32 * (int64_t)warp + (threadIdx.x & 31);
+  const int64_t r_first = warp < WS_PLANNERS && k_first < count ? load_index(a, u0 + k_first) : -1;
+  const ibp_meta m = load_meta(a.meta);
+  if (m.dtype != a.dtype || m.block_elems != a.block_elems) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, IBP_ERR_META);
+    return;
+  }
+  const Code code = make_code(m);
+  for (int k = threadIdx.x; k < PLAN_SLOTS; k += blockDim.x) {
+    mbar_init(&planned[k], 1);
+    mbar_init(&freed[k], 1);
+  }
+  if (threadIdx.x == 0) {
+    make_runs(~code.mask32, sruns);
+    abort_flag = 0;
+  }
+  mbar_init_fence();
+  __syncthreads();
+  volatile int *abort = &abort_flag;
+  if (warp < WS_PLANNERS) {
+    ws_plan(a, code, u0, count, r_first, plans, planned, freed, abort);
+    return;
+  }
+  uint8_t *warp_smem = smem + (size_t)(warp - WS_PLANNERS) * 2 * (32 / TL) * a.unit_bytes;
+  switch (sruns.n) {
+    case 0: ws_decode<0, TL>(a, code, sruns, count, plans, planned, freed, warp_smem, abort); break;
+    case 1: ws_decode<1, TL>(a, code, sruns, count, plans, planned, freed, warp_smem, abort); break;
+    case 2: ws_decode<2, TL>(a, code, sruns, count, plans, planned, freed, warp_smem, abort); break;
+    case 3: ws_decode<3, TL>(a, code, sruns, count, plans, planned, freed, warp_smem, abort); break;
+    case 4: ws_decode<4, TL>(a, code, sruns, count, plans, planned, freed, warp_smem, abort); break;
+    default: ws_decode<-1, TL>(a, code, sruns, count, plans, planned, freed, warp_smem, abort); break;
+  }
 }
 
 int ilog2(int x) {
@@ -261,7 +558,7 @@ int ilog2(int x) {
 
 template <int TL>
 int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
-  const size_t smem = (size_t)GATHER_WARPS * 2 * (32 / TL) * a.unit_bytes;
+  const size_t smem = (size_t)GATHER_WARPS * team_warp_bytes(TL, a.unit_bytes);
   static int configured[64] = {0};
   if (dev.device < 64 && !configured[dev.device]) {
     if (cudaFuncSetAttribute(gather_kernel<TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -281,12 +578,53 @@ int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
+template <int TL>
+int launch_ws_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
+  const size_t smem = (size_t)WS_DECODERS * 2 * (32 / TL) * a.unit_bytes;
+  static int configured[64] = {0};
+  if (dev.device < 64 && !configured[dev.device]) {
+    if (cudaFuncSetAttribute(gather_ws_kernel<TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.max_smem_optin - 16384) != cudaSuccess)
+      return IBP_ERR_CUDA;
+    configured[dev.device] = 1;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_ws_kernel<TL>, WS_THREADS,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    return IBP_ERR_CUDA;
+  const int64_t want = std::max<int64_t>(1, (a.n_units + 63) / 64);
+  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
+  gather_ws_kernel<TL><<<grid, WS_THREADS, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+}
+
+int launch_ws(GatherArgs a, const RowGeom &g, const DeviceInfo &dev, cudaStream_t s) {
+  const int block_bytes = g.lwb * 4;
+  a.seg_blocks = std::max(1, std::min({g.nb, 32, SEG_TARGET_BYTES / block_bytes}));
+  a.nseg = (g.nb + a.seg_blocks - 1) / a.seg_blocks;
+  a.unit_bytes = ((a.seg_blocks * block_bytes + 64 + 127) / 128) * 128 + 32;
+  a.n_units = a.n_idx * a.nseg;
+  const int nvec = a.seg_blocks * g.lwb / 4;
+  int tl = 4;
+  while (tl < 32 && tl * 4 < nvec) tl *= 2;
+  // plan slots must be a multiple of the decoder teams and of 32 * planners
+  static_assert(PLAN_SLOTS % (32 * WS_PLANNERS) == 0, "plan ring vs planners");
+  static_assert(PLAN_SLOTS % (WS_DECODERS * 8) == 0, "plan ring vs decoder teams");
+  switch (tl) {
+    case 4: return launch_ws_tl<4>(a, dev, s);
+    case 8: return launch_ws_tl<8>(a, dev, s);
+    case 16: return launch_ws_tl<16>(a, dev, s);
+    default: return launch_ws_tl<32>(a, dev, s);
+  }
+}
+
 }  // namespace
 
 int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
                   uint32_t dtype, const uint32_t *d_bitmask, const ibp_meta *d_meta,
                   const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
-                  cudaStream_t s) {
+                  bool slots_in_device_memory, cudaStream_t s) {
   if (n_idx == 0) return IBP_OK;
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
@@ -306,6 +644,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const R
   a.lwb_shift = ilog2(g.lwb);
   a.nb = g.nb;
   a.raw_words = g.raw_words;
+  a.raw_bytes = g.raw_bytes;
+  if (slots_in_device_memory) return launch_ws(a, g, dev, s);
   const int block_bytes = g.lwb * 4;
   a.seg_blocks = std::max(1, std::min({g.nb, 32, SEG_TARGET_BYTES / block_bytes}));
   a.nseg = (g.nb + a.seg_blocks - 1) / a.seg_blocks;
@@ -313,7 +653,6 @@ int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const R
   // last field; padded so that the teams' buffers start 8 banks apart
   a.unit_bytes = ((a.seg_blocks * block_bytes + 64 + 127) / 128) * 128 + 32;
   a.n_units = n_idx * a.nseg;
-  a.raw_bytes = g.raw_bytes;
   // team size: about four 16-byte vectors per lane
   const int nvec = a.seg_blocks * g.lwb / 4;
   int tl = 4;

@@ -36,10 +36,12 @@ int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, ui
 int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                     const ibp_meta *d_meta, void *slots, int64_t slot_bytes, uint32_t *d_bitmask,
                     uint32_t *d_row_bits, int32_t *d_status, cudaStream_t s);
+// slots_in_device_memory selects the warp-specialised bulk-copy kernel (device
+// memory) or the cp.async kernel (page-locked host memory read zero-copy).
 int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
                   uint32_t dtype, const uint32_t *d_bitmask, const ibp_meta *d_meta,
                   const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
-                  cudaStream_t s);
+                  bool slots_in_device_memory, cudaStream_t s);
 int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
                  int64_t raw_bytes, ibp_stats *d_stats, cudaStream_t s);
 int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s);
