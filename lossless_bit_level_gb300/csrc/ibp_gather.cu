@@ -35,7 +35,7 @@ namespace ibp {
 namespace {
 
 constexpr int GATHER_WARPS = 8;         // warps per CTA
-constexpr int GATHER_NBUF = 4;          // staging buffers per team (units in flight + 1)
+constexpr int GATHER_NBUF = 2;          // staging buffers per team (units in flight + 1)
 constexpr int SEG_TARGET_BYTES = 4096;  // raw bytes per segment (at most 32 blocks)
 
 struct GatherArgs {
@@ -333,7 +333,7 @@ __host__ __device__ inline size_t team_warp_bytes(int tl, int unit_bytes) {
 }
 
 template <int TL>
-__global__ void __launch_bounds__(GATHER_WARPS * 32, 2) gather_kernel(GatherArgs a) {
+__global__ void __launch_bounds__(GATHER_WARPS * 32, 3) gather_kernel(GatherArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
   const ibp_meta m = load_meta(a.meta);
@@ -645,7 +645,14 @@ int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const R
   a.nb = g.nb;
   a.raw_words = g.raw_words;
   a.raw_bytes = g.raw_bytes;
-  if (slots_in_device_memory) return launch_ws(a, g, dev, s);
+  // Slots in device memory with units of more than 1 KiB: the warp-specialised
+  // kernel (planning off the decoders' path pays once a unit takes several vectors
+  // per lane). Small units, and slots in host memory, which the link paces: the
+  // team kernel (every warp decodes; measured faster there).
+  const int block_bytes_all = g.lwb * 4;
+  const int unit_raw = std::max(1, std::min({g.nb, 32, SEG_TARGET_BYTES / block_bytes_all})) *
+                       block_bytes_all;
+  if (slots_in_device_memory && unit_raw > 1024) return launch_ws(a, g, dev, s);
   const int block_bytes = g.lwb * 4;
   a.seg_blocks = std::max(1, std::min({g.nb, 32, SEG_TARGET_BYTES / block_bytes}));
   a.nseg = (g.nb + a.seg_blocks - 1) / a.seg_blocks;
