@@ -606,6 +606,28 @@ def main():
                 "clocks": clk_h}
             del dstore
         extra["e2e"] = run_e2e(store, host_batches, max(20, steps // 10), warmup, dev)
+        # preprocessing stages with rows and slots in HBM
+        if residency == "host":
+            dstore = Store.__new__(Store)
+            dstore.__dict__.update(store.__dict__)
+            dstore.rows = store.rows.to(dev)
+            dstore.slots = torch.empty((n, store.slot_bytes), dtype=torch.uint8, device=dev)
+            dstore.bitmask = torch.zeros_like(store.bitmask)
+            dstore.row_bits = torch.zeros_like(store.row_bits)
+            dstore.status = torch.zeros_like(store.status)
+            mt, _ = time_stage(dstore.build_meta, reps, flush)
+            ct, _ = time_stage(dstore.compress, reps, flush)
+            torch.cuda.synchronize()
+            same = bool(torch.equal(dstore.bitmask, store.bitmask))
+            comp_bytes = table_raw + float(stored.sum())
+            extra["stages_hbm"] = {
+                "build_meta": {"gbs_raw_in": table_raw / mt / 1e9, "ms": mt * 1e3,
+                               "frac_of_hbm": table_raw / mt / 1e9 / hbm_peak},
+                "compress": {"gbs_raw_in": table_raw / ct / 1e9, "ms": ct * 1e3,
+                             "frac_of_hbm": comp_bytes / ct / 1e9 / hbm_peak,
+                             "same_bitmask_as_host_run": same}}
+            del dstore
+            torch.cuda.empty_cache()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
