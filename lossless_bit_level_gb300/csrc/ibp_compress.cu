@@ -48,103 +48,49 @@ struct CompressArgs {
   int64_t raw_bytes;
 };
 
-// Pack one 32-lane-word chunk. Lane l holds value v of width F_l bits, where
-// all lanes of a segment share one width (one segment of 32 lanes, or two of 16
-// when a block is 16 lane words). Returns the payload word owned by this lane
-// (valid for lane < *nwords).
-__device__ __forceinline__ uint32_t pack_chunk(uint32_t v, uint32_t F, bool two_seg,
-                                               uint32_t *nwords) {
-  const int lane = threadIdx.x & 31;
-  uint32_t F0, F1, n0, n1;
-  if (two_seg) {
-    F0 = __shfl_sync(FULL, F, 0);
-    F1 = __shfl_sync(FULL, F, 16);
-    n0 = F0 >> 1;  // 16 lanes * F bits / 32
-    n1 = F1 >> 1;
-  } else {
-    F0 = F;  // uniform
-    F1 = 0;
-    n0 = F0;
-    n1 = 0;
-  }
-  *nwords = n0 + n1;
-  uint32_t Fmin = 32;
-  if (F0 > 0) Fmin = min(Fmin, F0);
-  if (F1 > 0) Fmin = min(Fmin, F1);
-  if (n0 + n1 == 0) return 0;
-  const uint32_t K = (32 + Fmin - 1) / Fmin + 1;
-  // this lane's segment
-  uint32_t t = (uint32_t)lane, base = 0, Fs = F0, seg_lanes = two_seg ? 16u : 32u;
-  if ((uint32_t)lane >= n0) {
-    t = (uint32_t)lane - n0;
-    base = 16;
-    Fs = F1;
-  }
-  const bool owner = (uint32_t)lane < n0 + n1 && Fs > 0;
-  const uint32_t l0 = owner ? base + (32 * t) / Fs : 0;
-  uint32_t P = 0;
-  for (uint32_t it = 0; it < K; ++it) {
-    const uint32_t l = l0 + it;
-    const uint32_t vl = __shfl_sync(FULL, v, (int)min(l, 31u));
-    if (owner && l < base + seg_lanes) {
-      const int shift = (int)((l - base) * Fs) - (int)(32 * t);
-      if (shift < 32 && shift > -(int)Fs) P |= shift >= 0 ? (vl << shift) : (vl >> (-shift));
-    }
-  }
-  return P;
-}
-
-template <int NR>
+// Encode one staged row. LWB = lane words per block (16, 32 or 64). Lane l works on
+// lane words [128 i + 4 l, 128 i + 4 l + 4) of each 128-word span i; a block is then
+// a group of LWB/4 consecutive lanes of a span.
+template <int NR, int LWB>
 __device__ bool compress_row(const CompressArgs &a, const Code &code, const RegRuns<NR> &runs,
-                             const SharedRuns &sruns, int64_t r, uint32_t *RAW, uint32_t *OUT,
-                             uint32_t *HDR) {
+                             const SharedRuns &sruns, int64_t r, const uint32_t *RAW,
+                             uint32_t *OUT, uint32_t *HDR) {
+  constexpr int GS = LWB / 4;  // lanes per block
+  constexpr int BPS = 32 / GS;  // blocks per span
   const int lane = threadIdx.x & 31;
   const int nvec = a.raw_words / 4;
-  // a. stage the raw row
-  const uint4 *src = reinterpret_cast<const uint4 *>(a.rows + r * a.raw_bytes);
-  for (int v = lane; v < nvec; v += 32) reinterpret_cast<uint4 *>(RAW)[v] = src[v];
-  __syncwarp();
+  const int nspan = (a.raw_words + 127) >> 7;
+  const uint4 *RAW4 = reinterpret_cast<const uint4 *>(RAW);
 
-  // b. participation bits
-  const int nchunks = a.raw_words / 32 + ((a.raw_words & 31) ? 1 : 0);
-  uint32_t hacc = 0, cnt_all = 0, pair_ok = 1;
-  for (int c = 0; c < nchunks; ++c) {
-    const int lw = 32 * c + lane;
-    const bool in = lw < a.raw_words;
-    const uint32_t x = in ? RAW[lw] : code.bitval32;
-    const uint32_t M = __ballot_sync(FULL, (x & code.mask32) == code.bitval32);
-    uint32_t bits, nbits, b;
-    if (a.lwb == 16) {
-      b = 2 * c;
-      bits = ((M & 0xFFFFu) == 0xFFFFu ? 1u : 0u) | ((M >> 16) == 0xFFFFu ? 2u : 0u);
-      nbits = 2;
-    } else if (a.lwb == 32) {
-      b = c;
-      bits = M == FULL ? 1u : 0u;
-      nbits = 1;
-    } else {  // 64: two chunks per block
-      if ((c & 1) == 0) {
-        pair_ok = M == FULL;
-        continue;
-      }
-      b = c >> 1;
-      bits = (pair_ok && M == FULL) ? 1u : 0u;
-      nbits = 1;
+  // b. participation bits: a block's bit is the AND of its lanes' ballot bits,
+  // folded with shifts; a span's BPS bits never straddle a header word.
+  uint32_t hacc = 0, cnt_all = 0;
+  for (int i = 0; i < nspan; ++i) {
+    const int v = 32 * i + lane;
+    bool ok = true;
+    if (v < nvec) {
+      const uint4 x = RAW4[v];
+      ok = ((x.x & code.mask32) == code.bitval32) & ((x.y & code.mask32) == code.bitval32) &
+           ((x.z & code.mask32) == code.bitval32) & ((x.w & code.mask32) == code.bitval32);
     }
-    if (b + nbits > (uint32_t)a.nb) {  // half-used last chunk (16-lane-word blocks)
-      nbits = (uint32_t)a.nb - b;
-      bits &= low_mask(nbits);
-    }
-    hacc |= bits << (b & 31);
-    cnt_all += __popc(bits);
-    const uint32_t last = b + nbits - 1;
-    if ((last & 31) == 31 || last == (uint32_t)a.nb - 1) {
-      if (lane == 0) HDR[b >> 5] = hacc;
+    uint32_t A = __ballot_sync(FULL, ok);
+#pragma unroll
+    for (int sft = 1; sft < GS; sft <<= 1) A &= A >> sft;  // bit GS*j: AND of group j
+    uint32_t frag = 0;
+#pragma unroll
+    for (int j = 0; j < BPS; ++j) frag |= ((A >> (GS * j)) & 1u) << j;
+    const int b0 = i * BPS;
+    if (b0 + BPS > a.nb) frag &= low_mask((uint32_t)(a.nb - b0));
+    hacc |= frag << (b0 & 31);
+    cnt_all += __popc(frag);
+    if (((b0 + BPS) & 31) == 0 || b0 + BPS >= a.nb) {
+      if (lane == 0) HDR[b0 >> 5] = hacc;
       hacc = 0;
     }
   }
-  const uint32_t shrink = 32u - (uint32_t)code.fc;
-  const uint32_t total = (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * cnt_all);
+  const uint32_t fc = (uint32_t)code.fc;
+  const uint32_t shrink = 32u - fc;
+  const uint32_t total = (uint32_t)a.nb + (uint32_t)LWB * (32u * (uint32_t)a.nb - shrink * cnt_all);
   const uint32_t sw = (total + 31) >> 5;
   const bool comp = (int64_t)sw * 4 < a.raw_bytes;
   if (a.row_bits && lane == 0) a.row_bits[r] = total;
@@ -152,48 +98,94 @@ __device__ bool compress_row(const CompressArgs &a, const Code &code, const RegR
 
   uint4 *dst = reinterpret_cast<uint4 *>(a.slots + r * a.slot_bytes);
   if (!comp) {
-    for (int v = lane; v < nvec; v += 32) dst[v] = reinterpret_cast<const uint4 *>(RAW)[v];
+    for (int v = lane; v < nvec; v += 32) dst[v] = RAW4[v];
     return false;
   }
 
-  // c. pack
-  const uint32_t nbw = (uint32_t)a.nb >> 5, sh = (uint32_t)a.nb & 31u;
-  for (uint32_t q = lane; q < nbw; q += 32) OUT[q] = HDR[q];
-  uint32_t carry = sh ? HDR[nbw] : 0u;  // low sh bits of the partly filled word
-  uint32_t off = nbw;
-  const bool two_seg = a.lwb == 16;
-  for (int c = 0; c < nchunks; ++c) {
-    const int lw = 32 * c + lane;
-    const bool in = lw < a.raw_words;
-    const uint32_t x = in ? RAW[lw] : 0u;
-    const uint32_t b = (uint32_t)lw >> a.lwb_shift;
-    const bool p = in && ((HDR[b >> 5] >> (b & 31)) & 1u);
-    const uint32_t F = in ? (p ? (uint32_t)code.fc : 32u) : 0u;
-    const uint32_t v = p ? extract<NR>(x, runs, sruns) : x;
-    uint32_t nw;
-    const uint32_t P = pack_chunk(v, F, two_seg, &nw);
-    if (nw == 0) continue;
-    if (sh == 0) {
-      if ((uint32_t)lane < nw) OUT[off + lane] = P;
-    } else {
-      const uint32_t prev = __shfl_up_sync(FULL, P, 1);
-      const uint32_t lo = lane == 0 ? carry : (prev >> (32 - sh));
-      if ((uint32_t)lane < nw) OUT[off + lane] = (P << sh) | lo;
-      carry = __shfl_sync(FULL, P, (int)nw - 1) >> (32 - sh);
-    }
-    off += nw;
-  }
-  if (sh && lane == 0) OUT[off] = carry;
-  // zero the tail of the last 16-byte vector
+  // c. pack. The stream is assembled in OUT: zero it, put the header bits in, then
+  // every lane ORs its bits in (only a chunk's first and last words can be shared
+  // with a neighbour, and OR makes the order irrelevant).
   const uint32_t nout = (sw + 3) & ~3u;
-  if ((uint32_t)lane < nout - sw) OUT[sw + lane] = 0u;
+  for (uint32_t v = lane; v < nout / 4; v += 32)
+    reinterpret_cast<uint4 *>(OUT)[v] = make_uint4(0u, 0u, 0u, 0u);
   __syncwarp();
-  // d. store the stream
+  const uint32_t nhw = ((uint32_t)a.nb + 31) >> 5;
+  for (uint32_t q = lane; q < nhw; q += 32) OUT[q] = HDR[q];
+  __syncwarp();
+  uint32_t base = (uint32_t)a.nb;  // stream position of the current span
+  for (int i = 0; i < nspan; ++i) {
+    const int v = 32 * i + lane;
+    const bool in = v < nvec;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (in) x = RAW4[v];
+    const uint32_t blk = (uint32_t)(4 * v) / LWB;
+    const bool p = in && ((HDR[blk >> 5] >> (blk & 31)) & 1u);
+    const uint32_t F = in ? (p ? fc : 32u) : 0u;  // bits per lane word
+    // the lane's chunk: its four fields, lowest word first, as c0..c3 (4F <= 128 bits)
+    uint32_t c0, c1, c2, c3;
+    if (!p) {
+      c0 = x.x;
+      c1 = x.y;
+      c2 = x.z;
+      c3 = x.w;
+    } else if (F == 0) {
+      c0 = c1 = c2 = c3 = 0u;
+    } else {
+      const uint64_t f0 = extract<NR>(x.x, runs, sruns), f1 = extract<NR>(x.y, runs, sruns);
+      const uint64_t f2 = extract<NR>(x.z, runs, sruns), f3 = extract<NR>(x.w, runs, sruns);
+      const uint64_t lo = f0 | (f1 << F), hi = f2 | (f3 << F);  // 2F < 64 bits each
+      const uint64_t w01 = lo | (hi << (2 * F));
+      const uint64_t w23 = hi >> (64 - 2 * F);
+      c0 = (uint32_t)w01;
+      c1 = (uint32_t)(w01 >> 32);
+      c2 = (uint32_t)w23;
+      c3 = (uint32_t)(w23 >> 32);
+    }
+    const uint32_t T = 4 * F;  // chunk bits
+    // exclusive prefix of chunk sizes over the span's lanes
+    uint32_t incl = T;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t pos = base + incl - T;
+    base += __shfl_sync(FULL, incl, 31);
+    if (T) {
+      const uint32_t sh = pos & 31u, q = pos >> 5;
+      const uint32_t nw = (sh + T + 31) >> 5;  // words touched (1..5)
+      const uint32_t W0 = c0 << sh;
+      const uint32_t W1 = __funnelshift_l(c0, c1, sh);
+      const uint32_t W2 = __funnelshift_l(c1, c2, sh);
+      const uint32_t W3 = __funnelshift_l(c2, c3, sh);
+      const uint32_t W4 = __funnelshift_l(c3, 0u, sh);
+      atomicOr(&OUT[q], W0);
+      if (nw > 1) atomicOr(&OUT[q + 1], W1);
+      if (nw > 2) atomicOr(&OUT[q + 2], W2);
+      if (nw > 3) atomicOr(&OUT[q + 3], W3);
+      if (nw > 4) atomicOr(&OUT[q + 4], W4);
+    }
+  }
+  __syncwarp();
+  // d. store the stream (tail of the last 16-byte vector is zero)
   for (uint32_t v = lane; v < nout / 4; v += 32) dst[v] = reinterpret_cast<const uint4 *>(OUT)[v];
   return true;
 }
 
-template <int NR>
+// Stage row r into RAW with 16-byte cp.async copies (one commit group).
+__device__ __forceinline__ void prefetch_row(const CompressArgs &a, int64_t r, uint32_t *RAW) {
+  if (r < a.n_rows) {
+    const uint8_t *src = a.rows + r * a.raw_bytes;
+    const int nvec = a.raw_words / 4;
+    for (int v = threadIdx.x & 31; v < nvec; v += 32)
+      cp_async16(reinterpret_cast<uint8_t *>(RAW) + 16 * v, src + 16 * v);
+  }
+  cp_async_commit();
+}
+
+// A warp takes rows unit*32 + k for k = warp, warp + warps, ... of each of the CTA's
+// units in turn, and stages its next row while it encodes the current one.
+template <int NR, int LWB>
 __device__ void compress_body(const CompressArgs &a, const Code &code, const SharedRuns &sruns,
                               uint8_t *smem, uint32_t *flags) {
   const RegRuns<NR> runs = load_runs<NR>(sruns);
@@ -201,15 +193,35 @@ __device__ void compress_body(const CompressArgs &a, const Code &code, const Sha
   const int warp = threadIdx.x >> 5;
   uint8_t *mine = smem + (size_t)warp * a.warp_bytes;
   uint32_t *HDR = reinterpret_cast<uint32_t *>(mine);
-  uint32_t *RAW = HDR + a.hdr_words;
-  uint32_t *OUT = RAW + a.raw_words;
+  uint32_t *RAW0 = HDR + a.hdr_words;
+  uint32_t *OUT = RAW0 + 2 * a.raw_words;
+  if ((int64_t)blockIdx.x >= a.n_units) return;
+  // position of the row after (unit, k) in this warp's sequence
+  auto next_of = [&](int64_t &unit, int &k) {
+    k += a.warps;
+    if (k >= 32) {
+      k = warp;
+      unit += gridDim.x;
+    }
+  };
+  int64_t pu = blockIdx.x;
+  int pk = warp;
+  if (pk < 32) prefetch_row(a, pu * 32 + pk, RAW0);
+  int b = 0;
   for (int64_t unit = blockIdx.x; unit < a.n_units; unit += gridDim.x) {
     for (int k = warp; k < 32; k += a.warps) {
+      next_of(pu, pk);
+      if (pu < a.n_units) prefetch_row(a, pu * 32 + pk, RAW0 + (b ^ 1) * a.raw_words);
+      else cp_async_commit();
+      cp_async_wait<1>();
+      __syncwarp();
       const int64_t r = unit * 32 + k;
       bool comp = false;
-      if (r < a.n_rows) comp = compress_row<NR>(a, code, runs, sruns, r, RAW, OUT, HDR);
+      if (r < a.n_rows)
+        comp = compress_row<NR, LWB>(a, code, runs, sruns, r, RAW0 + b * a.raw_words, OUT, HDR);
       if (lane == 0) flags[k] = comp ? 1u : 0u;
       __syncwarp();
+      b ^= 1;
     }
     __syncthreads();
     if (warp == 0) {
@@ -218,8 +230,10 @@ __device__ void compress_body(const CompressArgs &a, const Code &code, const Sha
     }
     __syncthreads();
   }
+  cp_async_wait<0>();
 }
 
+template <int LWB>
 __global__ void __launch_bounds__(COMPRESS_MAX_WARPS * 32) compress_kernel(CompressArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
@@ -233,12 +247,12 @@ __global__ void __launch_bounds__(COMPRESS_MAX_WARPS * 32) compress_kernel(Compr
   if (threadIdx.x == 0) make_runs(~code.mask32, sruns);
   __syncthreads();
   switch (sruns.n) {
-    case 0: compress_body<0>(a, code, sruns, smem, flags); break;
-    case 1: compress_body<1>(a, code, sruns, smem, flags); break;
-    case 2: compress_body<2>(a, code, sruns, smem, flags); break;
-    case 3: compress_body<3>(a, code, sruns, smem, flags); break;
-    case 4: compress_body<4>(a, code, sruns, smem, flags); break;
-    default: compress_body<-1>(a, code, sruns, smem, flags); break;
+    case 0: compress_body<0, LWB>(a, code, sruns, smem, flags); break;
+    case 1: compress_body<1, LWB>(a, code, sruns, smem, flags); break;
+    case 2: compress_body<2, LWB>(a, code, sruns, smem, flags); break;
+    case 3: compress_body<3, LWB>(a, code, sruns, smem, flags); break;
+    case 4: compress_body<4, LWB>(a, code, sruns, smem, flags); break;
+    default: compress_body<-1, LWB>(a, code, sruns, smem, flags); break;
   }
 }
 
@@ -246,6 +260,26 @@ int ilog2(int x) {
   int s = 0;
   while ((1 << s) < x) ++s;
   return s;
+}
+
+template <int LWB>
+int launch_lwb(const CompressArgs &a, const DeviceInfo &dev, int limit, size_t smem,
+               cudaStream_t s) {
+  static int configured[64] = {0};
+  if (dev.device < 64 && !configured[dev.device]) {
+    if (cudaFuncSetAttribute(compress_kernel<LWB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             limit) != cudaSuccess)
+      return IBP_ERR_CUDA;
+    configured[dev.device] = 1;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<LWB>, a.warps * 32,
+                                                    smem) != cudaSuccess ||
+      per_sm < 1)
+    return IBP_ERR_CUDA;
+  const int grid = (int)std::min<int64_t>(a.n_units, (int64_t)dev.sm_count * per_sm);
+  compress_kernel<LWB><<<grid, a.warps * 32, smem, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
 }  // namespace
@@ -273,28 +307,18 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
   a.raw_words = g.raw_words;
   a.raw_bytes = g.raw_bytes;
   a.hdr_words = (((g.nb + 31) / 32) + 3) & ~3;
-  // header + raw row + stream (never longer than the raw row when kept)
-  a.warp_bytes = 4 * (a.hdr_words + 2 * g.raw_words);
+  // header + two staged raw rows + stream (never longer than the raw row when kept)
+  a.warp_bytes = 4 * (a.hdr_words + 3 * g.raw_words);
   const int limit = std::min(COMPRESS_SMEM_BUDGET, dev.max_smem_optin - 2048);
   a.warps = std::min(COMPRESS_MAX_WARPS, limit / a.warp_bytes);
   if (a.warps < 1) return IBP_ERR_UNSUPPORTED;
   a.n_units = (n_rows + 31) / 32;
   const size_t smem = (size_t)a.warps * a.warp_bytes;
-  static int configured[64] = {0};
-  if (dev.device < 64 && !configured[dev.device]) {
-    if (cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             limit) != cudaSuccess)
-      return IBP_ERR_CUDA;
-    configured[dev.device] = 1;
+  switch (g.lwb) {
+    case 16: return launch_lwb<16>(a, dev, limit, smem, s);
+    case 32: return launch_lwb<32>(a, dev, limit, smem, s);
+    default: return launch_lwb<64>(a, dev, limit, smem, s);
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel, a.warps * 32,
-                                                    smem) != cudaSuccess ||
-      per_sm < 1)
-    return IBP_ERR_CUDA;
-  const int grid = (int)std::min<int64_t>(a.n_units, (int64_t)dev.sm_count * per_sm);
-  compress_kernel<<<grid, a.warps * 32, smem, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
 }  // namespace ibp
