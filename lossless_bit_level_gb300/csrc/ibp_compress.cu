@@ -6,19 +6,20 @@
 // per block, run on the GPU over zero-copy memory) and "System integration"
 // (fixed-size buffer per row, GPU bitmask of compressed rows).
 //
-// One warp encodes one row; a CTA owns 32 consecutive rows so that it writes
-// whole bitmask words (no atomics, deterministic). Per row:
-//   a. the raw row is staged in shared memory with 128-bit loads (read once,
-//      also when it sits in host memory);
-//   b. match pass: lane-strided lane words, ballot per 32 lane words -> the
-//      participation bit of each block -> header words; the compressed-block
-//      count gives the row's exact size and the raw-or-compressed decision;
-//   c. pack pass (compressed rows only): per 32 lane words each lane extracts
-//      its field; the lane that owns payload word t collects the fields that
-//      overlap it with shuffles (each word is built by one lane, no atomics);
-//      the payload is shifted past the nb header bits with a carry word and
-//      written to a shared-memory copy of the stream;
-//   d. the stream (or the raw row) is written to the slot with 128-bit stores.
+// One warp encodes one row at a time; warps take rows grid-strided and stage the
+// next row with cp.async while encoding the current one. Per row:
+//   a. (staged) the raw row in shared memory, read once, also from host memory;
+//   b. match pass: each lane tests four consecutive lane words (one 16-byte shared
+//      load); a block's participation bit is the AND of its lanes' ballot bits;
+//      the compressed-block count gives the row's exact size and the
+//      raw-or-compressed decision;
+//   c. pack pass (compressed rows only): each lane extracts its four fields,
+//      concatenates them into one chunk, finds the chunk's stream position with a
+//      warp scan of chunk sizes and ORs its words into a shared-memory copy of the
+//      stream (only a chunk's first and last words can be shared with a
+//      neighbour, and OR makes the order irrelevant);
+//   d. the stream (or the raw row) is written to the slot with 128-bit stores, and
+//      the row's bitmask bit is set or cleared with one atomic (one writer per bit).
 #include <algorithm>
 
 #include "ibp_device.cuh"
@@ -183,11 +184,13 @@ __device__ __forceinline__ void prefetch_row(const CompressArgs &a, int64_t r, u
   cp_async_commit();
 }
 
-// A warp takes rows unit*32 + k for k = warp, warp + warps, ... of each of the CTA's
-// units in turn, and stages its next row while it encodes the current one.
+// Warps take rows grid-strided (row warp_gid, then + total warps, ...) and stage each
+// one's next row while encoding the current. Every row sets or clears its own bit of
+// the bitmask with one atomic (each bit has exactly one writer, so the final words
+// do not depend on the order); warp 0 of CTA 0 clears the bits past n_rows.
 template <int NR, int LWB>
 __device__ void compress_body(const CompressArgs &a, const Code &code, const SharedRuns &sruns,
-                              uint8_t *smem, uint32_t *flags) {
+                              uint8_t *smem) {
   const RegRuns<NR> runs = load_runs<NR>(sruns);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -195,40 +198,26 @@ __device__ void compress_body(const CompressArgs &a, const Code &code, const Sha
   uint32_t *HDR = reinterpret_cast<uint32_t *>(mine);
   uint32_t *RAW0 = HDR + a.hdr_words;
   uint32_t *OUT = RAW0 + 2 * a.raw_words;
-  if ((int64_t)blockIdx.x >= a.n_units) return;
-  // position of the row after (unit, k) in this warp's sequence
-  auto next_of = [&](int64_t &unit, int &k) {
-    k += a.warps;
-    if (k >= 32) {
-      k = warp;
-      unit += gridDim.x;
-    }
-  };
-  int64_t pu = blockIdx.x;
-  int pk = warp;
-  if (pk < 32) prefetch_row(a, pu * 32 + pk, RAW0);
+  const int64_t first = (int64_t)blockIdx.x * a.warps + warp;
+  const int64_t step = (int64_t)gridDim.x * a.warps;
+  if (first == 0 && lane == 0 && (a.n_rows & 31))
+    atomicAnd(&a.bitmask[a.n_rows >> 5], low_mask((uint32_t)(a.n_rows & 31)));
+  if (first >= a.n_rows) return;
+  prefetch_row(a, first, RAW0);
   int b = 0;
-  for (int64_t unit = blockIdx.x; unit < a.n_units; unit += gridDim.x) {
-    for (int k = warp; k < 32; k += a.warps) {
-      next_of(pu, pk);
-      if (pu < a.n_units) prefetch_row(a, pu * 32 + pk, RAW0 + (b ^ 1) * a.raw_words);
-      else cp_async_commit();
-      cp_async_wait<1>();
-      __syncwarp();
-      const int64_t r = unit * 32 + k;
-      bool comp = false;
-      if (r < a.n_rows)
-        comp = compress_row<NR, LWB>(a, code, runs, sruns, r, RAW0 + b * a.raw_words, OUT, HDR);
-      if (lane == 0) flags[k] = comp ? 1u : 0u;
-      __syncwarp();
-      b ^= 1;
+  for (int64_t r = first; r < a.n_rows; r += step) {
+    prefetch_row(a, r + step, RAW0 + (b ^ 1) * a.raw_words);  // no-op past the end
+    cp_async_wait<1>();
+    __syncwarp();
+    const bool comp =
+        compress_row<NR, LWB>(a, code, runs, sruns, r, RAW0 + b * a.raw_words, OUT, HDR);
+    if (lane == 0) {
+      const uint32_t bit = 1u << (r & 31);
+      if (comp) atomicOr(&a.bitmask[r >> 5], bit);
+      else atomicAnd(&a.bitmask[r >> 5], ~bit);
     }
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t word = __ballot_sync(FULL, flags[lane] != 0);
-      if (lane == 0) a.bitmask[unit] = word;
-    }
-    __syncthreads();
+    __syncwarp();
+    b ^= 1;
   }
   cp_async_wait<0>();
 }
@@ -237,7 +226,6 @@ template <int LWB>
 __global__ void __launch_bounds__(COMPRESS_MAX_WARPS * 32) compress_kernel(CompressArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
-  __shared__ uint32_t flags[32];
   const ibp_meta m = load_meta(a.meta);
   if (m.dtype != a.dtype || m.block_elems != a.block_elems) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, IBP_ERR_META);
@@ -247,12 +235,12 @@ __global__ void __launch_bounds__(COMPRESS_MAX_WARPS * 32) compress_kernel(Compr
   if (threadIdx.x == 0) make_runs(~code.mask32, sruns);
   __syncthreads();
   switch (sruns.n) {
-    case 0: compress_body<0, LWB>(a, code, sruns, smem, flags); break;
-    case 1: compress_body<1, LWB>(a, code, sruns, smem, flags); break;
-    case 2: compress_body<2, LWB>(a, code, sruns, smem, flags); break;
-    case 3: compress_body<3, LWB>(a, code, sruns, smem, flags); break;
-    case 4: compress_body<4, LWB>(a, code, sruns, smem, flags); break;
-    default: compress_body<-1, LWB>(a, code, sruns, smem, flags); break;
+    case 0: compress_body<0, LWB>(a, code, sruns, smem); break;
+    case 1: compress_body<1, LWB>(a, code, sruns, smem); break;
+    case 2: compress_body<2, LWB>(a, code, sruns, smem); break;
+    case 3: compress_body<3, LWB>(a, code, sruns, smem); break;
+    case 4: compress_body<4, LWB>(a, code, sruns, smem); break;
+    default: compress_body<-1, LWB>(a, code, sruns, smem); break;
   }
 }
 
@@ -277,7 +265,8 @@ int launch_lwb(const CompressArgs &a, const DeviceInfo &dev, int limit, size_t s
                                                     smem) != cudaSuccess ||
       per_sm < 1)
     return IBP_ERR_CUDA;
-  const int grid = (int)std::min<int64_t>(a.n_units, (int64_t)dev.sm_count * per_sm);
+  const int64_t want = (a.n_rows + a.warps - 1) / a.warps;
+  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
   compress_kernel<LWB><<<grid, a.warps * 32, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
