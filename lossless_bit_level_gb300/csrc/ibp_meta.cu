@@ -75,7 +75,25 @@ __global__ void __launch_bounds__(META_THREADS)
   const int64_t npairs = (nvec + 1) / 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int steps = 0;
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < npairs; k += stride) {
+  int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // four steps at a time: all eight 16-byte loads are issued before any is used
+  for (; k + 3 * stride < npairs; k += 4 * stride) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t kk = k + j * stride;
+      a[j] = v[2 * kk];
+      b[j] = (2 * kk + 1 < nvec) ? v[2 * kk + 1] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) add8(P, a[j], b[j]);
+    steps += 4;
+    if (steps >= 252) {
+      flush_eights(P);
+      steps = 0;
+    }
+  }
+  for (; k < npairs; k += stride) {
     const uint4 a = v[2 * k];
     const uint4 b = (2 * k + 1 < nvec) ? v[2 * k + 1] : make_uint4(0, 0, 0, 0);
     add8(P, a, b);
