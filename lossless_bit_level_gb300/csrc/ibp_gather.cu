@@ -332,8 +332,10 @@ __host__ __device__ inline size_t team_warp_bytes(int tl, int unit_bytes) {
   return (size_t)GATHER_NBUF * (32 / tl) * (unit_bytes + sizeof(StagedMeta));
 }
 
-template <int TL>
-__global__ void __launch_bounds__(GATHER_WARPS * 32, 3) gather_kernel(GatherArgs a) {
+// MINB: resident CTAs per SM the register budget is sized for (4 for slots in
+// device memory, 3 for host memory; measured best for each).
+template <int TL, int MINB>
+__global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
   const ibp_meta m = load_meta(a.meta);
@@ -556,25 +558,25 @@ int ilog2(int x) {
   return s;
 }
 
-template <int TL>
+template <int TL, int MINB>
 int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const size_t smem = (size_t)GATHER_WARPS * team_warp_bytes(TL, a.unit_bytes);
   static int configured[64] = {0};
   if (dev.device < 64 && !configured[dev.device]) {
-    if (cudaFuncSetAttribute(gather_kernel<TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gather_kernel<TL, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dev.max_smem_optin - (int)sizeof(SharedRuns) - 1024) != cudaSuccess)
       return IBP_ERR_CUDA;
     configured[dev.device] = 1;
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL>, GATHER_WARPS * 32,
-                                                    smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL, MINB>,
+                                                    GATHER_WARPS * 32, smem) != cudaSuccess ||
       per_sm < 1)
     return IBP_ERR_CUDA;
   const int64_t units_per_cta = (int64_t)GATHER_WARPS * (32 / TL);
   const int64_t want = (a.n_units + units_per_cta - 1) / units_per_cta;
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
-  gather_kernel<TL><<<grid, GATHER_WARPS * 32, smem, s>>>(a);
+  gather_kernel<TL, MINB><<<grid, GATHER_WARPS * 32, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
@@ -664,11 +666,15 @@ int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const R
   const int nvec = a.seg_blocks * g.lwb / 4;
   int tl = 4;
   while (tl < 32 && tl * 4 < nvec) tl *= 2;
+  if (slots_in_device_memory) {  // units of at most 1 KiB: team size 4 or 8
+    if (tl == 4) return launch_tl<4, 4>(a, dev, s);
+    return launch_tl<8, 4>(a, dev, s);
+  }
   switch (tl) {
-    case 4: return launch_tl<4>(a, dev, s);
-    case 8: return launch_tl<8>(a, dev, s);
-    case 16: return launch_tl<16>(a, dev, s);
-    default: return launch_tl<32>(a, dev, s);
+    case 4: return launch_tl<4, 3>(a, dev, s);
+    case 8: return launch_tl<8, 3>(a, dev, s);
+    case 16: return launch_tl<16, 3>(a, dev, s);
+    default: return launch_tl<32, 3>(a, dev, s);
   }
 }
 
