@@ -230,6 +230,24 @@ def measure_hbm_copy(dev, nbytes=1 << 30, reps=10):
     return best
 
 
+def job_throughput(t_local: float, bytes_per_step_local: float, dist=None, device=None):
+    """Whole-job throughput of independent replicas: every rank processed
+    bytes_per_step_local per step; the job's step time is the slowest rank's, so the
+    value is the sum of all ranks' bytes over that time. Returns (t_step, GB/s)."""
+    world = 1
+    total = bytes_per_step_local
+    t = t_local
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        tt = torch.tensor([t_local, bytes_per_step_local], dtype=torch.float64, device=device)
+        tmax = tt[:1].clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        tsum = tt[1:].clone()
+        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+        t, total = float(tmax.item()), float(tsum.item())
+    return t, total / t / 1e9
+
+
 # ----------------------------------------------------------------------------- the codec
 
 class Store:
@@ -549,13 +567,8 @@ def main():
         attempt += 1
         if not clocks_rejected(clk) or attempt >= 2:
             break
-    t_step = float(np.mean(per_step))
-    if dist is not None:
-        tt = torch.tensor([t_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
     out_bytes = wl["batch"] * store.raw_bytes
-    value = world * out_bytes / t_step / 1e9
+    t_step, value = job_throughput(float(np.mean(per_step)), out_bytes, dist, dev)
     stored_per_step = float(np.mean([gathered_stored[k % nb] for k in range(steps)]))
     link_bytes = stored_per_step  # compressed bytes crossing the link per launch
     residency = wl["residency"]

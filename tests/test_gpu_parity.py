@@ -263,3 +263,32 @@ def test_probe_read_checksum():
         torch.cuda.synchronize()
         got = int(sink.cpu().numpy().view(np.uint64)[0])
         assert got == exp
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_gather_in_cuda_graph(where):
+    """A gather captured once in a CUDA graph and replayed on new index contents."""
+    words = words_of(gen.gnn_dense(8000))
+    n, L = words.shape
+    rows_t = to_torch(words, "device")
+    meta = gpu_meta(rows_t, FP32, 0.9, 32)
+    store = GpuStore(n, L, FP32, 32, where)
+    gpu_compress(rows_t, meta, store)
+    idx = torch.zeros(3000, dtype=torch.int64, device="cuda")
+    out = torch.zeros((3000, L), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ibp.decompress_gather(store.slots, n, L, FP32, 32, store.bitmask, meta, idx, out, status)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ibp.decompress_gather(store.slots, n, L, FP32, 32, store.bitmask, meta, idx, out, status,
+                              stream=s)
+    for k in range(3):
+        ix = gen.zipf_indices(n, 3000, 1.0, part=50 + k, workload=gen.GNN_DENSE)
+        idx.copy_(torch.from_numpy(ix))
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), words[ix])
