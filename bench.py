@@ -315,15 +315,17 @@ def time_stage(fn, reps, flush=None):
 
 def timed_gather(store, batches, out, steps, warmup, flush, barrier):
     """W warm-up steps, then K timed steps; per-step CUDA events on the launch stream
-    (the L2 flush between steps sits outside the events). Returns seconds per step
-    list and the clock summary."""
+    (the L2 flush between steps sits outside the events). The clock sampler starts
+    before the warm-up, so that the warm-up steps, not the first timed one, absorb
+    whatever the pause of its start-up leaves behind. Returns seconds per step list
+    and the clock summary."""
     s = torch.cuda.current_stream()
-    for k in range(warmup):
-        store.gather(batches[k % len(batches)], out)
-    torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     with ClockSampler(torch.cuda.current_device()) as clk:
+        for k in range(warmup):
+            flush()
+            store.gather(batches[k % len(batches)], out)
         barrier()
         torch.cuda.synchronize()
         for k in range(steps):
@@ -339,31 +341,42 @@ def timed_gather(store, batches, out, steps, warmup, flush, barrier):
 
 def run_e2e(store, host_batches, steps, warmup, dev):
     """Through the public API with host buffers: pinned index batch -> device, gather,
-    gathered rows -> pinned host, all inside the timed region of each step."""
+    gathered rows -> pinned host, all inside the timed region of each step. Steps
+    alternate between two streams with their own buffers, so that the read-back of
+    step k (device -> host) overlaps the gather of step k+1 (host -> device); every
+    step still makes both copies."""
     n_idx = host_batches[0].numel()
-    idx_d = torch.empty(n_idx, dtype=torch.int64, device=dev)
-    out_d = torch.empty((n_idx, store.L), dtype=store.word_dtype, device=dev)
-    out_h = torch.empty((n_idx, store.L), dtype=store.word_dtype, pin_memory=True)
-    s = torch.cuda.current_stream()
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    idx_d = [torch.empty(n_idx, dtype=torch.int64, device=dev) for _ in range(2)]
+    out_d = [torch.empty((n_idx, store.L), dtype=store.word_dtype, device=dev) for _ in range(2)]
+    out_h = [torch.empty((n_idx, store.L), dtype=store.word_dtype, pin_memory=True)
+             for _ in range(2)]
+    main = torch.cuda.current_stream()
 
     def step(k):
-        idx_d.copy_(host_batches[k % len(host_batches)], non_blocking=True)
-        store.gather(idx_d, out_d)
-        out_h.copy_(out_d, non_blocking=True)
+        j = k % 2
+        with torch.cuda.stream(streams[j]):
+            idx_d[j].copy_(host_batches[k % len(host_batches)], non_blocking=True)
+            store.gather(idx_d[j], out_d[j])
+            out_h[j].copy_(out_d[j], non_blocking=True)
 
     for k in range(warmup):
         step(k)
     torch.cuda.synchronize()
-    a, b = event_pair(s)
-    a.record(s)
+    a, b = event_pair(main)
+    a.record(main)
+    for st in streams:
+        st.wait_event(a)
     for k in range(steps):
         step(k)
-    b.record(s)
+    for st in streams:
+        main.wait_stream(st)
+    b.record(main)
     b.synchronize()
     t = a.elapsed_time(b) * 1e-3 / steps
     return {"value": n_idx * store.raw_bytes / t / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": n_idx * 8, "d2h_bytes_per_step": n_idx * store.raw_bytes,
-            "ms_per_step": t * 1e3}
+            "ms_per_step": t * 1e3, "streams": 2}
 
 
 # ----------------------------------------------------------------------------- oracle arm

@@ -60,6 +60,9 @@ class Oracle:
         lib.ibpo_decompress_gather.argtypes = [vp, i64, i64, i64, i32, i64, vp, u32, u32, vp,
                                                i64, vp]
         lib.ibpo_decompress_gather.restype = i32
+        lib.ibpo_select_meta.argtypes = [vp, i64, i64, i32, dbl, i64, ctypes.POINTER(u32),
+                                         ctypes.POINTER(u32), vp, vp, ctypes.POINTER(i32)]
+        lib.ibpo_select_meta.restype = i32
         self.lib = lib
         self.path = path
 
@@ -76,6 +79,25 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"oracle build_meta rejected its arguments ({rc})")
         return mask.value, bitval.value
+
+    def select_meta(self, rows: np.ndarray, T: float, block_elems: int):
+        """Saving-aware mask choice over a 2-D array of rows.
+        Returns (mask, bitval, [(candidate mask, stored bytes), ...])."""
+        a = np.ascontiguousarray(rows)
+        if a.ndim != 2:
+            raise ValueError("rows must be 2-D")
+        w = _width(a)
+        n, L = a.shape
+        mask, bitval, nc = ctypes.c_uint32(0), ctypes.c_uint32(0), ctypes.c_int(0)
+        cm = np.zeros(33, dtype=np.uint32)
+        cb = np.zeros(33, dtype=np.int64)
+        rc = self.lib.ibpo_select_meta(_ptr(a), n, L, w, float(T), int(block_elems),
+                                       ctypes.byref(mask), ctypes.byref(bitval), _ptr(cm),
+                                       _ptr(cb), ctypes.byref(nc))
+        if rc != OK:
+            raise ValueError(f"oracle select_meta rejected its arguments ({rc})")
+        cands = [(int(cm[k]), int(cb[k])) for k in range(nc.value)]
+        return mask.value, bitval.value, cands
 
     def compress(self, rows: np.ndarray, block_elems: int, mask: int, bitval: int,
                  slot_bytes_: int | None = None):
@@ -156,6 +178,10 @@ def slot_bytes(row_elems: int, w_bits: int) -> int:
 
 def build_meta(elems: np.ndarray, T: float) -> tuple[int, int]:
     return default().build_meta(elems, T)
+
+
+def select_meta(rows: np.ndarray, T: float, block_elems: int):
+    return default().select_meta(rows, T, block_elems)
 
 
 def compress(rows: np.ndarray, block_elems: int, mask: int, bitval: int,

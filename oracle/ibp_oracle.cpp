@@ -25,6 +25,8 @@
 
 #include <string.h>
 
+#include <vector>
+
 namespace {
 
 /* read element e of a little-endian array of w-bit words */
@@ -275,4 +277,80 @@ extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int
     }
   }
   return status;
+}
+
+/* Saving-aware mask selection: start from the threshold rule's mask and drop
+   its least-held positions one group at a time; compress the rows under every
+   mask so obtained and keep the one that stores them in the fewest bytes. */
+extern "C" int ibpo_select_meta(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                                double T, int64_t block_elems, uint32_t *mask_out,
+                                uint32_t *bitval_out, uint32_t *cand_mask, int64_t *cand_bytes,
+                                int *n_cand) {
+  if (!rows || n_rows <= 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
+      row_elems % block_elems != 0 || !(T >= 0.0 && T <= 1.0) || !mask_out || !bitval_out)
+    return IBPO_BAD_ARG;
+  const int64_t n_elems = n_rows * row_elems;
+  uint32_t mask0 = 0, bitval0 = 0;
+  if (ibpo_build_meta(rows, n_elems, w_bits, T, &mask0, &bitval0) != IBPO_OK) return IBPO_BAD_ARG;
+
+  /* how many elements hold the majority value of each position */
+  const unsigned char *base = (const unsigned char *)rows;
+  int64_t ones[32];
+  for (int j = 0; j < 32; ++j) ones[j] = 0;
+  for (int64_t e = 0; e < n_elems; ++e) {
+    uint32_t x = load_elem(base, e, w_bits);
+    for (int j = 0; j < w_bits; ++j) ones[j] += bit_of(x, j);
+  }
+  int64_t held[32];
+  for (int j = 0; j < w_bits; ++j) {
+    int64_t c1 = ones[j], c0 = n_elems - c1;
+    held[j] = c1 > c0 ? c1 : c0;
+  }
+
+  /* the candidate masks, largest first */
+  std::vector<uint32_t> cands;
+  uint32_t cur = mask0;
+  cands.push_back(cur);
+  while (cur != 0) {
+    int64_t fewest = -1;
+    for (int j = 0; j < w_bits; ++j)
+      if (bit_of(cur, j) && (fewest < 0 || held[j] < fewest)) fewest = held[j];
+    for (int j = 0; j < w_bits; ++j)
+      if (bit_of(cur, j) && held[j] == fewest) cur &= ~(1u << j);
+    cands.push_back(cur);
+  }
+
+  /* score each by compressing every row with it */
+  const int64_t raw_bytes = row_elems * (w_bits / 8);
+  const int64_t sb = ibpo_slot_bytes(row_elems, w_bits);
+  std::vector<unsigned char> slots((size_t)(n_rows * sb));
+  std::vector<uint32_t> bitmask((size_t)((n_rows + 31) / 32));
+  std::vector<uint32_t> row_bits((size_t)n_rows);
+  std::vector<int64_t> total(cands.size());
+  for (size_t k = 0; k < cands.size(); ++k) {
+    uint32_t mk = cands[k], bk = bitval0 & cands[k];
+    if (ibpo_compress(rows, n_rows, row_elems, w_bits, block_elems, mk, bk, slots.data(), sb,
+                      bitmask.data(), row_bits.data()) != IBPO_OK)
+      return IBPO_BAD_ARG;
+    int64_t sum = 0;
+    for (int64_t r = 0; r < n_rows; ++r) {
+      int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);
+      sum += compressed ? 4 * (((int64_t)row_bits[r] + 31) / 32) : raw_bytes;
+    }
+    total[k] = sum;
+  }
+  size_t best = 0;
+  for (size_t k = 1; k < cands.size(); ++k)
+    if (total[k] < total[best]) best = k; /* strict: ties keep the larger mask */
+
+  *mask_out = cands[best];
+  *bitval_out = bitval0 & cands[best];
+  if (cand_mask && cand_bytes) {
+    for (int k = 0; k < 33; ++k) {
+      cand_mask[k] = k < (int)cands.size() ? cands[k] : 0u;
+      cand_bytes[k] = k < (int)cands.size() ? total[k] : -1;
+    }
+  }
+  if (n_cand) *n_cand = (int)cands.size();
+  return IBPO_OK;
 }

@@ -55,6 +55,24 @@ extern "C" {
 int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, double T,
                     uint32_t *mask_out, uint32_t *bitval_out);
 
+/* Saving-aware mask selection (a variant of preprocessing that trades some
+ * invariant positions for more matching blocks; the threshold rule alone can keep
+ * a position whose rare exceptions spoil most blocks).
+ * Candidates: candidate 0 is the threshold rule's mask M0 (ibpo_build_meta over
+ * all n_rows*row_elems elements); candidate k+1 is candidate k without the
+ * positions, among those it still holds, whose majority value is held by the
+ * fewest elements (positions with equal counts leave together); the last
+ * candidate is the empty mask. Each candidate's bitval is M0's bitval restricted
+ * to it. Each candidate is scored by compressing all rows with it (ibpo_compress)
+ * and summing the bytes each row occupies (4*ceil(bits/32) when compressed, else
+ * the raw row); the smallest sum wins, ties going to the lower k (the larger mask).
+ * Writes the winner to mask_out/bitval_out; when cand_mask/cand_bytes are not
+ * null (33 entries each) writes every candidate's mask and byte total and
+ * *n_cand = number of candidates (1..w+1). Returns IBPO_OK or IBPO_BAD_ARG. */
+int ibpo_select_meta(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits, double T,
+                     int64_t block_elems, uint32_t *mask_out, uint32_t *bitval_out,
+                     uint32_t *cand_mask, int64_t *cand_bytes, int *n_cand);
+
 /* Slot size for a row: raw bytes L*w/8 rounded up to a multiple of 16. */
 int64_t ibpo_slot_bytes(int64_t row_elems, int w_bits);
 

@@ -20,7 +20,11 @@ Compression for ML -- Extended", technical summary, core algorithm):
   * lossless round trip (the decoded row equals the original word for word) on
     +-0, denormals, +-Inf, NaN payloads and all-ones words;
   * decode of the hand-worked stream words (typed in from the golden file, not
-    produced by the oracle).
+    produced by the oracle);
+  * saving-aware mask selection: two hand-worked examples
+    (tests/golden/select_examples.txt) and a threshold sweep (every distinct mask
+    the threshold rule gives for thresholds at or above T, plus the empty mask,
+    scored with the numpy size formula) that must reach the same minimum.
 """
 from __future__ import annotations
 
@@ -279,6 +283,100 @@ def check_round_trip_specials(o):
                     assert np.array_equal(out, x[idx]), (w, B, T, hex(mk))
 
 
+def load_select_examples():
+    out, cur = {}, None
+    with open(os.path.join(GOLDEN, "select_examples.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "example":
+                cur = out.setdefault(vals[0], {})
+            elif key == "T":
+                cur["T"] = float(vals[0])
+            elif key == "block":
+                cur["block"] = int(vals[0])
+            elif key == "candidates":
+                cur["candidates"] = [(int(v.split(":")[0], 16), int(v.split(":")[1]))
+                                     for v in vals]
+            elif key == "choice":
+                cur["choice"] = (int(vals[0], 16), int(vals[1], 16))
+    return out
+
+
+def fp32_bit26_rows() -> np.ndarray:
+    """The formula of the fp32_bit26 example: one bit-26 exception per row."""
+    r = np.arange(8, dtype=np.uint32)[:, None]
+    e = np.arange(32, dtype=np.uint32)[None, :]
+    return (np.uint32(0x38000000) | np.where(e == r, np.uint32(1 << 26), np.uint32(0))
+            | (e << np.uint32(3)) | (r & np.uint32(7))).astype(np.uint32)
+
+
+def check_select_examples(o):
+    ex = load_select_examples()
+    rows = {"fp16_hand": load_hand_example()["rows"], "fp32_bit26": fp32_bit26_rows()}
+    for name, d in ex.items():
+        mask, bitval, cands = o.select_meta(rows[name], d["T"], d["block"])
+        assert cands == d["candidates"], (name, [(hex(m), b) for m, b in cands])
+        assert (mask, bitval) == d["choice"], (name, hex(mask), hex(bitval))
+
+
+def stored_total(rows: np.ndarray, B: int, mask: int, bitval: int) -> int:
+    """Bytes the rows take under (mask, bitval), from the size formula alone."""
+    n, L = rows.shape
+    w = 8 * rows.dtype.itemsize
+    m = w - bin(mask).count("1")
+    bits = (1 + np.where(block_matches(rows, B, mask, bitval), B * m, B * w)).sum(axis=1)
+    words = (bits + 31) // 32
+    raw = L * w // 8
+    return int(np.where(4 * words < raw, 4 * words, raw).sum())
+
+
+def threshold_family(rows: np.ndarray, T: float):
+    """Every distinct mask of the threshold rule at thresholds >= T (counts are
+    integers, so thresholds halfway between them reach every mask), plus the empty
+    mask; each with bitval = the majority values of its positions."""
+    N = rows.size
+    masks = {}
+    for T2 in [T] + [(c - 0.5) / N for c in range(1, N + 1) if (c - 0.5) / N >= T]:
+        mk, bv = brute_meta(rows, T2)
+        masks[mk] = bv
+    masks.setdefault(0, 0)
+    return masks
+
+
+def check_select_threshold_sweep(o):
+    g = np.random.default_rng(4242)
+    cases = []
+    for trial in range(24):
+        dt, w = ((np.uint16, 16), (np.uint32, 32))[trial % 2]
+        B = (1, 2, 4, 8)[trial % 4]
+        n, L = int(g.integers(1, 9)), B * int(g.integers(1, 5))
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 4)) - 1))
+        flip = g.random(size=(n, L)) < (0.0, 0.03, 0.1, 0.5)[trial % 4 if trial < 20 else 3]
+        const = np.uint64(int(g.integers(0, 1 << w)))
+        x = np.where(flip, base, (base & ~hi) | (const & hi)).astype(dt)
+        # one exception per row in a high position that the threshold rule keeps
+        if trial % 3 == 0:
+            x[:, 0] ^= dt(1 << (w - 3))
+        cases.append((x, float((0.5, 0.75, 0.9)[trial % 3]), B))
+    for x, T, B in cases:
+        fam = threshold_family(x, T)
+        scored = sorted(((stored_total(x, B, mk, bv), -bin(mk).count("1"), mk, bv)
+                         for mk, bv in fam.items()))
+        best_bytes, _, best_mask, best_bitval = scored[0]
+        mask, bitval, cands = o.select_meta(x, T, B)
+        assert (mask, bitval) == (best_mask, best_bitval), (hex(mask), hex(best_mask), T, B)
+        assert sorted(m for m, _ in cands) == sorted(fam), ([hex(m) for m, _ in cands],
+                                                            [hex(m) for m in fam])
+        for mk, b in cands:
+            assert b == stored_total(x, B, mk, fam[mk])
+        assert dict(cands)[mask] == best_bytes
+
+
 ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_meta_closed_forms, check_size_formula, check_stream_layout,
-              check_round_trip_specials]
+              check_round_trip_specials, check_select_examples,
+              check_select_threshold_sweep]

@@ -91,6 +91,16 @@ PLANTED = [
     ("bitval not reinserted", "x |= (uint32_t)bit_of(bitval, j) << j;", "x |= 0;"),
     ("bitval stores the minority value", "bitval |= (uint32_t)v << j;",
      "bitval |= (uint32_t)(1 - v) << j;"),
+    ("selection ties go to the smaller mask", "if (total[k] < total[best]) best = k;",
+     "if (total[k] <= total[best]) best = k;"),
+    ("selection drops the most-held positions first",
+     "if (bit_of(cur, j) && (fewest < 0 || held[j] < fewest)) fewest = held[j];",
+     "if (bit_of(cur, j) && (fewest < 0 || held[j] > fewest)) fewest = held[j];"),
+    ("selection drops tied positions one at a time",
+     "if (bit_of(cur, j) && held[j] == fewest) cur &= ~(1u << j);",
+     "if (bit_of(cur, j) && held[j] == fewest) { cur &= ~(1u << j); break; }"),
+    ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
+     "*bitval_out = bitval0;"),
 ]
 
 
