@@ -130,6 +130,41 @@ int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtyp
 int ibp_build_meta_noalloc(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
                            double T, uint32_t block_elems, ibp_meta *d_meta, ibp_stream_t s);
 
+/* Saving-aware metadata: a variant of preprocessing (the paper has no counterpart;
+ * it follows from "Core algorithm": the threshold rule picks positions one by one,
+ * but compression strips a block's invariant bits only when every one of them
+ * holds in every element, so a position whose few exceptions fall in many blocks
+ * can cost more than it saves).
+ * Candidates: candidate 0 is the mask ibp_build_meta gives for T (M0); candidate
+ * k+1 is candidate k without every position whose majority value is held by the
+ * fewest elements among the positions candidate k still has (equal counts leave
+ * together); the last candidate is the empty mask, so there are 1 to w+1 of them.
+ * Each candidate's bitval is M0's bitval restricted to it. Each candidate is scored
+ * by the bytes rows [0, n_rows) take when compressed with it: the sum over rows of
+ * 4*ceil(bits/32) for a row stored compressed and the raw row bytes otherwise.
+ * *d_meta receives the lowest-scoring candidate, ties going to the lower k (the
+ * larger mask). With T <= 0.5 every position is in M0 and the candidates are all
+ * the masks the threshold rule gives for any threshold, plus the empty mask.
+ * d_candidates (nullable; device memory of IBP_MAX_MASK_CANDIDATES entries): entry
+ * k receives candidate k and its score; entries past the last candidate receive
+ * mask = bitval = 0 and stored_bytes = -1.
+ * d_scratch: ibp_meta_select_scratch_bytes() bytes of device memory, overwritten.
+ * Reads the rows twice (counting, then scoring); same argument checks and codes as
+ * ibp_build_meta. */
+#define IBP_MAX_MASK_CANDIDATES 33
+
+typedef struct {
+  uint32_t mask;
+  uint32_t bitval;
+  int64_t stored_bytes; /* score of this candidate, or -1 for an unused entry */
+} ibp_mask_candidate;   /* 16 bytes */
+
+int ibp_meta_select_scratch_bytes(size_t *bytes);
+
+int ibp_build_meta_select(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                          double T, uint32_t block_elems, ibp_meta *d_meta,
+                          ibp_mask_candidate *d_candidates, void *d_scratch, ibp_stream_t s);
+
 /* Compression ("Core algorithm", compression; "System integration").
  * Encodes rows [0, n_rows) into their slots with the mask/bitval in *d_meta, whose
  * dtype and block_elems must equal the ones passed. Compressed rows hold their

@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 
 import torch
 
@@ -44,7 +45,9 @@ class Stats(ctypes.Structure):
 
 SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp_build_meta",
            "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read",
-           "ibp_build_meta_noalloc")
+           "ibp_build_meta_noalloc", "ibp_meta_select_scratch_bytes", "ibp_build_meta_select")
+
+MAX_MASK_CANDIDATES = 33
 
 
 def library_path() -> str:
@@ -73,6 +76,8 @@ def load() -> ctypes.CDLL:
     lib.ibp_query.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.ibp_probe_read.argtypes = [vp, i64, vp, vp]
     lib.ibp_build_meta_noalloc.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp]
+    lib.ibp_meta_select_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+    lib.ibp_build_meta_select.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
     for name in SYMBOLS[1:]:
         getattr(lib, name).restype = i32
     _lib = lib
@@ -144,6 +149,36 @@ def build_meta_noalloc(rows: torch.Tensor, T: float, block_elems: int, meta: tor
     _check(load().ibp_build_meta_noalloc(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
                                          int(block_elems), _ptr(meta), _stream(stream)),
            "ibp_build_meta_noalloc")
+
+
+def meta_select_scratch_bytes() -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().ibp_meta_select_scratch_bytes(ctypes.byref(out)),
+           "ibp_meta_select_scratch_bytes")
+    return out.value
+
+
+def build_meta_select(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Tensor,
+                      scratch: torch.Tensor, candidates: torch.Tensor | None = None,
+                      dtype: int | None = None, stream=None) -> None:
+    """ibp_build_meta_select: the saving-aware mask (the cheapest of the threshold
+    mask and its nested reductions) into ``meta``; ``candidates`` (optional,
+    MAX_MASK_CANDIDATES x 16 device bytes) receives every candidate and its score."""
+    n, L = _rows_shape(rows)
+    _check(load().ibp_build_meta_select(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
+                                        int(block_elems), _ptr(meta), _ptr(candidates),
+                                        _ptr(scratch), _stream(stream)), "ibp_build_meta_select")
+
+
+def read_candidates(candidates: torch.Tensor) -> list[tuple[int, int, int]]:
+    """(mask, bitval, stored_bytes) of every used entry of a candidate table."""
+    raw = candidates.detach().to("cpu").contiguous().view(torch.uint8).numpy().tobytes()
+    out = []
+    for k in range(MAX_MASK_CANDIDATES):
+        mask, bitval, stored = struct.unpack_from("<IIq", raw, 16 * k)
+        if stored >= 0:
+            out.append((mask, bitval, stored))
+    return out
 
 
 def compress(rows: torch.Tensor, block_elems: int, meta: torch.Tensor, slots: torch.Tensor,

@@ -205,6 +205,26 @@ int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtyp
                            reinterpret_cast<cudaStream_t>(s));
 }
 
+int ibp_meta_select_scratch_bytes(size_t *bytes) {
+  if (!bytes) return IBP_ERR_ARG;
+  *bytes = select_scratch_bytes();
+  return IBP_OK;
+}
+
+int ibp_build_meta_select(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                          double T, uint32_t block_elems, ibp_meta *d_meta,
+                          ibp_mask_candidate *d_candidates, void *d_scratch, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_rows <= 0 || !(T >= 0.0 && T <= 1.0)) return IBP_ERR_ARG;
+  if (!pointer_ok(rows, Where::device_or_host, 16) || !pointer_ok(d_meta, Where::device_only, 16) ||
+      !pointer_ok(d_scratch, Where::device_only, 16) ||
+      (d_candidates && !pointer_ok(d_candidates, Where::device_only, 16)))
+    return IBP_ERR_ARG;
+  return launch_build_meta_select(rows, n_rows, g, (uint32_t)dtype, T, d_meta, d_candidates,
+                                  d_scratch, reinterpret_cast<cudaStream_t>(s));
+}
+
 int ibp_compress(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
                  uint32_t block_elems, const ibp_meta *d_meta, void *slots, int64_t slot_bytes,
                  uint32_t *d_row_bitmask, uint32_t *d_row_bits, int32_t *d_status,

@@ -33,6 +33,14 @@ int device_info(DeviceInfo *out);
 
 int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, uint32_t block_elems,
                       int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s);
+// The positional population count of the preprocessing stage: clears the 32
+// 64-bit counters, then adds every n_words 32-bit word into them.
+int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *counters,
+                      cudaStream_t s);
+int launch_build_meta_select(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
+                             double T, ibp_meta *d_meta, ibp_mask_candidate *d_candidates,
+                             void *d_scratch, cudaStream_t s);
+size_t select_scratch_bytes();
 int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                     const ibp_meta *d_meta, void *slots, int64_t slot_bytes, uint32_t *d_bitmask,
                     uint32_t *d_row_bits, int32_t *d_status, cudaStream_t s);

@@ -151,11 +151,10 @@ __global__ void meta_finalize_kernel(const unsigned long long *counters, int64_t
 
 }  // namespace
 
-int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, uint32_t block_elems,
-                      int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s) {
+int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *counters,
+                      cudaStream_t s) {
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
-  unsigned long long *counters = static_cast<unsigned long long *>(d_scratch);
   if (cudaMemsetAsync(counters, 0, 32 * sizeof(unsigned long long), s) != cudaSuccess)
     return IBP_ERR_CUDA;
   const int64_t nvec = n_words / 4;
@@ -166,7 +165,13 @@ int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, ui
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * 8);
   meta_count_kernel<<<grid, META_THREADS, 0, s>>>(static_cast<const uint4 *>(rows), nvec, tail,
                                                   ntail, counters);
-  if (cudaGetLastError() != cudaSuccess) return IBP_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+}
+
+int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, uint32_t block_elems,
+                      int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s) {
+  unsigned long long *counters = static_cast<unsigned long long *>(d_scratch);
+  if (int rc = launch_meta_count(rows, n_words, counters, s)) return rc;
   meta_finalize_kernel<<<1, 32, 0, s>>>(counters, n_elems, width_of(dtype), T, (uint32_t)dtype,
                                         block_elems, d_meta);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;

@@ -39,6 +39,7 @@ def test_size_queries(lib):
     assert ibp.slot_bytes(11008, ibp.BF16) == 22016
     assert ibp.slot_bytes(33, ibp.FP16) == 80
     assert ibp.meta_scratch_bytes() == 256
+    assert ibp.meta_select_scratch_bytes() == 1024
     with pytest.raises(ibp.IBPError):
         ibp.slot_bytes(0, ibp.FP32)
     with pytest.raises(ibp.IBPError) as e:
@@ -68,4 +69,14 @@ def test_argument_errors_before_cuda(lib):
     assert lib.ibp_decompress_gather(None, 512, 10, 128, ibp.FP32, 32, None, None, None, 4, None,
                                      None, None) == ibp.ERR_ARG
     assert lib.ibp_probe_read(None, 17, None, None) == ibp.ERR_ARG
+    assert lib.ibp_build_meta_select(None, 10, 128, ibp.FP32, 0.9, 32, None, None, None,
+                                     None) == ibp.ERR_ARG
+    assert lib.ibp_build_meta_select(vp(16), 0, 128, ibp.FP32, 0.9, 32, vp(16), None, vp(16),
+                                     None) == ibp.ERR_ARG
+    assert lib.ibp_build_meta_select(vp(16), 10, 128, ibp.FP32, -0.1, 32, vp(16), None, vp(16),
+                                     None) == ibp.ERR_ARG
+    assert lib.ibp_build_meta_select(vp(16), 10, 128, ibp.FP32, 0.9, 16, vp(16), None, vp(16),
+                                     None) == ibp.ERR_UNSUPPORTED
+    assert lib.ibp_build_meta_select(vp(16), 10, 128, 5, 0.9, 32, vp(16), None, vp(16),
+                                     None) == ibp.ERR_DTYPE
     assert ibp.status_string(ibp.ERR_CORRUPT) == "corrupt slot header"
