@@ -298,6 +298,68 @@ class Store:
         return np.where(flags == 1, 4 * ((bits + 31) // 32), self.raw_bytes)
 
 
+class MaskSelect:
+    """The saving-aware mask selection of a store's rows (meta + candidate table)."""
+
+    def __init__(self, store):
+        self.store = store
+        dev = store.meta.device
+        self.meta = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.scratch = torch.empty(ibp.meta_select_scratch_bytes() // 4, dtype=torch.int32,
+                                   device=dev)
+        self.cand = torch.zeros((ibp.MAX_MASK_CANDIDATES, 4), dtype=torch.int32, device=dev)
+
+    def run(self):
+        st = self.store
+        ibp.build_meta_select(st.rows, st.T, st.B, self.meta, self.scratch, self.cand,
+                              dtype=st.dtype)
+
+
+def mask_select_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, table_raw,
+                    out_bytes, residency, link, hbm_peak):
+    """The saving-aware mask variant: time the selection over the table, recompress
+    the store with the chosen mask (into the same slot buffer; the legs of the
+    threshold mask are done by then) and time the same gather on it."""
+    sel = MaskSelect(store)
+    sel_t, _ = time_stage(sel.run, reps, flush)
+    torch.cuda.synchronize()
+    cands = ibp.read_candidates(sel.cand)
+    sstore = Store.__new__(Store)
+    sstore.__dict__.update(store.__dict__)
+    sstore.meta = sel.meta
+    sstore.bitmask = torch.zeros_like(store.bitmask)
+    sstore.row_bits = torch.zeros_like(store.row_bits)
+    sstore.status = torch.zeros_like(store.status)
+    sstore.compress()
+    torch.cuda.synchronize()
+    assert int(sstore.status.item()) == 0
+    st = sstore.stats()
+    stored = sstore.stored_per_row()
+    per_step, clk = timed_gather(sstore, batches, out, max(50, steps // 4), warmup, flush,
+                                 barrier)
+    ts = float(np.mean(per_step))
+    gathered = float(np.mean([stored[b.cpu().numpy()].sum() for b in batches]))
+    peak = link["h2d_memcpy_gbs"] if residency == "host" else hbm_peak
+    sel_frac = 2 * table_raw / sel_t / 1e9 / peak
+    mask = int(sel.meta[0].item()) & 0xFFFFFFFF
+    g = {"value": out_bytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3,
+         "stored_bytes_per_launch": gathered, "clocks": clk}
+    if residency == "host":
+        g["link_frac_algorithmic"] = gathered / ts / 1e9 / peak
+    else:
+        alg = wl["batch"] * 8 + gathered + out_bytes
+        g["hbm_frac"] = alg / ts / 1e9 / hbm_peak
+    return {
+        "mask": f"{mask:#010x}", "bitval": f"{int(sel.meta[1].item()) & 0xFFFFFFFF:#010x}",
+        "candidates": [{"mask": f"{m:#010x}", "stored_bytes": b} for m, _, b in cands],
+        "space_saving_pct": 100.0 * (1.0 - st.stored_bytes / st.raw_bytes),
+        "space_saving_gathered_pct": 100.0 * (1.0 - gathered / out_bytes),
+        "select": {"ms": sel_t * 1e3, "gbs_raw_in": table_raw / sel_t / 1e9,
+                   "frac": sel_frac, "bound": "host_link" if residency == "host" else "hbm",
+                   "reads_rows": 2},
+        "gather": g}
+
+
 def time_stage(fn, reps, flush=None):
     s = torch.cuda.current_stream()
     ts = []
@@ -643,6 +705,8 @@ def main():
             dstore.status = torch.zeros_like(store.status)
             mt, _ = time_stage(dstore.build_meta, reps, flush)
             ct, _ = time_stage(dstore.compress, reps, flush)
+            sel_d = MaskSelect(dstore)
+            sdt, _ = time_stage(sel_d.run, reps, flush)
             torch.cuda.synchronize()
             same = bool(torch.equal(dstore.bitmask, store.bitmask))
             comp_bytes = table_raw + float(stored.sum())
@@ -651,9 +715,15 @@ def main():
                                "frac_of_hbm": table_raw / mt / 1e9 / hbm_peak},
                 "compress": {"gbs_raw_in": table_raw / ct / 1e9, "ms": ct * 1e3,
                              "frac_of_hbm": comp_bytes / ct / 1e9 / hbm_peak,
-                             "same_bitmask_as_host_run": same}}
-            del dstore
+                             "same_bitmask_as_host_run": same},
+                "build_meta_select": {"gbs_raw_in": table_raw / sdt / 1e9, "ms": sdt * 1e3,
+                                      "frac_of_hbm": 2 * table_raw / sdt / 1e9 / hbm_peak,
+                                      "reads_rows": 2}}
+            del dstore, sel_d
             torch.cuda.empty_cache()
+        extra["mask_select"] = mask_select_leg(store, wl, batches, out, steps, warmup, flush,
+                                               barrier, reps, table_raw, out_bytes, residency,
+                                               link, hbm_peak)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,

@@ -63,6 +63,11 @@ class Oracle:
         lib.ibpo_select_meta.argtypes = [vp, i64, i64, i32, dbl, i64, ctypes.POINTER(u32),
                                          ctypes.POINTER(u32), vp, vp, ctypes.POINTER(i32)]
         lib.ibpo_select_meta.restype = i32
+        lib.ibpo_pack.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, vp, vp]
+        lib.ibpo_pack.restype = i32
+        lib.ibpo_decompress_gather_packed.argtypes = [vp, vp, i64, i64, i32, i64, vp, u32, u32,
+                                                      vp, i64, vp]
+        lib.ibpo_decompress_gather_packed.restype = i32
         self.lib = lib
         self.path = path
 
@@ -79,6 +84,50 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"oracle build_meta rejected its arguments ({rc})")
         return mask.value, bitval.value
+
+    def pack(self, slots: np.ndarray, row_elems: int, dtype, bitmask: np.ndarray,
+             row_bits: np.ndarray, sel: np.ndarray | None = None):
+        """Packed store of rows ``sel`` (all rows if None) of a 2-D slotted store.
+        Returns (offsets i64[n_sel+1], packed u8[total], bitmask u32, row_bits u32)."""
+        s = np.ascontiguousarray(slots)
+        n = s.shape[0]
+        w = 8 * np.dtype(dtype).itemsize
+        bm = np.ascontiguousarray(bitmask, dtype=np.uint32)
+        rb = np.ascontiguousarray(row_bits, dtype=np.uint32)
+        sl = None if sel is None else np.ascontiguousarray(sel, dtype=np.int64)
+        n_sel = n if sl is None else sl.size
+        offsets = np.zeros(n_sel + 1, dtype=np.int64)
+        rc = self.lib.ibpo_pack(_ptr(s), s.shape[1], n, row_elems, w, _ptr(bm), _ptr(rb), _ptr(sl),
+                                n_sel, _ptr(offsets), None, None, None)
+        if rc != OK:
+            raise ValueError(f"oracle pack rejected its arguments ({rc})")
+        packed = np.zeros(int(offsets[-1]), dtype=np.uint8)
+        pbm = np.zeros((n_sel + 31) // 32, dtype=np.uint32)
+        prb = np.zeros(n_sel, dtype=np.uint32)
+        rc = self.lib.ibpo_pack(_ptr(s), s.shape[1], n, row_elems, w, _ptr(bm), _ptr(rb), _ptr(sl),
+                                n_sel, _ptr(offsets), _ptr(packed), _ptr(pbm), _ptr(prb))
+        if rc != OK:
+            raise ValueError(f"oracle pack rejected its arguments ({rc})")
+        return offsets, packed, pbm, prb
+
+    def decompress_gather_packed(self, packed: np.ndarray, offsets: np.ndarray, row_elems: int,
+                                 dtype, block_elems: int, bitmask: np.ndarray, mask: int,
+                                 bitval: int, idx: np.ndarray, out: np.ndarray | None = None):
+        """Rebuild rows ``idx`` of a packed store. Returns (out, status)."""
+        dt = np.dtype(dtype)
+        w = 8 * dt.itemsize
+        p = np.ascontiguousarray(packed, dtype=np.uint8)
+        off = np.ascontiguousarray(offsets, dtype=np.int64)
+        ix = np.ascontiguousarray(idx, dtype=np.int64)
+        bm = np.ascontiguousarray(bitmask, dtype=np.uint32)
+        if out is None:
+            out = np.zeros((ix.size, row_elems), dtype=dt)
+        rc = self.lib.ibpo_decompress_gather_packed(_ptr(p), _ptr(off), off.size - 1, row_elems, w,
+                                                    int(block_elems), _ptr(bm), int(mask),
+                                                    int(bitval), _ptr(ix), ix.size, _ptr(out))
+        if rc == BAD_ARG:
+            raise ValueError("oracle decompress_gather_packed rejected its arguments")
+        return out, rc
 
     def select_meta(self, rows: np.ndarray, T: float, block_elems: int):
         """Saving-aware mask choice over a 2-D array of rows.
@@ -178,6 +227,16 @@ def slot_bytes(row_elems: int, w_bits: int) -> int:
 
 def build_meta(elems: np.ndarray, T: float) -> tuple[int, int]:
     return default().build_meta(elems, T)
+
+
+def pack(slots, row_elems, dtype, bitmask, row_bits, sel=None):
+    return default().pack(slots, row_elems, dtype, bitmask, row_bits, sel)
+
+
+def decompress_gather_packed(packed, offsets, row_elems, dtype, block_elems, bitmask, mask,
+                             bitval, idx, out=None):
+    return default().decompress_gather_packed(packed, offsets, row_elems, dtype, block_elems,
+                                              bitmask, mask, bitval, idx, out)
 
 
 def select_meta(rows: np.ndarray, T: float, block_elems: int):

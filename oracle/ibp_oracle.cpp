@@ -222,10 +222,41 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
   return IBPO_OK;
 }
 
-/* Decompression-gather: for each requested row read the participation bits,
-   walk the blocks in order (each block's start is the sum of the sizes of the
-   blocks before it), and rebuild every element by putting the invariant bits
-   back in place. */
+/* Decompression of one row from its stored bytes (slot or packed entry, `avail`
+   bytes of it readable): read the participation bits, walk the blocks in order
+   (each block's start is the sum of the sizes of the blocks before it), and
+   rebuild every element by putting the invariant bits back in place. Returns
+   IBPO_OK, or IBPO_CORRUPT (orow untouched) when the stream the participation bits
+   describe would not have been stored compressed or does not fit `avail`. */
+static int decode_row(const unsigned char *slot, int64_t avail, int compressed, int64_t row_elems,
+                      int w_bits, int64_t block_elems, uint32_t mask, uint32_t bitval,
+                      unsigned char *orow) {
+  const int64_t raw_bytes = row_elems * (w_bits / 8);
+  const int64_t nb = row_elems / block_elems;
+  const int m = w_bits - popcount_w(mask, w_bits);
+  if (!compressed) {
+    if (avail < raw_bytes) return IBPO_CORRUPT;
+    for (int64_t k = 0; k < raw_bytes; ++k) orow[k] = slot[k];
+    return IBPO_OK;
+  }
+  if (avail * 8 < nb) return IBPO_CORRUPT;
+  int64_t bits = 0;
+  for (int64_t b = 0; b < nb; ++b) bits += 1 + block_elems * (get_bit(slot, b) ? m : w_bits);
+  if (4 * ((bits + 31) / 32) >= raw_bytes || 4 * ((bits + 31) / 32) > avail) return IBPO_CORRUPT;
+  int64_t pos = nb; /* first payload bit */
+  for (int64_t b = 0; b < nb; ++b) {
+    int match = get_bit(slot, b);
+    for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+      uint32_t x;
+      if (match) x = reinsert(get_field(slot, &pos, m), mask, bitval, w_bits);
+      else x = get_field(slot, &pos, w_bits);
+      store_elem(orow, e, w_bits, x);
+    }
+  }
+  return IBPO_OK;
+}
+
+/* Decompression-gather: rebuild each requested row from its slot. */
 extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
                                       int64_t row_elems, int w_bits, int64_t block_elems,
                                       const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
@@ -240,41 +271,83 @@ extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int
   const unsigned char *in = (const unsigned char *)slots;
   unsigned char *dst = (unsigned char *)out;
   const int64_t raw_bytes = row_elems * (w_bits / 8);
-  const int64_t nb = row_elems / block_elems;
-  const int m = w_bits - popcount_w(mask, w_bits);
   int status = IBPO_OK;
-
   for (int64_t i = 0; i < n_idx; ++i) {
     int64_t r = idx[i];
-    unsigned char *orow = dst + i * raw_bytes;
     if (r < 0 || r >= n_rows) {
       if (status == IBPO_OK) status = IBPO_BAD_INDEX;
       continue;
     }
-    const unsigned char *slot = in + r * slot_bytes;
     int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);
-    if (!compressed) {
-      for (int64_t k = 0; k < raw_bytes; ++k) orow[k] = slot[k];
+    int rc = decode_row(in + r * slot_bytes, slot_bytes, compressed, row_elems, w_bits,
+                        block_elems, mask, bitval, dst + i * raw_bytes);
+    if (rc != IBPO_OK && status == IBPO_OK) status = rc;
+  }
+  return status;
+}
+
+/* Packed store: each selected row's used bytes, rounded up to 16, end to end. */
+extern "C" int ibpo_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems,
+                         int w_bits, const uint32_t *bitmask, const uint32_t *row_bits,
+                         const int64_t *sel, int64_t n_sel, int64_t *offsets, void *packed,
+                         uint32_t *pack_bitmask, uint32_t *pack_row_bits) {
+  if (!slots || !bitmask || !row_bits || !offsets || n_rows < 0 || n_sel < 0 || row_elems <= 0 ||
+      !valid_width(w_bits) || slot_bytes < ibpo_slot_bytes(row_elems, w_bits) ||
+      (!sel && n_sel > n_rows))
+    return IBPO_BAD_ARG;
+  const unsigned char *in = (const unsigned char *)slots;
+  unsigned char *out = (unsigned char *)packed;
+  const int64_t raw_bytes = row_elems * (w_bits / 8);
+  if (packed && pack_bitmask)
+    for (int64_t q = 0; q < (n_sel + 31) / 32; ++q) pack_bitmask[q] = 0;
+  int64_t at = 0;
+  for (int64_t i = 0; i < n_sel; ++i) {
+    int64_t r = sel ? sel[i] : i;
+    if (r < 0 || r >= n_rows) return IBPO_BAD_INDEX;
+    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);
+    int64_t used = compressed ? 4 * (((int64_t)row_bits[r] + 31) / 32) : raw_bytes;
+    int64_t len = (used + 15) / 16 * 16;
+    offsets[i] = at;
+    if (packed) {
+      for (int64_t k = 0; k < len; ++k) out[at + k] = in[r * slot_bytes + k];
+      if (pack_bitmask && compressed) pack_bitmask[i / 32] |= 1u << (i % 32);
+      if (pack_row_bits) pack_row_bits[i] = row_bits[r];
+    }
+    at += len;
+  }
+  offsets[n_sel] = at;
+  return IBPO_OK;
+}
+
+/* Decompression-gather from a packed store. */
+extern "C" int ibpo_decompress_gather_packed(const void *packed, const int64_t *offsets,
+                                             int64_t n_rows, int64_t row_elems, int w_bits,
+                                             int64_t block_elems, const uint32_t *bitmask,
+                                             uint32_t mask, uint32_t bitval, const int64_t *idx,
+                                             int64_t n_idx, void *out) {
+  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
+      row_elems % block_elems != 0)
+    return IBPO_BAD_ARG;
+  if (n_idx == 0) return IBPO_OK;
+  if (!packed || !offsets || !bitmask || !idx || !out) return IBPO_BAD_ARG;
+  mask &= width_mask(w_bits);
+  bitval &= mask;
+  const unsigned char *in = (const unsigned char *)packed;
+  unsigned char *dst = (unsigned char *)out;
+  const int64_t raw_bytes = row_elems * (w_bits / 8);
+  int status = IBPO_OK;
+  for (int64_t i = 0; i < n_idx; ++i) {
+    int64_t r = idx[i];
+    if (r < 0 || r >= n_rows) {
+      if (status == IBPO_OK) status = IBPO_BAD_INDEX;
       continue;
     }
-    /* the stream length the participation bits describe must fit the rule the
-       compressor used, else the slot is corrupt */
-    int64_t bits = 0;
-    for (int64_t b = 0; b < nb; ++b) bits += 1 + block_elems * (get_bit(slot, b) ? m : w_bits);
-    if (4 * ((bits + 31) / 32) >= raw_bytes) {
-      if (status == IBPO_OK) status = IBPO_CORRUPT;
-      continue;
-    }
-    int64_t pos = nb; /* first payload bit */
-    for (int64_t b = 0; b < nb; ++b) {
-      int match = get_bit(slot, b);
-      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
-        uint32_t x;
-        if (match) x = reinsert(get_field(slot, &pos, m), mask, bitval, w_bits);
-        else x = get_field(slot, &pos, w_bits);
-        store_elem(orow, e, w_bits, x);
-      }
-    }
+    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);
+    int64_t avail = offsets[r + 1] - offsets[r];
+    int rc = avail < 0 ? IBPO_CORRUPT
+                       : decode_row(in + offsets[r], avail, compressed, row_elems, w_bits,
+                                    block_elems, mask, bitval, dst + i * raw_bytes);
+    if (rc != IBPO_OK && status == IBPO_OK) status = rc;
   }
   return status;
 }

@@ -55,6 +55,28 @@ extern "C" {
 int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, double T,
                     uint32_t *mask_out, uint32_t *bitval_out);
 
+/* Packed store (technical summary, "System integration": the compressed GPU
+ * cache that raises the cache's effective capacity). Rows sel[0..n_sel) of a
+ * slotted store (sel == NULL: rows 0..n_sel) are laid end to end: entry i holds the
+ * used prefix of slot sel[i] (4*ceil(bits/32) bytes for a compressed row, the raw
+ * row otherwise) rounded up to a multiple of 16 bytes (bytes copied from the slot).
+ * offsets[i] = byte offset of entry i; offsets[n_sel] = total bytes (n_sel + 1
+ * entries). pack_bitmask bit i / pack_row_bits[i] = the source row's bitmask bit
+ * and bit count. packed may be NULL to compute only the offsets. Returns IBPO_OK,
+ * IBPO_BAD_ARG, or IBPO_BAD_INDEX for a selection outside [0, n_rows). */
+int ibpo_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems,
+              int w_bits, const uint32_t *bitmask, const uint32_t *row_bits, const int64_t *sel,
+              int64_t n_sel, int64_t *offsets, void *packed, uint32_t *pack_bitmask,
+              uint32_t *pack_row_bits);
+
+/* Decompress-gather from a packed store: as ibpo_decompress_gather, with row r's
+ * bytes at packed + offsets[r] and offsets[r+1] - offsets[r] of them; a row whose
+ * stream (or raw row) does not fit its entry is treated as corrupt. */
+int ibpo_decompress_gather_packed(const void *packed, const int64_t *offsets, int64_t n_rows,
+                                  int64_t row_elems, int w_bits, int64_t block_elems,
+                                  const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
+                                  const int64_t *idx, int64_t n_idx, void *out);
+
 /* Saving-aware mask selection (a variant of preprocessing that trades some
  * invariant positions for more matching blocks; the threshold rule alone can keep
  * a position whose rare exceptions spoil most blocks).

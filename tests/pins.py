@@ -24,7 +24,11 @@ Compression for ML -- Extended", technical summary, core algorithm):
   * saving-aware mask selection: two hand-worked examples
     (tests/golden/select_examples.txt) and a threshold sweep (every distinct mask
     the threshold rule gives for thresholds at or above T, plus the empty mask,
-    scored with the numpy size formula) that must reach the same minimum.
+    scored with the numpy size formula) that must reach the same minimum;
+  * packed store: the hand-worked rows packed in a chosen order (entry sizes and
+    bytes typed in from the golden file), offsets from the size formula on random
+    stores, lossless gathers from the packed bytes, and a truncated entry reported
+    as corrupt.
 """
 from __future__ import annotations
 
@@ -376,7 +380,68 @@ def check_select_threshold_sweep(o):
         assert dict(cands)[mask] == best_bytes
 
 
+def check_pack_hand_example(o):
+    """Rows 1, 0, 1 of the hand-worked example packed end to end: each entry is the
+    row's stream words (typed in from the golden file) padded to 16 bytes."""
+    d = load_hand_example()
+    n, L = d["rows"].shape
+    slots = np.zeros((n, 16), dtype=np.uint8)
+    for r, words in enumerate(d["streams"]):
+        slots[r, : 4 * len(words)] = np.array(words, dtype="<u4").view(np.uint8)
+    bitmask = np.array([d["bitmask"]], dtype=np.uint32)
+    row_bits = np.array(d["row_bits"], dtype=np.uint32)
+    sel = np.array([1, 0, 1], dtype=np.int64)
+    offsets, packed, pbm, prb = o.pack(slots, L, np.uint16, bitmask, row_bits, sel)
+    # row0: 50 bits -> 8 B -> 16; row1: 90 bits -> 12 B -> 16
+    assert offsets.tolist() == [0, 16, 32, 48]
+    for i, r in enumerate(sel):
+        words = d["streams"][r]
+        assert packed[16 * i: 16 * i + 4 * len(words)].view("<u4").tolist() == words
+    assert int(pbm[0]) == 0b111
+    assert prb.tolist() == [90, 50, 90]
+    out, rc = o.decompress_gather_packed(packed, offsets, L, np.uint16, d["block"], pbm,
+                                         d["mask"], d["bitval"], np.array([2, 1, 0, 1]))
+    assert rc == 0
+    assert np.array_equal(out, d["rows"][[1, 0, 1, 0]])
+
+
+def check_pack_round_trip(o):
+    g = np.random.default_rng(99)
+    for dt, w, B, L in ((np.uint32, 32, 32, 128), (np.uint16, 16, 64, 256), (np.uint32, 32, 4, 36)):
+        n = 120
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 2)) - 1))
+        flip = g.random(size=(n, L)) < 0.004
+        x = np.where(flip, base, (base & ~hi) | (np.uint64(0x3C1E3C1E) & hi)).astype(dt)
+        x[::7] = base[::7].astype(dt)  # some rows stored raw
+        mask, bitval = o.build_meta(x, 0.9)
+        slots, bitmask, row_bits = o.compress(x, B, mask, bitval)
+        sel = g.integers(0, n, size=200)
+        offsets, packed, pbm, prb = o.pack(slots, L, dt, bitmask, row_bits, sel)
+        # entry sizes from the size formula alone
+        m = w - bin(mask).count("1")
+        bits = (1 + np.where(block_matches(x, B, mask, bitval), B * m, B * w)).sum(axis=1)
+        words = (bits + 31) // 32
+        raw = L * w // 8
+        used = np.where(4 * words < raw, 4 * words, raw)
+        sizes = (used[sel] + 15) // 16 * 16
+        assert np.array_equal(np.diff(offsets), sizes)
+        assert offsets[0] == 0 and packed.size == sizes.sum()
+        idx = g.integers(0, sel.size, size=300)
+        out, rc = o.decompress_gather_packed(packed, offsets, L, dt, B, pbm, mask, bitval, idx)
+        assert rc == 0
+        assert np.array_equal(out, x[sel[idx]])
+        # an entry cut short is corrupt, and its output row is left alone
+        i = int(np.nonzero(np.diff(offsets) >= 32)[0][0])
+        bad = offsets.copy()
+        bad[i + 1] = bad[i] + 16 * ((int(used[sel[i]]) - 1) // 16)  # one 16-byte piece short
+        sentinel = np.full((1, L), 7, dtype=dt)
+        out, rc = o.decompress_gather_packed(packed, bad, L, dt, B, pbm, mask, bitval,
+                                             np.array([i]), out=sentinel.copy())
+        assert rc == -6 and np.array_equal(out, sentinel)
+
+
 ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_meta_closed_forms, check_size_formula, check_stream_layout,
               check_round_trip_specials, check_select_examples,
-              check_select_threshold_sweep]
+              check_select_threshold_sweep, check_pack_hand_example, check_pack_round_trip]

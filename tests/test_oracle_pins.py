@@ -99,6 +99,11 @@ PLANTED = [
     ("selection drops tied positions one at a time",
      "if (bit_of(cur, j) && held[j] == fewest) cur &= ~(1u << j);",
      "if (bit_of(cur, j) && held[j] == fewest) { cur &= ~(1u << j); break; }"),
+    ("packed entries rounded to 4 bytes", "int64_t len = (used + 15) / 16 * 16;",
+     "int64_t len = (used + 3) / 4 * 4;"),
+    ("packed entry length not checked",
+     "if (4 * ((bits + 31) / 32) >= raw_bytes || 4 * ((bits + 31) / 32) > avail) return IBPO_CORRUPT;",
+     "if (4 * ((bits + 31) / 32) >= raw_bytes) return IBPO_CORRUPT;"),
     ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
      "*bitval_out = bitval0;"),
 ]
