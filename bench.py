@@ -349,7 +349,7 @@ def mask_select_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps
     else:
         alg = wl["batch"] * 8 + gathered + out_bytes
         g["hbm_frac"] = alg / ts / 1e9 / hbm_peak
-    return {
+    return sstore, {
         "mask": f"{mask:#010x}", "bitval": f"{int(sel.meta[1].item()) & 0xFFFFFFFF:#010x}",
         "candidates": [{"mask": f"{m:#010x}", "stored_bytes": b} for m, _, b in cands],
         "space_saving_pct": 100.0 * (1.0 - st.stored_bytes / st.raw_bytes),
@@ -358,6 +358,66 @@ def mask_select_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps
                    "frac": sel_frac, "bound": "host_link" if residency == "host" else "hbm",
                    "reads_rows": 2},
         "gather": g}
+
+
+class PackedStore:
+    """A packed store (rows end to end) of every row of a slotted store."""
+
+    def __init__(self, store, where, dev):
+        self.n, self.L, self.dtype, self.B, self.meta = (store.n, store.L, store.dtype, store.B,
+                                                         store.meta)
+        self.offsets = torch.zeros(self.n + 1, dtype=torch.int64, device=dev)
+        scratch = torch.empty(ibp.pack_scratch_bytes(self.n) // 8, dtype=torch.int64,
+                              device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ibp.pack_offsets(store.bitmask, store.row_bits, self.n, self.L, self.dtype, self.offsets,
+                         scratch, status=self.status)
+        self.total = int(self.offsets[-1].item())
+        if where == "host":
+            self.packed = torch.empty(self.total, dtype=torch.uint8, pin_memory=True)
+        else:
+            self.packed = torch.empty(self.total, dtype=torch.uint8, device=dev)
+        self.bitmask = torch.zeros_like(store.bitmask)
+        self.row_bits = torch.zeros_like(store.row_bits)
+        self.pack_fn = lambda: ibp.pack(store.slots, self.n, self.L, self.dtype, store.bitmask,
+                                        store.row_bits, self.offsets, self.packed, self.bitmask,
+                                        self.row_bits, status=self.status)
+        self.pack_fn()
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0
+
+    def gather(self, idx, out, status=None):
+        ibp.decompress_gather_packed(self.packed, self.offsets, self.n, self.L, self.dtype,
+                                     self.B, self.bitmask, self.meta, idx, out, status)
+
+
+def packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier, table_raw, out_bytes,
+               link, hbm_peak, dev):
+    """The packed store ("cache-compression mode") of the table compressed with the
+    saving-aware mask, in pinned host memory and in HBM: the same gathers, reading
+    exactly each row's stored bytes (16-byte rounded)."""
+    res = {"store": "rows compressed with the saving-aware mask, packed end to end"}
+    for where in ("host", "device"):
+        ps = PackedStore(sstore, where, dev)
+        pt, _ = time_stage(ps.pack_fn, 3, flush)
+        per_step, clk = timed_gather(ps, batches, out, max(50, steps // 4), warmup, flush,
+                                     barrier)
+        ts = float(np.mean(per_step))
+        off = ps.offsets.cpu().numpy()
+        entry = np.diff(off)
+        gathered = float(np.mean([entry[b.cpu().numpy()].sum() for b in batches]))
+        r = {"value": out_bytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3,
+             "packed_bytes": ps.total, "capacity_gain": table_raw / ps.total,
+             "entry_bytes_per_launch": gathered, "pack_ms": pt * 1e3, "clocks": clk}
+        if where == "host":
+            r["link_frac_algorithmic"] = gathered / ts / 1e9 / link["h2d_memcpy_gbs"]
+        else:
+            alg = wl["batch"] * 24 + gathered + out_bytes  # index, two offsets, entry, row
+            r["hbm_frac"] = alg / ts / 1e9 / hbm_peak
+        res[where] = r
+        del ps
+        torch.cuda.empty_cache()
+    return res
 
 
 def time_stage(fn, reps, flush=None):
@@ -721,9 +781,12 @@ def main():
                                       "reads_rows": 2}}
             del dstore, sel_d
             torch.cuda.empty_cache()
-        extra["mask_select"] = mask_select_leg(store, wl, batches, out, steps, warmup, flush,
-                                               barrier, reps, table_raw, out_bytes, residency,
-                                               link, hbm_peak)
+        sstore, extra["mask_select"] = mask_select_leg(store, wl, batches, out, steps, warmup,
+                                                       flush, barrier, reps, table_raw,
+                                                       out_bytes, residency, link, hbm_peak)
+        extra["packed"] = packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier,
+                                     table_raw, out_bytes, link, hbm_peak, dev)
+        del sstore
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,

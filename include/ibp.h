@@ -191,6 +191,54 @@ int ibp_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
                           const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
                           ibp_stream_t s);
 
+/* Packed store ("System integration": compressing a GPU cache's rows raises its
+ * effective capacity; the paper has no layout for it, so this one is the
+ * library's). A slotted store keeps every row in a raw-size slot (a row can be
+ * rewritten in place); a packed store lays rows end to end and is read only:
+ *   entry i = the used prefix of slot d_sel[i] (d_sel null: row i) -- the
+ *     4*ceil(bits/32) stream bytes of a compressed row, or the raw row -- rounded up
+ *     to a multiple of 16 bytes, copied from the slot (stream padding included);
+ *   d_offsets[i] = byte offset of entry i; d_offsets[n_sel] = total bytes
+ *     (n_sel + 1 uint64 entries, device memory).
+ * Entry i of the packed store is row i: its bitmask bit and bit count are the
+ * source row's. Build it in three calls: ibp_pack_offsets, read d_offsets[n_sel]
+ * to size the buffer, ibp_pack. */
+
+/* Device scratch ibp_pack_offsets needs for n_sel entries (8 bytes per 4096). */
+int ibp_pack_scratch_bytes(int64_t n_sel, size_t *bytes);
+
+/* Entry offsets of a packed store of rows d_sel[0..n_sel) of a slotted store
+ * described by d_row_bitmask and d_row_bits (both as written by ibp_compress;
+ * row_bits is required here). A selection outside [0, n_rows) gets a 0-byte entry
+ * and IBP_ERR_INDEX in *d_status. Asynchronous on s. */
+int ibp_pack_offsets(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                     int64_t row_elems, int dtype, const int64_t *d_sel, int64_t n_sel,
+                     uint64_t *d_offsets, void *d_scratch, int32_t *d_status, ibp_stream_t s);
+
+/* Copy the entries into packed (device or registered host memory, packed_bytes
+ * long, 16-byte aligned) and write the packed store's bitmask d_pack_bitmask
+ * (ceil(n_sel/32) words, fully rewritten) and, when non-null, d_pack_row_bits
+ * (n_sel words). An entry whose offsets disagree with its row's size, are not
+ * 16-byte aligned or leave the buffer is skipped with IBP_ERR_CORRUPT in
+ * *d_status; a bad selection with IBP_ERR_INDEX. slots and packed must not
+ * overlap. */
+int ibp_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems, int dtype,
+             const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, const int64_t *d_sel,
+             int64_t n_sel, const uint64_t *d_offsets, void *packed, uint64_t packed_bytes,
+             uint32_t *d_pack_bitmask, uint32_t *d_pack_row_bits, int32_t *d_status,
+             ibp_stream_t s);
+
+/* ibp_decompress_gather on a packed store of n_rows entries: row r is read from
+ * packed + d_offsets[r], d_offsets[r+1] - d_offsets[r] bytes of it. Rows of at most
+ * 32 blocks are staged whole (exactly their entry) with no header round trip. An
+ * entry whose offsets are unaligned, decreasing or past packed_bytes, or too short
+ * for the row its header describes, is skipped with IBP_ERR_CORRUPT. */
+int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
+                                 const uint64_t *d_offsets, int64_t n_rows, int64_t row_elems,
+                                 int dtype, uint32_t block_elems, const uint32_t *d_row_bitmask,
+                                 const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
+                                 void *out, int32_t *d_status, ibp_stream_t s);
+
 /* Statistics of a store: reduces the bitmask and the per-row bit counts written
  * by ibp_compress into *d_stats (device memory), asynchronously on s. */
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,

@@ -45,7 +45,8 @@ class Stats(ctypes.Structure):
 
 SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp_build_meta",
            "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read",
-           "ibp_build_meta_noalloc", "ibp_meta_select_scratch_bytes", "ibp_build_meta_select")
+           "ibp_build_meta_noalloc", "ibp_meta_select_scratch_bytes", "ibp_build_meta_select",
+           "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -78,6 +79,12 @@ def load() -> ctypes.CDLL:
     lib.ibp_build_meta_noalloc.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp]
     lib.ibp_meta_select_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
     lib.ibp_build_meta_select.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
+    u64 = ctypes.c_uint64
+    lib.ibp_pack_scratch_bytes.argtypes = [i64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.ibp_pack_offsets.argtypes = [vp, vp, i64, i64, i32, vp, i64, vp, vp, vp, vp]
+    lib.ibp_pack.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, u64, vp, vp, vp, vp]
+    lib.ibp_decompress_gather_packed.argtypes = [vp, u64, vp, i64, i64, i32, u32, vp, vp, vp, i64,
+                                                 vp, vp, vp]
     for name in SYMBOLS[1:]:
         getattr(lib, name).restype = i32
     _lib = lib
@@ -207,6 +214,55 @@ def decompress_gather(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: i
                                         int(block_elems), _ptr(bitmask), _ptr(meta), _ptr(idx),
                                         idx.numel(), _ptr(out), _ptr(status), _stream(stream)),
            "ibp_decompress_gather")
+
+
+def pack_scratch_bytes(n_sel: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().ibp_pack_scratch_bytes(int(n_sel), ctypes.byref(out)), "ibp_pack_scratch_bytes")
+    return out.value
+
+
+def pack_offsets(bitmask: torch.Tensor, row_bits: torch.Tensor, n_rows: int, row_elems: int,
+                 dtype: int, offsets: torch.Tensor, scratch: torch.Tensor,
+                 sel: torch.Tensor | None = None, n_sel: int | None = None,
+                 status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_pack_offsets: entry offsets ([n_sel + 1] int64 on the device) of a packed
+    store of rows ``sel`` (all rows when None)."""
+    if sel is not None and sel.dtype != torch.int64:
+        raise ValueError("sel must be int64")
+    ns = int(n_sel) if n_sel is not None else (sel.numel() if sel is not None else int(n_rows))
+    _check(load().ibp_pack_offsets(_ptr(bitmask), _ptr(row_bits), int(n_rows), int(row_elems),
+                                   int(dtype), _ptr(sel), ns, _ptr(offsets), _ptr(scratch),
+                                   _ptr(status), _stream(stream)), "ibp_pack_offsets")
+
+
+def pack(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int, bitmask: torch.Tensor,
+         row_bits: torch.Tensor, offsets: torch.Tensor, packed: torch.Tensor,
+         pack_bitmask: torch.Tensor, pack_row_bits: torch.Tensor | None = None,
+         sel: torch.Tensor | None = None, n_sel: int | None = None,
+         status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_pack: copy the entries of a packed store into ``packed``."""
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(int(n_rows), 1)
+    ns = int(n_sel) if n_sel is not None else (sel.numel() if sel is not None else int(n_rows))
+    _check(load().ibp_pack(_ptr(slots), sb, int(n_rows), int(row_elems), int(dtype),
+                           _ptr(bitmask), _ptr(row_bits), _ptr(sel), ns, _ptr(offsets),
+                           _ptr(packed), packed.numel() * packed.element_size(),
+                           _ptr(pack_bitmask), _ptr(pack_row_bits), _ptr(status),
+                           _stream(stream)), "ibp_pack")
+
+
+def decompress_gather_packed(packed: torch.Tensor, offsets: torch.Tensor, n_rows: int,
+                             row_elems: int, dtype: int, block_elems: int, bitmask: torch.Tensor,
+                             meta: torch.Tensor, idx: torch.Tensor, out: torch.Tensor,
+                             status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_decompress_gather_packed: rows ``idx`` of a packed store into ``out``."""
+    if idx.dtype != torch.int64:
+        raise ValueError("idx must be int64")
+    _check(load().ibp_decompress_gather_packed(
+        _ptr(packed), packed.numel() * packed.element_size(), _ptr(offsets), int(n_rows),
+        int(row_elems), int(dtype), int(block_elems), _ptr(bitmask), _ptr(meta), _ptr(idx),
+        idx.numel(), _ptr(out), _ptr(status), _stream(stream)), "ibp_decompress_gather_packed")
 
 
 def query(bitmask: torch.Tensor, row_bits: torch.Tensor, n_rows: int, row_elems: int, dtype: int,

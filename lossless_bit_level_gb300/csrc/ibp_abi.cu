@@ -259,9 +259,79 @@ int ibp_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
       !pointer_ok(out, Where::device_only, 16) ||
       (d_status && !pointer_ok(d_status, Where::device_only, 4)))
     return IBP_ERR_ARG;
-  return launch_gather(slots, slot_bytes, n_rows, g, (uint32_t)dtype, d_row_bitmask, d_meta, d_idx,
-                       n_idx, out, d_status, in_device_memory(slots),
+  return launch_gather(slots, slot_bytes, nullptr, 0, n_rows, g, (uint32_t)dtype, d_row_bitmask,
+                       d_meta, d_idx, n_idx, out, d_status, in_device_memory(slots),
                        reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_pack_scratch_bytes(int64_t n_sel, size_t *bytes) {
+  if (!bytes || n_sel < 0) return IBP_ERR_ARG;
+  *bytes = pack_scratch_bytes(n_sel);
+  return IBP_OK;
+}
+
+int ibp_pack_offsets(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                     int64_t row_elems, int dtype, const int64_t *d_sel, int64_t n_sel,
+                     uint64_t *d_offsets, void *d_scratch, int32_t *d_status, ibp_stream_t s) {
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (n_rows < 0 || n_sel < 0 || row_elems <= 0 || row_elems > MAX_ROW_ELEMS) return IBP_ERR_ARG;
+  if (!d_sel && n_sel > n_rows) return IBP_ERR_ARG;
+  if (!pointer_ok(d_offsets, Where::device_only, 8) || !pointer_ok(d_scratch, Where::device_only, 8) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  if (n_sel > 0 && (!pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+                    !pointer_ok(d_row_bits, Where::device_only, 4) ||
+                    (d_sel && !pointer_ok(d_sel, Where::device_only, 8))))
+    return IBP_ERR_ARG;
+  return launch_pack_offsets(d_row_bitmask, d_row_bits, n_rows, row_elems * width_of(dtype) / 8,
+                             d_sel, n_sel, d_offsets, d_scratch, d_status,
+                             reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems, int dtype,
+             const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, const int64_t *d_sel,
+             int64_t n_sel, const uint64_t *d_offsets, void *packed, uint64_t packed_bytes,
+             uint32_t *d_pack_bitmask, uint32_t *d_pack_row_bits, int32_t *d_status,
+             ibp_stream_t s) {
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (n_rows < 0 || n_sel < 0 || row_elems <= 0 || row_elems > MAX_ROW_ELEMS) return IBP_ERR_ARG;
+  const int64_t raw_bytes = row_elems * width_of(dtype) / 8;
+  if (slot_bytes < (raw_bytes + 15) / 16 * 16 || slot_bytes % 16 != 0) return IBP_ERR_ARG;
+  if (!d_sel && n_sel > n_rows) return IBP_ERR_ARG;
+  if (n_sel == 0) return IBP_OK;
+  if (!pointer_ok(slots, Where::device_or_host, 16) || !pointer_ok(packed, Where::device_or_host, 16) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      !pointer_ok(d_row_bits, Where::device_only, 4) ||
+      (d_sel && !pointer_ok(d_sel, Where::device_only, 8)) ||
+      !pointer_ok(d_offsets, Where::device_only, 8) ||
+      !pointer_ok(d_pack_bitmask, Where::device_only, 4) ||
+      (d_pack_row_bits && !pointer_ok(d_pack_row_bits, Where::device_only, 4)) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_pack(slots, slot_bytes, n_rows, raw_bytes, d_row_bitmask, d_row_bits, d_sel, n_sel,
+                     d_offsets, packed, packed_bytes, d_pack_bitmask, d_pack_row_bits, d_status,
+                     reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
+                                 const uint64_t *d_offsets, int64_t n_rows, int64_t row_elems,
+                                 int dtype, uint32_t block_elems, const uint32_t *d_row_bitmask,
+                                 const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
+                                 void *out, int32_t *d_status, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_rows < 0 || n_idx < 0) return IBP_ERR_ARG;
+  if (n_idx == 0) return IBP_OK;
+  if (!pointer_ok(packed, Where::device_or_host, 16) ||
+      !pointer_ok(d_offsets, Where::device_only, 8) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      !pointer_ok(d_meta, Where::device_only, 16) || !pointer_ok(d_idx, Where::device_only, 8) ||
+      !pointer_ok(out, Where::device_only, 16) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_gather(packed, 0, d_offsets, packed_bytes, n_rows, g, (uint32_t)dtype,
+                       d_row_bitmask, d_meta, d_idx, n_idx, out, d_status,
+                       in_device_memory(packed), reinterpret_cast<cudaStream_t>(s));
 }
 
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,

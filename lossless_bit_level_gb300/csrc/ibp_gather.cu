@@ -23,6 +23,9 @@
 //      of the vector, its participation bit, popcount of the earlier bits ->
 //      bit position; funnel-shift each field out of shared memory, deposit it
 //      over the non-invariant positions of bitval; 128-bit store.
+// Packed stores (rows end to end, entry r at offsets[r], 16-byte aligned): the
+// row's entry length comes with its offset, so a one-segment row is staged whole,
+// exactly its stored bytes, without reading its header first.
 // The loop is software-pipelined two deep: the next unit's plan and staging are
 // issued before the current unit is decoded, and the index two units ahead is
 // prefetched, so header and body round trips overlap with decode.
@@ -39,8 +42,10 @@ constexpr int GATHER_NBUF = 2;          // staging buffers per team (units in fl
 constexpr int SEG_TARGET_BYTES = 4096;  // raw bytes per segment (at most 32 blocks)
 
 struct GatherArgs {
-  const uint8_t *slots;
-  int64_t slot_bytes;
+  const uint8_t *slots;      // slotted store, or the packed store's bytes
+  int64_t slot_bytes;        // slotted store only
+  const uint64_t *offsets;   // packed store: entry offsets [n_rows + 1]; null if slotted
+  uint64_t packed_bytes;     // packed store: size of the buffer at slots
   int64_t n_rows;
   const uint32_t *bitmask;
   const ibp_meta *meta;
@@ -88,8 +93,25 @@ __device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u) {
   return __ldg(a.idx + i);
 }
 
+// Offsets of a packed store's entry r (both 0 for a slotted store or a bad index).
+struct EntrySpan {
+  uint64_t o0, o1;
+};
+
+__device__ __forceinline__ EntrySpan load_span(const GatherArgs &a, int64_t r) {
+  EntrySpan e{0, 0};
+  if (a.offsets && r >= 0 && r < a.n_rows) {
+    e.o0 = __ldg(a.offsets + r);
+    e.o1 = __ldg(a.offsets + r + 1);
+  }
+  return e;
+}
+
+// PACKED: a packed store (a.offsets set); span: the entry's offsets, loaded ahead
+// by the caller. A slotted store's instantiation carries none of it.
+template <bool PACKED>
 __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, int64_t u,
-                                          int64_t r, bool leader) {
+                                          int64_t r, bool leader, EntrySpan span) {
   Unit un;
   un.src = a.slots;
   un.out_word = 0;
@@ -112,19 +134,37 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
     if (leader) report(a.status, IBP_ERR_INDEX);
     return un;
   }
-  const uint8_t *slot = a.slots + r * a.slot_bytes;
   const uint32_t nvec = (uint32_t)(nblk * a.lwb / 4);
-  if (a.nseg == 1 && a.n_rows <= 0xFFFFFFFFll && whole_slot(a, shrink)) {
-    // stage the slot's whole raw-size prefix at once: the bitmask bit and, for a
-    // compressed row, the participation bits are read later, off the critical path
+  const uint8_t *slot;
+  int64_t avail;  // readable bytes of the row's slot or entry
+  if (PACKED) {
+    const uint64_t o0 = span.o0, o1 = span.o1;
+    if (o1 < o0 || (o0 & 15) || (o1 & 15) || o1 > a.packed_bytes) {
+      if (leader) report(a.status, IBP_ERR_CORRUPT);
+      return un;
+    }
+    slot = a.slots + o0;
+    avail = (int64_t)(o1 - o0);
+  } else {
+    slot = a.slots + r * a.slot_bytes;
+    avail = a.slot_bytes;
+  }
+  if (a.nseg == 1 && a.n_rows <= 0xFFFFFFFFll && (PACKED || whole_slot(a, shrink))) {
+    // stage the slot's whole raw-size prefix (a packed entry: all of it) at once:
+    // the bitmask bit and, for a compressed row, the participation bits are read
+    // later, off the critical path
     un.src = slot;
-    un.nchunk = nvec;
+    un.nchunk = (uint32_t)min((int64_t)nvec, avail >> 4);
     un.nvec = nvec;
     un.lsb = PARSE_HEADER;
     un.segp = (uint32_t)r;
     return un;
   }
   if (!((__ldg(a.bitmask + (r >> 5)) >> (r & 31)) & 1u)) {  // stored raw
+    if (PACKED && avail < a.raw_bytes) {
+      if (leader) report(a.status, IBP_ERR_CORRUPT);
+      return un;
+    }
     un.src = slot + (size_t)b0 * a.lwb * 4;
     un.nchunk = nvec;
     un.nvec = nvec;
@@ -133,6 +173,10 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   // participation bits: nb bits at the start of the slot
   const uint32_t *hw = reinterpret_cast<const uint32_t *>(slot);
   const int nhw = (a.nb + 31) >> 5;
+  if (PACKED && avail < 4 * nhw) {
+    if (leader) report(a.status, IBP_ERR_CORRUPT);
+    return un;
+  }
   uint32_t cnt_all = 0, cnt0 = 0, lo = 0, hi = 0;
   const int q0 = b0 >> 5;
   for (int q = 0; q < nhw; ++q) {
@@ -148,7 +192,8 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   if (q0 + 1 >= nhw) hi = 0;
   const uint32_t segp = window(lo, hi, (uint32_t)(b0 & 31)) & low_mask((uint32_t)nblk);
   const uint32_t total = (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * cnt_all);
-  if ((int64_t)((total + 31) >> 5) * 4 >= a.raw_bytes) {
+  const int64_t used = (int64_t)((total + 31) >> 5) * 4;
+  if (used >= a.raw_bytes || (PACKED && used > avail)) {
     if (leader) report(a.status, IBP_ERR_CORRUPT);
     return un;
   }
@@ -184,16 +229,21 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
   const uint32_t *S = reinterpret_cast<const uint32_t *>(buf);
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + un.out_word);
   uint32_t segp = un.segp, lsb = un.lsb, nvec = un.nvec;
-  if (lsb == PARSE_HEADER) {  // whole slot staged
+  if (lsb == PARSE_HEADER) {  // whole slot (or packed entry) staged, un.nchunk pieces
     if (!((un.bmw >> (segp & 31)) & 1u)) {  // stored raw: the slot prefix is the row
       segp = 0;
       lsb = 0;
+      if (un.nchunk < nvec) {  // a packed entry shorter than the raw row
+        if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
+        nvec = 0;
+      }
     } else {  // participation bits are S[0] (one segment, nb <= 32)
-      segp = S[0] & low_mask((uint32_t)a.nb);
+      segp = un.nchunk ? (S[0] & low_mask((uint32_t)a.nb)) : 0u;
       lsb = (uint32_t)a.nb;
       const uint32_t total =
           (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * __popc(segp));
-      if ((int64_t)((total + 31) >> 5) * 4 >= a.raw_bytes) {
+      const int64_t used = (int64_t)((total + 31) >> 5) * 4;
+      if (used >= a.raw_bytes || used > 16 * (int64_t)un.nchunk) {
         if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
         nvec = 0;
       }
@@ -239,10 +289,10 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
 // Decode-time fields of a staged unit, kept in shared memory next to its buffer.
 struct __align__(16) StagedMeta {
   int64_t out_word;
-  uint32_t lsb, segp, nvec, bmw;
+  uint32_t lsb, segp, nvec, bmw, nchunk;
 };
 
-template <int NR, int TL>
+template <int NR, int TL, bool PACKED>
 __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedRuns &sruns,
                             uint8_t *warp_smem, StagedMeta *warp_meta) {
   constexpr int TPW = 32 / TL;  // teams per warp
@@ -262,14 +312,25 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
   if (base >= a.n_units) return;
   int64_t u_plan = base + team;  // next unit this team plans
   int64_t r_plan = load_index(a, u_plan);
+  // packed stores: the unit after next's index and the next unit's entry span are
+  // loaded one step ahead, so neither dependent load waits in front of staging
+  int64_t r_next = PACKED ? load_index(a, u_plan + stride) : -1;
+  EntrySpan span_plan = PACKED ? load_span(a, r_plan) : EntrySpan{0, 0};
   int k_plan = 0;                // buffer it goes to
   uint32_t pend_bmw = 0;         // bitmask word loaded for the last planned unit,
   int pend_k = -1;               // stored into its meta one step later
 
   // plan one unit, stage its bytes, record what decoding it will need
   auto plan_and_stage = [&]() {
-    const int64_t r_after = load_index(a, u_plan + stride);  // prefetch
-    const Unit un = plan_unit(a, shrink, u_plan, r_plan, leader);
+    int64_t r_after;
+    EntrySpan span_after{0, 0};
+    if (PACKED) {
+      r_after = load_index(a, u_plan + 2 * stride);  // prefetch, two units ahead
+      span_after = load_span(a, r_next);            // the next unit's entry
+    } else {
+      r_after = load_index(a, u_plan + stride);  // prefetch
+    }
+    const Unit un = plan_unit<PACKED>(a, shrink, u_plan, r_plan, leader, span_plan);
     if (leader && pend_k >= 0) metas[pend_k * TPW].bmw = pend_bmw;
     pend_bmw = un.lsb == PARSE_HEADER ? __ldg(a.bitmask + (un.segp >> 5)) : 0u;
     pend_k = k_plan;
@@ -280,13 +341,20 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
       m.segp = un.segp;
       m.nvec = un.nvec;
       m.bmw = 0;
+      m.nchunk = un.nchunk;
       metas[k_plan * TPW] = m;
     }
     stage_unit<TL>(un, bufs + k_plan * buf_step, tl);
     cp_async_commit();
     k_plan = k_plan + 1 == GATHER_NBUF ? 0 : k_plan + 1;
     u_plan += stride;
-    r_plan = r_after;
+    if (PACKED) {
+      r_plan = r_next;
+      r_next = r_after;
+      span_plan = span_after;
+    } else {
+      r_plan = r_after;
+    }
   };
 
 #pragma unroll 1
@@ -299,7 +367,7 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     const StagedMeta m = metas[k_dec * TPW];
     Unit un;
     un.src = nullptr;
-    un.nchunk = 0;
+    un.nchunk = m.nchunk;
     un.out_word = m.out_word;
     un.lsb = m.lsb;
     un.segp = m.segp;
@@ -314,16 +382,16 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
   cp_async_wait<0>();
 }
 
-template <int TL>
+template <int TL, bool PACKED>
 __device__ void dispatch_runs(const GatherArgs &a, const Code &code, const SharedRuns &sruns,
                               uint8_t *warp_smem, StagedMeta *warp_meta) {
   switch (sruns.n) {
-    case 0: gather_body<0, TL>(a, code, sruns, warp_smem, warp_meta); break;
-    case 1: gather_body<1, TL>(a, code, sruns, warp_smem, warp_meta); break;
-    case 2: gather_body<2, TL>(a, code, sruns, warp_smem, warp_meta); break;
-    case 3: gather_body<3, TL>(a, code, sruns, warp_smem, warp_meta); break;
-    case 4: gather_body<4, TL>(a, code, sruns, warp_smem, warp_meta); break;
-    default: gather_body<-1, TL>(a, code, sruns, warp_smem, warp_meta); break;
+    case 0: gather_body<0, TL, PACKED>(a, code, sruns, warp_smem, warp_meta); break;
+    case 1: gather_body<1, TL, PACKED>(a, code, sruns, warp_smem, warp_meta); break;
+    case 2: gather_body<2, TL, PACKED>(a, code, sruns, warp_smem, warp_meta); break;
+    case 3: gather_body<3, TL, PACKED>(a, code, sruns, warp_smem, warp_meta); break;
+    case 4: gather_body<4, TL, PACKED>(a, code, sruns, warp_smem, warp_meta); break;
+    default: gather_body<-1, TL, PACKED>(a, code, sruns, warp_smem, warp_meta); break;
   }
 }
 
@@ -334,7 +402,7 @@ __host__ __device__ inline size_t team_warp_bytes(int tl, int unit_bytes) {
 
 // MINB: resident CTAs per SM the register budget is sized for (4 for slots in
 // device memory, 3 for host memory; measured best for each).
-template <int TL, int MINB>
+template <int TL, int MINB, bool PACKED>
 __global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
@@ -349,7 +417,7 @@ __global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherA
   uint8_t *warp_smem = smem + (threadIdx.x >> 5) * team_warp_bytes(TL, a.unit_bytes);
   StagedMeta *warp_meta = reinterpret_cast<StagedMeta *>(
       warp_smem + (size_t)GATHER_NBUF * (32 / TL) * a.unit_bytes);
-  dispatch_runs<TL>(a, code, sruns, warp_smem, warp_meta);
+  dispatch_runs<TL, PACKED>(a, code, sruns, warp_smem, warp_meta);
 }
 
 // ---------------------------------------------------------------------------
@@ -406,7 +474,8 @@ __device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64
     r_next = k + step < count ? load_index(a, u0 + k + step) : -1;  // prefetch
     bool ok = true;
     if (have) {
-      const Unit un = plan_unit(a, shrink, u0 + k, r, true);
+      const Unit un = a.offsets ? plan_unit<true>(a, shrink, u0 + k, r, true, load_span(a, r))
+                                : plan_unit<false>(a, shrink, u0 + k, r, true, EntrySpan{0, 0});
       const int slot = (int)(k % PLAN_SLOTS);
       ok = mbar_wait(&freed[slot], (uint32_t)((k / PLAN_SLOTS) & 1) ^ 1u, abort);
       if (ok) {
@@ -558,25 +627,25 @@ int ilog2(int x) {
   return s;
 }
 
-template <int TL, int MINB>
+template <int TL, int MINB, bool PACKED>
 int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const size_t smem = (size_t)GATHER_WARPS * team_warp_bytes(TL, a.unit_bytes);
   static int configured[64] = {0};
   if (dev.device < 64 && !configured[dev.device]) {
-    if (cudaFuncSetAttribute(gather_kernel<TL, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gather_kernel<TL, MINB, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dev.max_smem_optin - (int)sizeof(SharedRuns) - 1024) != cudaSuccess)
       return IBP_ERR_CUDA;
     configured[dev.device] = 1;
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL, MINB>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL, MINB, PACKED>,
                                                     GATHER_WARPS * 32, smem) != cudaSuccess ||
       per_sm < 1)
     return IBP_ERR_CUDA;
   const int64_t units_per_cta = (int64_t)GATHER_WARPS * (32 / TL);
   const int64_t want = (a.n_units + units_per_cta - 1) / units_per_cta;
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
-  gather_kernel<TL, MINB><<<grid, GATHER_WARPS * 32, smem, s>>>(a);
+  gather_kernel<TL, MINB, PACKED><<<grid, GATHER_WARPS * 32, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
@@ -621,18 +690,36 @@ int launch_ws(GatherArgs a, const RowGeom &g, const DeviceInfo &dev, cudaStream_
   }
 }
 
+template <bool PACKED>
+int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const DeviceInfo &dev,
+                cudaStream_t s) {
+  if (slots_in_device_memory) {  // units of at most 1 KiB: team size 4 or 8
+    if (tl == 4) return launch_tl<4, 4, PACKED>(a, dev, s);
+    return launch_tl<8, 4, PACKED>(a, dev, s);
+  }
+  switch (tl) {
+    case 4: return launch_tl<4, 3, PACKED>(a, dev, s);
+    case 8: return launch_tl<8, 3, PACKED>(a, dev, s);
+    case 16: return launch_tl<16, 3, PACKED>(a, dev, s);
+    default: return launch_tl<32, 3, PACKED>(a, dev, s);
+  }
+}
+
 }  // namespace
 
-int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
-                  uint32_t dtype, const uint32_t *d_bitmask, const ibp_meta *d_meta,
-                  const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
-                  bool slots_in_device_memory, cudaStream_t s) {
+int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
+                  uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
+                  const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
+                  int64_t n_idx, void *out, int32_t *d_status, bool slots_in_device_memory,
+                  cudaStream_t s) {
   if (n_idx == 0) return IBP_OK;
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
   GatherArgs a;
   a.slots = static_cast<const uint8_t *>(slots);
   a.slot_bytes = slot_bytes;
+  a.offsets = d_offsets;
+  a.packed_bytes = packed_bytes;
   a.n_rows = n_rows;
   a.bitmask = d_bitmask;
   a.meta = d_meta;
@@ -666,16 +753,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const R
   const int nvec = a.seg_blocks * g.lwb / 4;
   int tl = 4;
   while (tl < 32 && tl * 4 < nvec) tl *= 2;
-  if (slots_in_device_memory) {  // units of at most 1 KiB: team size 4 or 8
-    if (tl == 4) return launch_tl<4, 4>(a, dev, s);
-    return launch_tl<8, 4>(a, dev, s);
-  }
-  switch (tl) {
-    case 4: return launch_tl<4, 3>(a, dev, s);
-    case 8: return launch_tl<8, 3>(a, dev, s);
-    case 16: return launch_tl<16, 3>(a, dev, s);
-    default: return launch_tl<32, 3>(a, dev, s);
-  }
+  if (d_offsets) return launch_team<true>(a, tl, slots_in_device_memory, dev, s);
+  return launch_team<false>(a, tl, slots_in_device_memory, dev, s);
 }
 
 }  // namespace ibp

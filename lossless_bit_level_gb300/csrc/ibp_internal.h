@@ -46,10 +46,23 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
                     uint32_t *d_row_bits, int32_t *d_status, cudaStream_t s);
 // slots_in_device_memory selects the warp-specialised bulk-copy kernel (device
 // memory) or the cp.async kernel (page-locked host memory read zero-copy).
-int launch_gather(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
-                  uint32_t dtype, const uint32_t *d_bitmask, const ibp_meta *d_meta,
-                  const int64_t *d_idx, int64_t n_idx, void *out, int32_t *d_status,
-                  bool slots_in_device_memory, cudaStream_t s);
+// d_offsets non-null: a packed store (entry r at slots + d_offsets[r], packed_bytes
+// long in all); otherwise slot r at slots + r * slot_bytes.
+int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
+                  uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
+                  const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
+                  int64_t n_idx, void *out, int32_t *d_status, bool slots_in_device_memory,
+                  cudaStream_t s);
+size_t pack_scratch_bytes(int64_t n_sel);
+int launch_pack_offsets(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                        int64_t raw_bytes, const int64_t *d_sel, int64_t n_sel,
+                        uint64_t *d_offsets, void *d_scratch, int32_t *d_status,
+                        cudaStream_t s);
+int launch_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t raw_bytes,
+                const uint32_t *d_bitmask, const uint32_t *d_row_bits, const int64_t *d_sel,
+                int64_t n_sel, const uint64_t *d_offsets, void *packed, uint64_t packed_bytes,
+                uint32_t *d_pack_bitmask, uint32_t *d_pack_row_bits, int32_t *d_status,
+                cudaStream_t s);
 int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
                  int64_t raw_bytes, ibp_stats *d_stats, cudaStream_t s);
 int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s);

@@ -40,6 +40,9 @@ def test_size_queries(lib):
     assert ibp.slot_bytes(33, ibp.FP16) == 80
     assert ibp.meta_scratch_bytes() == 256
     assert ibp.meta_select_scratch_bytes() == 1024
+    assert ibp.pack_scratch_bytes(0) == 8
+    assert ibp.pack_scratch_bytes(4096) == 8
+    assert ibp.pack_scratch_bytes(4097) == 16
     with pytest.raises(ibp.IBPError):
         ibp.slot_bytes(0, ibp.FP32)
     with pytest.raises(ibp.IBPError) as e:
@@ -79,4 +82,21 @@ def test_argument_errors_before_cuda(lib):
                                      None) == ibp.ERR_UNSUPPORTED
     assert lib.ibp_build_meta_select(vp(16), 10, 128, 5, 0.9, 32, vp(16), None, vp(16),
                                      None) == ibp.ERR_DTYPE
+    # packed store: sizes, null pointers, selection count, empty calls
+    assert lib.ibp_pack_offsets(None, None, 10, 128, ibp.FP32, None, 11, vp(16), vp(16), None,
+                                None) == ibp.ERR_ARG  # n_sel > n_rows without a selection
+    assert lib.ibp_pack_offsets(None, None, 10, 128, 4, None, 5, vp(16), vp(16), None,
+                                None) == ibp.ERR_DTYPE
+    assert lib.ibp_pack(None, 512, 10, 128, ibp.FP32, None, None, None, 0, None, None, 0, None,
+                        None, None, None) == ibp.OK  # nothing to pack
+    assert lib.ibp_pack(None, 496, 10, 128, ibp.FP32, None, None, None, 4, None, None, 0, None,
+                        None, None, None) == ibp.ERR_ARG  # slot smaller than a raw row
+    assert lib.ibp_pack(None, 512, 10, 128, ibp.FP32, None, None, None, 4, None, None, 0, None,
+                        None, None, None) == ibp.ERR_ARG
+    assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 32, None, None,
+                                            None, 0, None, None, None) == ibp.OK
+    assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 32, None, None,
+                                            None, 3, None, None, None) == ibp.ERR_ARG
+    assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 48, None, None,
+                                            None, 3, None, None, None) == ibp.ERR_ARG
     assert ibp.status_string(ibp.ERR_CORRUPT) == "corrupt slot header"
