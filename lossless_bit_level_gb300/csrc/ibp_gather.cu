@@ -154,7 +154,7 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
     // the bitmask bit and, for a compressed row, the participation bits are read
     // later, off the critical path
     un.src = slot;
-    un.nchunk = (uint32_t)min((int64_t)nvec, avail >> 4);
+    un.nchunk = PACKED ? (uint32_t)min((int64_t)nvec, avail >> 4) : nvec;
     un.nvec = nvec;
     un.lsb = PARSE_HEADER;
     un.segp = (uint32_t)r;
@@ -220,7 +220,7 @@ __device__ __forceinline__ void stage_unit(const Unit &un, uint8_t *buf, int tl)
   for (uint32_t c = tl; c < un.nchunk; c += TL) cp_async16(buf + 16 * c, un.src + 16 * c);
 }
 
-template <int NR, int TL>
+template <int NR, int TL, bool PACKED>
 __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &code,
                                             const RegRuns<NR> &runs, const SharedRuns &sruns,
                                             const Unit &un, const uint8_t *buf, int tl) {
@@ -233,17 +233,17 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
     if (!((un.bmw >> (segp & 31)) & 1u)) {  // stored raw: the slot prefix is the row
       segp = 0;
       lsb = 0;
-      if (un.nchunk < nvec) {  // a packed entry shorter than the raw row
+      if (PACKED && un.nchunk < nvec) {  // a packed entry shorter than the raw row
         if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
         nvec = 0;
       }
     } else {  // participation bits are S[0] (one segment, nb <= 32)
-      segp = un.nchunk ? (S[0] & low_mask((uint32_t)a.nb)) : 0u;
+      segp = (!PACKED || un.nchunk) ? (S[0] & low_mask((uint32_t)a.nb)) : 0u;
       lsb = (uint32_t)a.nb;
       const uint32_t total =
           (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * __popc(segp));
       const int64_t used = (int64_t)((total + 31) >> 5) * 4;
-      if (used >= a.raw_bytes || used > 16 * (int64_t)un.nchunk) {
+      if (used >= a.raw_bytes || (PACKED && used > 16 * (int64_t)un.nchunk)) {
         if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
         nvec = 0;
       }
@@ -341,7 +341,7 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
       m.segp = un.segp;
       m.nvec = un.nvec;
       m.bmw = 0;
-      m.nchunk = un.nchunk;
+      m.nchunk = PACKED ? un.nchunk : 0u;
       metas[k_plan * TPW] = m;
     }
     stage_unit<TL>(un, bufs + k_plan * buf_step, tl);
@@ -367,13 +367,13 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     const StagedMeta m = metas[k_dec * TPW];
     Unit un;
     un.src = nullptr;
-    un.nchunk = m.nchunk;
+    un.nchunk = PACKED ? m.nchunk : 0u;
     un.out_word = m.out_word;
     un.lsb = m.lsb;
     un.segp = m.segp;
     un.nvec = m.nvec;
     un.bmw = m.bmw;
-    decode_unit<NR, TL>(a, code, runs, sruns, un, bufs + k_dec * buf_step, tl);
+    decode_unit<NR, TL, PACKED>(a, code, runs, sruns, un, bufs + k_dec * buf_step, tl);
     __syncwarp();
     base += stride;
     if (base >= a.n_units) break;
@@ -567,7 +567,8 @@ __device__ void ws_decode(const GatherArgs &a, const Code &code, const SharedRun
     cp_async_commit();
     cp_async_wait<1>();
     __syncwarp();
-    decode_unit<NR, TL>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
+    if (a.offsets) decode_unit<NR, TL, true>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
+    else decode_unit<NR, TL, false>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
     __syncwarp();
     cur = nxt;
     k = kn;
@@ -693,9 +694,12 @@ int launch_ws(GatherArgs a, const RowGeom &g, const DeviceInfo &dev, cudaStream_
 template <bool PACKED>
 int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const DeviceInfo &dev,
                 cudaStream_t s) {
-  if (slots_in_device_memory) {  // units of at most 1 KiB: team size 4 or 8
-    if (tl == 4) return launch_tl<4, 4, PACKED>(a, dev, s);
-    return launch_tl<8, 4, PACKED>(a, dev, s);
+  // units of at most 1 KiB in device memory: team size 4 or 8, 4 CTAs per SM (3 for
+  // packed stores, whose extra span registers would spill at 4)
+  if (slots_in_device_memory) {
+    constexpr int MINB = PACKED ? 3 : 4;
+    if (tl == 4) return launch_tl<4, MINB, PACKED>(a, dev, s);
+    return launch_tl<8, MINB, PACKED>(a, dev, s);
   }
   switch (tl) {
     case 4: return launch_tl<4, 3, PACKED>(a, dev, s);
