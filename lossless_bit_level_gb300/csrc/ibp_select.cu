@@ -17,8 +17,9 @@
 //      of rows and walks them in 128-word chunks (a 16-byte load per lane, four
 //      chunks in flight). For each block it ORs the mismatch bits
 //      (x ^ bitval) & M0 over the block's words and finds the block's level: the
-//      first candidate whose mask misses all of them (a binary search over the
-//      nested masks). Lane k then counts, per row, the blocks whose level is <= k,
+//      first candidate whose mask misses all of them (byte-table lookups of the
+//      largest group rank among the bits). Lane k then counts, per row, the blocks
+//      whose level is <= k,
 //      i.e. the blocks that match candidate k, turns that into the row's stored
 //      bytes under candidate k, and accumulates them; one 64-bit atomic per lane
 //      and warp at the end;
@@ -47,6 +48,7 @@ struct SelectScratch {
   uint32_t keep[NCAND];             // candidate masks (w bits), 0 past the last
   uint32_t n_cand;                  // number of candidates (1 .. w+1)
   uint32_t bitval0;                 // bitval of M0
+  uint8_t level[32];                // position j: 1 + its group rank if in M0, else 0
 };
 
 __global__ void select_groups_kernel(SelectScratch *sc, int64_t n_elems, int w, double T) {
@@ -78,6 +80,8 @@ __global__ void select_groups_kernel(SelectScratch *sc, int64_t n_elems, int w, 
     const uint32_t mk = __ballot_sync(FULL, inv && rank >= k);
     if (j == 0) sc->keep[k] = (k <= groups) ? mk : 0u;
   }
+  // a block whose mismatch bits include position j matches candidate k iff k > rank
+  sc->level[j] = inv ? (uint8_t)(rank + 1) : (uint8_t)0;
   if (j == 0) {
     sc->n_cand = (uint32_t)groups + 1;
     sc->bitval0 = bitval0;
@@ -97,28 +101,47 @@ struct ScoreArgs {
 
 // LWB = 32-bit words per block (16, 32 or 64): a block spans LWB/4 lanes of a
 // 128-word chunk, and a chunk holds 32/(LWB/4) whole blocks.
+//
+// A block's level is the largest level[j] over its mismatch bits j (0 if none):
+// the block matches candidate k iff k >= level. It is read from four 256-entry
+// byte tables (one per byte of the lane word: the largest level among the byte's
+// set bits), so a block costs four shared-memory lookups.
 template <int LWB>
 __global__ void __launch_bounds__(SEL_THREADS) select_score_kernel(const ScoreArgs a) {
   constexpr int LPB = LWB / 4;
   constexpr int BPC = 32 / LPB;
-  __shared__ uint32_t K2[NCAND];  // candidate masks, 16-bit ones repeated in both halves
-  __shared__ uint32_t s_bv2, s_G;
-  if (threadIdx.x < NCAND) {
-    const uint32_t k = a.sc->keep[threadIdx.x];
-    K2[threadIdx.x] = (a.w == 16) ? (k | (k << 16)) : k;
+  __shared__ uint8_t lvl_tab[4][256];
+  __shared__ uint32_t s_M0, s_bv2, s_keep[32];
+  {
+    const int b = threadIdx.x >> 6;  // 256 threads: 4 tables x 64 threads x 4 entries
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int x = ((threadIdx.x & 63) << 2) + q;
+      int mx = 0;
+      for (int i = 0; i < 8; ++i)
+        if ((x >> i) & 1) {
+          const int pos = (8 * b + i) & (a.w - 1);  // 16-bit words: both halves alike
+          mx = max(mx, (int)a.sc->level[pos]);
+        }
+      lvl_tab[b][x] = (uint8_t)mx;
+    }
   }
+  if (threadIdx.x < 32) s_keep[threadIdx.x] = a.sc->keep[threadIdx.x];
   if (threadIdx.x == 0) {
-    const uint32_t bv = a.sc->bitval0;
+    const uint32_t k0 = a.sc->keep[0], bv = a.sc->bitval0;
+    s_M0 = (a.w == 16) ? (k0 | (k0 << 16)) : k0;
     s_bv2 = (a.w == 16) ? (bv | (bv << 16)) : bv;
-    s_G = a.sc->n_cand - 1;
   }
   __syncthreads();
-  const uint32_t M0 = K2[0], bv2 = s_bv2;
-  const int G = (int)s_G;
+  const uint32_t M0 = s_M0, bv2 = s_bv2;
   const int lane = threadIdx.x & 31;
   const uint32_t wmask = (a.w == 16) ? 0xFFFFu : 0xFFFFFFFFu;
-  const int m_k = a.w - __popc(K2[lane] & wmask);  // field width under candidate `lane`
-  const int cpr = (a.vpr + 31) / 32;               // chunks per row
+  // bits of a matching / a raw block under candidate `lane`
+  const uint32_t bm = (uint32_t)a.B * (uint32_t)(a.w - __popc(s_keep[lane] & wmask));
+  const uint32_t br = (uint32_t)a.B * (uint32_t)a.w;
+  const uint32_t raw = (uint32_t)a.raw_bytes;
+  const uint32_t nb = (uint32_t)a.nb;
+  const int cpr = (a.vpr + 31) / 32;  // chunks per row
 
   const int64_t warps = (int64_t)gridDim.x * SEL_WARPS;
   const int64_t wid = (int64_t)blockIdx.x * SEL_WARPS + threadIdx.x / 32;
@@ -126,7 +149,7 @@ __global__ void __launch_bounds__(SEL_THREADS) select_score_kernel(const ScoreAr
   int64_t r = wid * per;
   const int64_t r_end = min(a.n_rows, r + per);
   int c = 0;
-  int matched = 0;
+  uint32_t matched = 0;
   unsigned long long acc = 0;
   while (r < r_end) {
     uint4 x[SEL_UNROLL];
@@ -151,26 +174,18 @@ __global__ void __launch_bounds__(SEL_THREADS) select_score_kernel(const ScoreAr
       uint32_t D = ((x[u].x ^ bv2) | (x[u].y ^ bv2) | (x[u].z ^ bv2) | (x[u].w ^ bv2)) & M0;
 #pragma unroll
       for (int o = 1; o < LPB; o <<= 1) D |= __shfl_xor_sync(FULL, D, o);
-      // level: the first candidate whose mask misses every mismatch bit of the block
-      int lo = 0, hi = G;
-#pragma unroll
-      for (int it = 0; it < 6; ++it) {
-        if (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if ((D & K2[mid]) == 0u) hi = mid;
-          else lo = mid + 1;
-        }
-      }
+      const int lv = max(max((int)lvl_tab[0][D & 0xFFu], (int)lvl_tab[1][(D >> 8) & 0xFFu]),
+                         max((int)lvl_tab[2][(D >> 16) & 0xFFu], (int)lvl_tab[3][D >> 24]));
+      const uint32_t blk0 = (uint32_t)(cc[u] * BPC);
 #pragma unroll
       for (int b = 0; b < BPC; ++b) {
-        const int lb = __shfl_sync(FULL, lo, b * LPB);
-        matched += (cc[u] * BPC + b < a.nb && lb <= lane) ? 1 : 0;
+        const int lb = __shfl_sync(FULL, lv, b * LPB);
+        matched += (blk0 + b < nb && lb <= lane) ? 1u : 0u;
       }
       if (cc[u] == cpr - 1) {  // the row is complete
-        const int64_t bits = a.nb + (int64_t)matched * a.B * m_k +
-                             (int64_t)(a.nb - matched) * a.B * a.w;
-        const int64_t stored = 4 * ((bits + 31) / 32);
-        acc += (unsigned long long)(stored < a.raw_bytes ? stored : a.raw_bytes);
+        const uint32_t bits = nb + matched * bm + (nb - matched) * br;
+        const uint32_t stored = ((bits + 31u) >> 5) << 2;
+        acc += stored < raw ? stored : raw;
         matched = 0;
       }
     }
