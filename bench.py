@@ -420,6 +420,82 @@ def packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier, table_ra
     return res
 
 
+def offload_leg(dev, n_steps=8, token_counts=(256, 4096)):
+    """Overlapped offload pipeline on one LLaMA-7B-shaped decoder layer (q, k, v, o
+    4096 x 4096; gate, up 11008 x 4096; down 4096 x 11008; BF16 N(0, 0.02)) kept
+    compressed in page-locked host memory (threshold mask per tensor, T = 0.9,
+    B = 64) and streamed n_steps times through two device buffer sets while a
+    consumer runs one bf16 matmul per weight (tokens x in) @ (in x out). Per-layer
+    time for the compressed and the raw (cudaMemcpyAsync) loaders, overlapped with
+    the consumer and serialised with it."""
+    from lossless_bit_level_gb300.offload import CompressedTensor, OffloadPipeline, raw_loader
+
+    layer, raw = [], {}
+    for name in gen.LLM_MATRICES:
+        w = gen.llm_weight(0, name)
+        t = CompressedTensor.from_words(w, ibp.BF16, 0.9, 64, dev)
+        h = torch.empty(w.shape, dtype=torch.int16, pin_memory=True)
+        h.copy_(torch.from_numpy(w.view(np.int16)))
+        raw[id(t)] = h
+        layer.append(t)
+        del w
+    layers = [layer]
+    raw_bytes = sum(t.raw_bytes for t in layer)
+    stored = sum(t.stored_bytes() for t in layer)
+    res = {"workload": "one LLaMA-7B-shaped decoder layer, 7 BF16 weights N(0, 0.02), "
+                       f"streamed {n_steps} times; consumer: one bf16 matmul per weight",
+           "raw_bytes_per_layer": raw_bytes, "stored_bytes_per_layer": stored,
+           "saving_pct": 100.0 * (1.0 - stored / raw_bytes), "tokens": {}}
+    for tokens in token_counts:
+        xh = torch.randn(tokens, gen.LLM_HIDDEN, dtype=torch.bfloat16, device=dev)
+        xf = torch.randn(tokens, gen.LLM_FFN, dtype=torch.bfloat16, device=dev)
+
+        def consume(l, bufs):
+            for t, b in zip(layers[l], bufs):
+                x = xf if t.row_elems == gen.LLM_FFN else xh
+                torch.matmul(x, b.view(torch.bfloat16).t())
+
+        r = {}
+        warm = [t.empty_like(dev) for t in layer]
+        for _ in range(3):  # library start-up of the consumer's matmul shapes
+            consume(0, warm)
+        torch.cuda.synchronize()
+        del warm
+        for mode, load, overlap in (("ibp_overlap", None, True), ("raw_overlap", raw_loader(raw), True),
+                                    ("ibp_serial", None, False), ("raw_serial", raw_loader(raw), False)):
+            pipe = OffloadPipeline(layers, dev, load=load, overlap=overlap)
+            pipe.run(3, consume)
+            pipe.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(pipe.loader)
+            pipe.compute.wait_event(a)
+            pipe.run(n_steps, consume)
+            b.record(pipe.compute)
+            b.synchronize()
+            r[mode + "_ms_per_layer"] = a.elapsed_time(b) / n_steps
+            del pipe
+        s = torch.cuda.current_stream()
+        bufs = [t.empty_like(dev) for t in layer]
+        consume(0, bufs)
+        a, b = event_pair(s)
+        a.record(s)
+        for _ in range(n_steps):
+            consume(0, bufs)
+        b.record(s)
+        b.synchronize()
+        r["compute_only_ms_per_layer"] = a.elapsed_time(b) / n_steps
+        r["speedup_vs_raw_overlap"] = r["raw_overlap_ms_per_layer"] / r["ibp_overlap_ms_per_layer"]
+        r["ibp_decode_link_gbs"] = stored / (r["ibp_serial_ms_per_layer"] -
+                                            r["compute_only_ms_per_layer"]) / 1e6
+        res["tokens"][str(tokens)] = r
+        del bufs, xh, xf
+    for t in layer:
+        assert int(t.status.item()) == 0
+    del layers, layer, raw
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_stage(fn, reps, flush=None):
     s = torch.cuda.current_stream()
     ts = []
@@ -787,6 +863,8 @@ def main():
         extra["packed"] = packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier,
                                      table_raw, out_bytes, link, hbm_peak, dev)
         del sstore
+        if args.workload == "gnn_dense":
+            extra["offload"] = offload_leg(dev)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,

@@ -239,6 +239,15 @@ int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
                                  const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
                                  void *out, int32_t *d_status, ibp_stream_t s);
 
+/* Decompress a contiguous range of rows in order: out[i] = row row_begin + i for
+ * i < n_out (row_begin + n_out <= n_rows). The same as ibp_decompress_gather with
+ * d_idx = row_begin, row_begin + 1, ..., without an index array: for streaming
+ * whole tensors (a layer's weights, a sequence's K/V rows) out of a store. */
+int ibp_decompress_range(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems,
+                         int dtype, uint32_t block_elems, const uint32_t *d_row_bitmask,
+                         const ibp_meta *d_meta, int64_t row_begin, int64_t n_out, void *out,
+                         int32_t *d_status, ibp_stream_t s);
+
 /* Statistics of a store: reduces the bitmask and the per-row bit counts written
  * by ibp_compress into *d_stats (device memory), asynchronously on s. */
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,

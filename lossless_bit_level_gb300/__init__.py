@@ -46,7 +46,8 @@ class Stats(ctypes.Structure):
 SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp_build_meta",
            "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read",
            "ibp_build_meta_noalloc", "ibp_meta_select_scratch_bytes", "ibp_build_meta_select",
-           "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed")
+           "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed",
+           "ibp_decompress_range")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -80,6 +81,7 @@ def load() -> ctypes.CDLL:
     lib.ibp_meta_select_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
     lib.ibp_build_meta_select.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
     u64 = ctypes.c_uint64
+    lib.ibp_decompress_range.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, i64, i64, vp, vp, vp]
     lib.ibp_pack_scratch_bytes.argtypes = [i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.ibp_pack_offsets.argtypes = [vp, vp, i64, i64, i32, vp, i64, vp, vp, vp, vp]
     lib.ibp_pack.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, u64, vp, vp, vp, vp]
@@ -263,6 +265,19 @@ def decompress_gather_packed(packed: torch.Tensor, offsets: torch.Tensor, n_rows
         _ptr(packed), packed.numel() * packed.element_size(), _ptr(offsets), int(n_rows),
         int(row_elems), int(dtype), int(block_elems), _ptr(bitmask), _ptr(meta), _ptr(idx),
         idx.numel(), _ptr(out), _ptr(status), _stream(stream)), "ibp_decompress_gather_packed")
+
+
+def decompress_range(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
+                     block_elems: int, bitmask: torch.Tensor, meta: torch.Tensor, row_begin: int,
+                     n_out: int, out: torch.Tensor, status: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """ibp_decompress_range: rows row_begin .. row_begin + n_out - 1 into ``out``."""
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(int(n_rows), 1)
+    _check(load().ibp_decompress_range(_ptr(slots), sb, int(n_rows), int(row_elems), int(dtype),
+                                       int(block_elems), _ptr(bitmask), _ptr(meta),
+                                       int(row_begin), int(n_out), _ptr(out), _ptr(status),
+                                       _stream(stream)), "ibp_decompress_range")
 
 
 def query(bitmask: torch.Tensor, row_bits: torch.Tensor, n_rows: int, row_elems: int, dtype: int,

@@ -99,4 +99,13 @@ def test_argument_errors_before_cuda(lib):
                                             None, 3, None, None, None) == ibp.ERR_ARG
     assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 48, None, None,
                                             None, 3, None, None, None) == ibp.ERR_ARG
+    # contiguous ranges: inside the store, empty is a no-op
+    assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, 4, 0, None, None,
+                                    None) == ibp.OK
+    assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, 4, 7, None, None,
+                                    None) == ibp.ERR_ARG  # past the last row
+    assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, -1, 2, None,
+                                    None, None) == ibp.ERR_ARG
+    assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, 0, 2, None, None,
+                                    None) == ibp.ERR_ARG  # null pointers
     assert ibp.status_string(ibp.ERR_CORRUPT) == "corrupt slot header"
