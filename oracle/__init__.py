@@ -187,8 +187,8 @@ class Oracle:
 
 
 def _width(a: np.ndarray) -> int:
-    if a.dtype.itemsize not in (2, 4):
-        raise ValueError("elements must be 16- or 32-bit words")
+    if a.dtype.itemsize not in (1, 2, 4):
+        raise ValueError("elements must be 8-, 16- or 32-bit words")
     return 8 * a.dtype.itemsize
 
 

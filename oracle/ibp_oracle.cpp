@@ -19,7 +19,10 @@
  *  R5 majority value on a tie is 0;
  *  R6 with an empty mask every block "matches" and costs B*w bits anyway;
  *  R7 a row is kept compressed only when its stream needs fewer whole 32-bit
- *     words than the raw row has bytes / 4.
+ *     words than the raw row has bytes / 4;
+ *  R8 a row whose length is not a multiple of B ends in a shorter block holding
+ *     the remaining elements; it has its own participation bit and is sized like
+ *     the others (1 + len*m or 1 + len*w bits).
  */
 #include "ibp_oracle.h"
 
@@ -113,7 +116,15 @@ uint32_t get_field(const unsigned char *stream, int64_t *pos, int nbits) {
   return v;
 }
 
-int valid_width(int w_bits) { return w_bits == 16 || w_bits == 32; }
+int valid_width(int w_bits) { return w_bits == 8 || w_bits == 16 || w_bits == 32; }
+
+/* elements of block b of a row: B, except the last block of a row whose length is
+   not a multiple of B, which holds the remaining row_elems - b*B (R8) */
+int64_t block_len(int64_t b, int64_t row_elems, int64_t block_elems) {
+  int64_t end = (b + 1) * block_elems;
+  if (end > row_elems) end = row_elems;
+  return end - b * block_elems;
+}
 
 uint32_t width_mask(int w_bits) { return w_bits == 32 ? 0xFFFFFFFFu : ((1u << w_bits) - 1u); }
 
@@ -163,7 +174,7 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
                              int64_t block_elems, uint32_t mask, uint32_t bitval, void *slots,
                              int64_t slot_bytes, uint32_t *bitmask, uint32_t *row_bits) {
   if (!rows || !slots || !bitmask || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) ||
-      block_elems <= 0 || row_elems % block_elems != 0 ||
+      block_elems <= 0 ||
       slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
     return IBPO_BAD_ARG;
   mask &= width_mask(w_bits);
@@ -171,7 +182,7 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
   const unsigned char *in = (const unsigned char *)rows;
   unsigned char *out = (unsigned char *)slots;
   const int64_t raw_bytes = row_elems * (w_bits / 8);
-  const int64_t nb = row_elems / block_elems;
+  const int64_t nb = (row_elems + block_elems - 1) / block_elems;
   const int m = w_bits - popcount_w(mask, w_bits);
 
   for (int64_t q = 0; q < (n_rows + 31) / 32; ++q) bitmask[q] = 0;
@@ -184,11 +195,12 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
     int64_t bits = 0;
     for (int64_t b = 0; b < nb; ++b) {
       int match = 1;
-      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+      for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
+           ++e) {
         uint32_t x = load_elem(row, e, w_bits);
         if ((x & mask) != bitval) match = 0;
       }
-      bits += 1 + block_elems * (match ? m : w_bits);
+      bits += 1 + block_len(b, row_elems, block_elems) * (match ? m : w_bits);
     }
     if (row_bits) row_bits[r] = (uint32_t)bits;
 
@@ -203,7 +215,8 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
     /* header: all participation bits first (R2) */
     for (int64_t b = 0; b < nb; ++b) {
       int match = 1;
-      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e)
+      for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
+           ++e)
         if ((load_elem(row, e, w_bits) & mask) != bitval) match = 0;
       put_bit(slot, pos, match);
       pos += 1;
@@ -211,7 +224,8 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
     /* payloads, block by block */
     for (int64_t b = 0; b < nb; ++b) {
       int match = get_bit(slot, b);
-      for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+      for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
+           ++e) {
         uint32_t x = load_elem(row, e, w_bits);
         if (match) put_field(slot, &pos, extract_kept(x, mask, w_bits), m);
         else put_field(slot, &pos, x, w_bits);
@@ -232,7 +246,7 @@ static int decode_row(const unsigned char *slot, int64_t avail, int compressed, 
                       int w_bits, int64_t block_elems, uint32_t mask, uint32_t bitval,
                       unsigned char *orow) {
   const int64_t raw_bytes = row_elems * (w_bits / 8);
-  const int64_t nb = row_elems / block_elems;
+  const int64_t nb = (row_elems + block_elems - 1) / block_elems;
   const int m = w_bits - popcount_w(mask, w_bits);
   if (!compressed) {
     if (avail < raw_bytes) return IBPO_CORRUPT;
@@ -241,12 +255,14 @@ static int decode_row(const unsigned char *slot, int64_t avail, int compressed, 
   }
   if (avail * 8 < nb) return IBPO_CORRUPT;
   int64_t bits = 0;
-  for (int64_t b = 0; b < nb; ++b) bits += 1 + block_elems * (get_bit(slot, b) ? m : w_bits);
+  for (int64_t b = 0; b < nb; ++b)
+    bits += 1 + block_len(b, row_elems, block_elems) * (get_bit(slot, b) ? m : w_bits);
   if (4 * ((bits + 31) / 32) >= raw_bytes || 4 * ((bits + 31) / 32) > avail) return IBPO_CORRUPT;
   int64_t pos = nb; /* first payload bit */
   for (int64_t b = 0; b < nb; ++b) {
     int match = get_bit(slot, b);
-    for (int64_t e = b * block_elems; e < (b + 1) * block_elems; ++e) {
+    for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
+         ++e) {
       uint32_t x;
       if (match) x = reinsert(get_field(slot, &pos, m), mask, bitval, w_bits);
       else x = get_field(slot, &pos, w_bits);
@@ -262,7 +278,7 @@ extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int
                                       const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
                                       const int64_t *idx, int64_t n_idx, void *out) {
   if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
-      row_elems % block_elems != 0 || slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+      slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
     return IBPO_BAD_ARG;
   if (n_idx == 0) return IBPO_OK;
   if (!slots || !bitmask || !idx || !out) return IBPO_BAD_ARG;
@@ -325,8 +341,7 @@ extern "C" int ibpo_decompress_gather_packed(const void *packed, const int64_t *
                                              int64_t block_elems, const uint32_t *bitmask,
                                              uint32_t mask, uint32_t bitval, const int64_t *idx,
                                              int64_t n_idx, void *out) {
-  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
-      row_elems % block_elems != 0)
+  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0)
     return IBPO_BAD_ARG;
   if (n_idx == 0) return IBPO_OK;
   if (!packed || !offsets || !bitmask || !idx || !out) return IBPO_BAD_ARG;
@@ -360,7 +375,7 @@ extern "C" int ibpo_select_meta(const void *rows, int64_t n_rows, int64_t row_el
                                 uint32_t *bitval_out, uint32_t *cand_mask, int64_t *cand_bytes,
                                 int *n_cand) {
   if (!rows || n_rows <= 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
-      row_elems % block_elems != 0 || !(T >= 0.0 && T <= 1.0) || !mask_out || !bitval_out)
+      !(T >= 0.0 && T <= 1.0) || !mask_out || !bitval_out)
     return IBPO_BAD_ARG;
   const int64_t n_elems = n_rows * row_elems;
   uint32_t mask0 = 0, bitval0 = 0;

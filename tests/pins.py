@@ -21,6 +21,8 @@ Compression for ML -- Extended", technical summary, core algorithm):
     +-0, denormals, +-Inf, NaN payloads and all-ones words;
   * decode of the hand-worked stream words (typed in from the golden file, not
     produced by the oracle);
+  * 8-bit words and rows ending in a shorter block: a hand-worked example
+    (tests/golden/hand_example_u8_tail.txt) and the size formula with tails;
   * saving-aware mask selection: two hand-worked examples
     (tests/golden/select_examples.txt) and a threshold sweep (every distinct mask
     the threshold rule gives for thresholds at or above T, plus the empty mask,
@@ -40,10 +42,10 @@ import numpy as np
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
-def load_hand_example():
+def load_hand_example(name: str = "hand_example_fp16.txt", dtype=np.uint16):
     rows, streams = [], []
     d = {}
-    with open(os.path.join(GOLDEN, "hand_example_fp16.txt")) as f:
+    with open(os.path.join(GOLDEN, name)) as f:
         for line in f:
             line = line.strip()
             if not line or line.startswith("#"):
@@ -61,7 +63,7 @@ def load_hand_example():
                 d[key] = float(vals[0])
             elif key == "block":
                 d[key] = int(vals[0])
-    d["rows"] = np.array(rows, dtype=np.uint16)
+    d["rows"] = np.array(rows, dtype=dtype)
     d["streams"] = streams
     return d
 
@@ -175,6 +177,65 @@ def block_matches(rows: np.ndarray, B: int, mask: int, bitval: int) -> np.ndarra
     return ok.reshape(n, L // B, B).all(axis=2)
 
 
+def row_bits_formula(rows: np.ndarray, B: int, mask: int, bitval: int) -> np.ndarray:
+    """Per-row bit counts from the size formula, blocks of B elements and a shorter
+    last block when the row length is not a multiple of B; matches by numpy."""
+    n, L = rows.shape
+    w = 8 * rows.dtype.itemsize
+    m = w - bin(mask).count("1")
+    ok = (rows.astype(np.uint64) & np.uint64(mask)) == np.uint64(bitval)
+    bits = np.zeros(n, dtype=np.int64)
+    for b0 in range(0, L, B):
+        ln = min(B, L - b0)
+        match = ok[:, b0:b0 + ln].all(axis=1)
+        bits += 1 + np.where(match, ln * m, ln * w)
+    return bits
+
+
+def check_hand_example_u8_tail(o):
+    """8-bit words and a two-element last block, worked by hand (golden file)."""
+    d = load_hand_example("hand_example_u8_tail.txt", np.uint8)
+    mask, bitval = o.build_meta(d["rows"], d["T"])
+    assert (mask, bitval) == (d["mask"], d["bitval"]), (hex(mask), hex(bitval))
+    slots, bitmask, row_bits = o.compress(d["rows"], d["block"], mask, bitval)
+    assert list(row_bits) == d["row_bits"], list(row_bits)
+    assert int(bitmask[0]) == d["bitmask"]
+    assert slots[0, :4].view("<u4").tolist() == d["streams"][0]
+    assert np.array_equal(slots[1, :6], d["rows"][1])  # stored raw
+    # decode the typed-in stream
+    typed = np.zeros_like(slots)
+    typed[0, :4] = np.array(d["streams"][0], dtype="<u4").view(np.uint8)
+    typed[1, :6] = d["rows"][1]
+    out, rc = o.decompress_gather(typed, 2, 6, np.uint8, d["block"], bitmask, d["mask"],
+                                  d["bitval"], np.array([1, 0, 0]))
+    assert rc == 0 and np.array_equal(out, d["rows"][[1, 0, 0]])
+
+
+def check_tail_blocks_and_bytes(o):
+    """Rows whose length is not a multiple of B, for 8-, 16- and 32-bit words: bit
+    counts from the formula, the store rule, and lossless round trips."""
+    g = np.random.default_rng(31337)
+    for dt, w, B, L in ((np.uint8, 8, 32, 80), (np.uint8, 8, 64, 100), (np.uint16, 16, 32, 40),
+                        (np.uint32, 32, 64, 72), (np.uint32, 32, 5, 13), (np.uint8, 8, 3, 7),
+                        (np.uint16, 16, 64, 64 + 1)):
+        n = 48
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 2)) - 1))
+        flip = g.random(size=(n, L)) < 0.01
+        x = np.where(flip, base, (base & ~hi) | (np.uint64(0x5A5A5A5A) & hi)).astype(dt)
+        mask, bitval = o.build_meta(x, 0.9)
+        slots, bitmask, row_bits = o.compress(x, B, mask, bitval)
+        exp_bits = row_bits_formula(x, B, mask, bitval)
+        assert np.array_equal(row_bits.astype(np.int64), exp_bits), (w, B, L)
+        raw = L * w // 8
+        exp_flag = 4 * ((exp_bits + 31) // 32) < raw
+        got_flag = (bitmask[np.arange(n) // 32] >> (np.arange(n) % 32).astype(np.uint32)) & 1
+        assert np.array_equal(got_flag.astype(bool), exp_flag), (w, B, L)
+        idx = g.integers(0, n, size=100)
+        out, rc = o.decompress_gather(slots, n, L, dt, B, bitmask, mask, bitval, idx)
+        assert rc == 0 and np.array_equal(out, x[idx]), (w, B, L)
+
+
 def check_size_formula(o):
     g = np.random.default_rng(777)
     cases = [(np.uint32, 32, 32, 128), (np.uint32, 32, 64, 256), (np.uint16, 16, 64, 256),
@@ -257,6 +318,9 @@ def check_stream_layout(o):
 
 
 def special_words(w: int) -> list[int]:
+    if w == 8:  # FP8 E4M3 / E5M2 patterns: +-0, denormals, NaN/Inf encodings, all-ones
+        return [0x00, 0x80, 0x01, 0x07, 0x81, 0x7F, 0xFF, 0x7C, 0xFC, 0x7E, 0x38, 0xB8, 0x08,
+                0x3C]
     if w == 32:
         return [0x00000000, 0x80000000, 0x00000001, 0x007FFFFF, 0x80000001, 0x7F800000,
                 0xFF800000, 0x7FC00000, 0x7FC12345, 0x7F800001, 0xFFFFFFFF, 0x3F800000,
@@ -267,7 +331,7 @@ def special_words(w: int) -> list[int]:
 
 def check_round_trip_specials(o):
     g = np.random.default_rng(99)
-    for dt, w in ((np.uint32, 32), (np.uint16, 16)):
+    for dt, w in ((np.uint32, 32), (np.uint16, 16), (np.uint8, 8)):
         sp = np.array(special_words(w), dtype=dt)
         for B in (1, 2, 4, 8, 32):
             L = B * 4
@@ -444,4 +508,5 @@ def check_pack_round_trip(o):
 ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_meta_closed_forms, check_size_formula, check_stream_layout,
               check_round_trip_specials, check_select_examples,
-              check_select_threshold_sweep, check_pack_hand_example, check_pack_round_trip]
+              check_select_threshold_sweep, check_pack_hand_example, check_pack_round_trip,
+              check_hand_example_u8_tail, check_tail_blocks_and_bytes]

@@ -78,8 +78,12 @@ PLANTED = [
     ("threshold > instead of >=", "(double)cv >= T * (double)n_elems",
      "(double)cv > T * (double)n_elems"),
     ("tie picks 1", "int v = c1 > c0 ? 1 : 0;", "int v = c1 >= c0 ? 1 : 0;"),
-    ("participation bit dropped from size", "bits += 1 + block_elems * (match ? m : w_bits);",
-     "bits += block_elems * (match ? m : w_bits);"),
+    ("participation bit dropped from size",
+     "bits += 1 + block_len(b, row_elems, block_elems) * (match ? m : w_bits);",
+     "bits += block_len(b, row_elems, block_elems) * (match ? m : w_bits);"),
+    ("tail block sized as a full block",
+     "bits += 1 + block_len(b, row_elems, block_elems) * (match ? m : w_bits);",
+     "bits += 1 + block_elems * (match ? m : w_bits);"),
     ("kept bits taken from the mask", "    if (!bit_of(mask, j)) {\n      field",
      "    if (bit_of(mask, j)) {\n      field"),
     ("MSB-first bit order", "  int in_word = (int)(pos % 32);\n  int64_t byte = word * 4 + in_word / 8;\n  int in_byte = in_word % 8;\n  if (bit)",
