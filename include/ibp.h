@@ -19,17 +19,23 @@
  * Conventions shared by every call
  *   - A "row" is the unit stored in one slot (a feature vector, an embedding
  *     row, a weight row, a token's K or V). Rows are row_elems little-endian
- *     element words of w bits: w = 32 (IBP_FP32) or 16 (IBP_FP16, IBP_BF16).
+ *     element words of w bits: w = 32 (IBP_FP32), 16 (IBP_FP16, IBP_BF16) or 8
+ *     (IBP_W8).
  *     Only bit patterns are handled: +-0, denormals, Inf and NaN payloads are
  *     ordinary words and always round-trip exactly.
- *   - block_elems B must be 32 or 64 and divide row_elems; 1 <= row_elems <= 2^20.
+ *   - block_elems B must be 32 or 64; 1 <= row_elems <= 2^20. A row is cut into
+ *     nb = ceil(row_elems / B) blocks; when B does not divide row_elems the last
+ *     block holds the remaining elements (its own participation bit, sized
+ *     1 + len*m or 1 + len*w bits), and the row must then be a multiple of 16
+ *     bytes long (row_elems * w / 8 % 16 == 0).
  *   - Slot r of a store starts at slots + r*slot_bytes; slot_bytes is at least
  *     ibp_slot_bytes() (the raw row rounded up to 16 bytes) and a multiple of 16.
  *   - Stream format of a compressed row (bit i = bit i%32 of little-endian 32-bit
- *     word i/32): nb = row_elems/B participation bits, then each block in order,
- *     either B fields of m = w - popcount(mask) bits (the element's non-invariant
- *     bits, ascending) or B raw words. A row is stored compressed iff
- *     4*ceil(bits/32) < raw bytes, where bits = sum_b (1 + B*m) or (1 + B*w).
+ *     word i/32): nb participation bits, then each block in order, either one
+ *     field of m = w - popcount(mask) bits per element (the element's
+ *     non-invariant bits, ascending) or the raw words. A row is stored compressed
+ *     iff 4*ceil(bits/32) < raw bytes, where bits = sum_b (1 + len_b*m) or
+ *     (1 + len_b*w), len_b = B except for a shorter last block.
  *   - Bitmask: bit r of a store is bit r%32 of 32-bit word r/32.
  *   - Ownership: the caller owns and allocates every buffer; the library
  *     allocates nothing, keeps no per-call state and never synchronises a stream
@@ -57,7 +63,9 @@ extern "C" {
 
 typedef struct CUstream_st *ibp_stream_t; /* same object as cudaStream_t */
 
-typedef enum { IBP_FP32 = 0, IBP_FP16 = 1, IBP_BF16 = 2 } ibp_dtype;
+/* Element word widths: 32 bits (FP32), 16 bits (FP16, BF16), 8 bits (IBP_W8: FP8
+ * E4M3/E5M2, int8, uint8 -- only the width matters, bit patterns are opaque). */
+typedef enum { IBP_FP32 = 0, IBP_FP16 = 1, IBP_BF16 = 2, IBP_W8 = 3 } ibp_dtype;
 
 enum {
   IBP_OK = 0,

@@ -20,13 +20,16 @@ import torch
 
 from . import build_lib
 
-FP32, FP16, BF16 = 0, 1, 2
+FP32, FP16, BF16, W8 = 0, 1, 2, 3
 OK = 0
 ERR_ARG, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_INDEX, ERR_CORRUPT, ERR_META, ERR_TIMEOUT = (
     -1, -2, -3, -4, -5, -6, -7, -8)
 
 _TORCH_DTYPES = {torch.float32: FP32, torch.float16: FP16, torch.bfloat16: BF16}
-WIDTH = {FP32: 32, FP16: 16, BF16: 16}
+for _name in ("float8_e4m3fn", "float8_e5m2"):
+    if hasattr(torch, _name):
+        _TORCH_DTYPES[getattr(torch, _name)] = W8
+WIDTH = {FP32: 32, FP16: 16, BF16: 16, W8: 8}
 
 _lib = None
 

@@ -42,19 +42,25 @@ bool in_device_memory(const void *p) {
   return attr.type == cudaMemoryTypeDevice;
 }
 
-bool dtype_ok(int dtype) { return dtype == IBP_FP32 || dtype == IBP_FP16 || dtype == IBP_BF16; }
+bool dtype_ok(int dtype) {
+  return dtype == IBP_FP32 || dtype == IBP_FP16 || dtype == IBP_BF16 || dtype == IBP_W8;
+}
 
 int make_geom(int64_t row_elems, int dtype, uint32_t block_elems, RowGeom *g) {
   if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
   if (row_elems <= 0 || block_elems == 0) return IBP_ERR_ARG;
-  if (row_elems % block_elems != 0) return IBP_ERR_ARG;
   if (block_elems != 32 && block_elems != 64) return IBP_ERR_UNSUPPORTED;
   if (row_elems > MAX_ROW_ELEMS) return IBP_ERR_UNSUPPORTED;
-  g->w = width_of(dtype);
+  const int w = width_of(dtype);
+  // a shorter last block is allowed when the row is a whole number of 16-byte
+  // vectors (the kernels move rows in 16-byte pieces)
+  if (row_elems % block_elems != 0 && (row_elems * w / 8) % 16 != 0) return IBP_ERR_ARG;
+  g->w = w;
   g->epw = 32 / g->w;
   g->B = (int)block_elems;
   g->lwb = (int)block_elems * g->w / 32;
-  g->nb = (int)(row_elems / block_elems);
+  g->nb = (int)((row_elems + block_elems - 1) / block_elems);
+  g->lwt = (int)((row_elems - (int64_t)(g->nb - 1) * block_elems) * g->w / 32);
   g->raw_words = (int)(row_elems * g->w / 32);
   g->row_elems = row_elems;
   g->raw_bytes = row_elems * g->w / 8;

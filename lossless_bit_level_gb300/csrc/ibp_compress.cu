@@ -42,6 +42,7 @@ struct CompressArgs {
   const ibp_meta *meta;
   uint32_t dtype, block_elems;
   int lwb, lwb_shift, nb, raw_words;
+  int lwt;         // lane words of the last block (lwb, or fewer for a shorter tail)
   int warps;
   int warp_bytes;  // shared bytes per warp
   int hdr_words;   // header words reserved per warp (multiple of 4)
@@ -49,9 +50,11 @@ struct CompressArgs {
   int64_t raw_bytes;
 };
 
-// Encode one staged row. LWB = lane words per block (16, 32 or 64). Lane l works on
-// lane words [128 i + 4 l, 128 i + 4 l + 4) of each 128-word span i; a block is then
-// a group of LWB/4 consecutive lanes of a span.
+// Encode one staged row. LWB = lane words per block (8, 16, 32 or 64). Lane l works
+// on lane words [128 i + 4 l, 128 i + 4 l + 4) of each 128-word span i; a block is
+// then a group of LWB/4 consecutive lanes of a span. A shorter last block covers
+// fewer lanes of its group; the lanes past the row's end vote "match" and so
+// leave the AND to the block's own lanes.
 template <int NR, int LWB>
 __device__ bool compress_row(const CompressArgs &a, const Code &code, const RegRuns<NR> &runs,
                              const SharedRuns &sruns, int64_t r, const uint32_t *RAW,
@@ -65,7 +68,8 @@ __device__ bool compress_row(const CompressArgs &a, const Code &code, const RegR
 
   // b. participation bits: a block's bit is the AND of its lanes' ballot bits,
   // folded with shifts; a span's BPS bits never straddle a header word.
-  uint32_t hacc = 0, cnt_all = 0;
+  uint32_t hacc = 0, cnt_all = 0, last_frag = 0;
+  int last_b0 = 0;
   for (int i = 0; i < nspan; ++i) {
     const int v = 32 * i + lane;
     bool ok = true;
@@ -84,6 +88,8 @@ __device__ bool compress_row(const CompressArgs &a, const Code &code, const RegR
     if (b0 + BPS > a.nb) frag &= low_mask((uint32_t)(a.nb - b0));
     hacc |= frag << (b0 & 31);
     cnt_all += __popc(frag);
+    last_frag = frag;
+    last_b0 = b0;
     if (((b0 + BPS) & 31) == 0 || b0 + BPS >= a.nb) {
       if (lane == 0) HDR[b0 >> 5] = hacc;
       hacc = 0;
@@ -91,7 +97,11 @@ __device__ bool compress_row(const CompressArgs &a, const Code &code, const RegR
   }
   const uint32_t fc = (uint32_t)code.fc;
   const uint32_t shrink = 32u - fc;
-  const uint32_t total = (uint32_t)a.nb + (uint32_t)LWB * (32u * (uint32_t)a.nb - shrink * cnt_all);
+  // bits = nb + sum over blocks of lane words * (p ? fc : 32); every block has LWB
+  // lane words but the last, which has lwt
+  const uint32_t p_last = (last_frag >> (a.nb - 1 - last_b0)) & 1u;
+  const uint32_t total = (uint32_t)a.nb + 32u * (uint32_t)a.raw_words -
+                         shrink * ((uint32_t)LWB * cnt_all - (uint32_t)(LWB - a.lwt) * p_last);
   const uint32_t sw = (total + 31) >> 5;
   const bool comp = (int64_t)sw * 4 < a.raw_bytes;
   if (a.row_bits && lane == 0) a.row_bits[r] = total;
@@ -294,6 +304,7 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
   a.lwb_shift = ilog2(g.lwb);
   a.nb = g.nb;
   a.raw_words = g.raw_words;
+  a.lwt = g.lwt;
   a.raw_bytes = g.raw_bytes;
   a.hdr_words = (((g.nb + 31) / 32) + 3) & ~3;
   // header + two staged raw rows + stream (never longer than the raw row when kept)
@@ -304,6 +315,7 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
   a.n_units = (n_rows + 31) / 32;
   const size_t smem = (size_t)a.warps * a.warp_bytes;
   switch (g.lwb) {
+    case 8: return launch_lwb<8>(a, dev, limit, smem, s);
     case 16: return launch_lwb<16>(a, dev, limit, smem, s);
     case 32: return launch_lwb<32>(a, dev, limit, smem, s);
     default: return launch_lwb<64>(a, dev, limit, smem, s);

@@ -1,11 +1,11 @@
 // Device-side helpers shared by the IBP kernels.
 //
-// All kernels view a row as 32-bit "lane words": an FP32 element, or two 16-bit
-// elements (element 2k in the low half). With the 16-bit mask and bitval copied
-// into both halves, the packed form of a lane word's non-invariant bits is the
-// concatenation of the two elements' fields, low element first -- which is
-// exactly what the stream holds for two consecutive elements of one block. So one
-// code path serves FP32, FP16 and BF16.
+// All kernels view a row as 32-bit "lane words": an FP32 element, two 16-bit
+// elements or four 8-bit ones (the lowest-addressed element in the low bits). With
+// the mask and bitval repeated across the lane word, the packed form of a lane
+// word's non-invariant bits is the concatenation of its elements' fields, low
+// element first -- which is exactly what the stream holds for consecutive
+// elements of one block. So one code path serves every width.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -52,13 +52,22 @@ __device__ __forceinline__ uint32_t window(uint32_t lo, uint32_t hi, uint32_t sh
   return __funnelshift_r(lo, hi, sh);
 }
 
+// A w-bit pattern (w = 8, 16, 32) repeated across a 32-bit lane word.
+__device__ __forceinline__ uint32_t replicate(uint32_t x, int w) {
+  if (w == 8) return (x & 0xFFu) * 0x01010101u;
+  if (w == 16) return (x & 0xFFFFu) * 0x00010001u;
+  return x;
+}
+
+__device__ __forceinline__ int dtype_width(uint32_t dtype) {
+  return dtype == IBP_FP32 ? 32 : (dtype == IBP_W8 ? 8 : 16);
+}
+
 __device__ __forceinline__ Code make_code(const ibp_meta &m) {
   Code c;
-  const bool w16 = m.dtype != IBP_FP32;
-  uint32_t mask = w16 ? (m.mask & 0xFFFFu) : m.mask;
-  uint32_t bitval = (w16 ? (m.bitval & 0xFFFFu) : m.bitval) & mask;
-  c.mask32 = w16 ? (mask | (mask << 16)) : mask;
-  c.bitval32 = w16 ? (bitval | (bitval << 16)) : bitval;
+  const int w = dtype_width(m.dtype);
+  c.mask32 = replicate(m.mask, w);
+  c.bitval32 = replicate(m.bitval, w) & c.mask32;
   c.fc = 32 - __popc(c.mask32);
   return c;
 }

@@ -56,6 +56,7 @@ struct GatherArgs {
   int32_t *status;
   uint32_t dtype, block_elems;
   int lwb, lwb_shift, nb, raw_words;
+  int lwt;  // lane words of the last block (lwb, or fewer for a shorter tail)
   int seg_blocks, nseg;
   int unit_bytes;  // shared staging bytes per unit (one buffer)
   int64_t n_units;
@@ -135,7 +136,9 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
     if (leader) report(a.status, IBP_ERR_INDEX);
     return un;
   }
-  const uint32_t nvec = (uint32_t)(nblk * a.lwb / 4);
+  const bool last_seg = b0 + nblk == a.nb;  // holds the row's last block
+  const uint32_t seg_words = (uint32_t)(nblk * a.lwb - (last_seg ? a.lwb - a.lwt : 0));
+  const uint32_t nvec = seg_words / 4;
   const uint8_t *slot;
   int64_t avail;  // readable bytes of the row's slot or entry
   if (PACKED) {
@@ -178,13 +181,16 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
     if (leader) report(a.status, IBP_ERR_CORRUPT);
     return un;
   }
-  uint32_t cnt_all = 0, cnt0 = 0, lo = 0, hi = 0;
+  uint32_t cnt_all = 0, cnt0 = 0, lo = 0, hi = 0, p_last = 0;
   const int q0 = b0 >> 5;
   for (int q = 0; q < nhw; ++q) {
     uint32_t word = hw[q];
     if (q == q0) lo = word;
     if (q == q0 + 1) hi = word;
-    if (q == nhw - 1) word &= low_mask((uint32_t)(a.nb - 32 * q));
+    if (q == nhw - 1) {
+      word &= low_mask((uint32_t)(a.nb - 32 * q));
+      p_last = (word >> ((a.nb - 1) & 31)) & 1u;
+    }
     const uint32_t c = __popc(word);
     cnt_all += c;
     if (32 * q + 32 <= b0) cnt0 += c;
@@ -192,14 +198,19 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   }
   if (q0 + 1 >= nhw) hi = 0;
   const uint32_t segp = window(lo, hi, (uint32_t)(b0 & 31)) & low_mask((uint32_t)nblk);
-  const uint32_t total = (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * cnt_all);
+  // bits = nb + sum over blocks of lane words * (p ? fc : 32); the last block has
+  // lwt lane words, every other one lwb
+  const uint32_t short_last = (uint32_t)(a.lwb - a.lwt) * p_last;
+  const uint32_t total = (uint32_t)a.nb + 32u * (uint32_t)a.raw_words -
+                         shrink * ((uint32_t)a.lwb * cnt_all - short_last);
   const int64_t used = (int64_t)((total + 31) >> 5) * 4;
   if (used >= a.raw_bytes || (PACKED && used > avail)) {
     if (leader) report(a.status, IBP_ERR_CORRUPT);
     return un;
   }
   const uint32_t st = (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)b0 - shrink * cnt0);
-  const uint32_t en = st + (uint32_t)a.lwb * (32u * (uint32_t)nblk - shrink * __popc(segp));
+  const uint32_t en = st + 32u * seg_words -
+                      shrink * ((uint32_t)a.lwb * __popc(segp) - (last_seg ? short_last : 0u));
   const uint32_t w0 = (st >> 5) & ~3u;
   const uint32_t w1 = ((en + 127) >> 7) << 2;
   un.src = slot + (size_t)w0 * 4;
@@ -241,8 +252,10 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
     } else {  // participation bits are S[0] (one segment, nb <= 32)
       segp = (!PACKED || un.nchunk) ? (S[0] & low_mask((uint32_t)a.nb)) : 0u;
       lsb = (uint32_t)a.nb;
+      const uint32_t p_last = (segp >> (a.nb - 1)) & 1u;
       const uint32_t total =
-          (uint32_t)a.nb + (uint32_t)a.lwb * (32u * (uint32_t)a.nb - shrink * __popc(segp));
+          (uint32_t)a.nb + 32u * (uint32_t)a.raw_words -
+          shrink * ((uint32_t)a.lwb * __popc(segp) - (uint32_t)(a.lwb - a.lwt) * p_last);
       const int64_t used = (int64_t)((total + 31) >> 5) * 4;
       if (used >= a.raw_bytes || (PACKED && used > 16 * (int64_t)un.nchunk)) {
         if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
@@ -743,6 +756,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.lwb_shift = ilog2(g.lwb);
   a.nb = g.nb;
   a.raw_words = g.raw_words;
+  a.lwt = g.lwt;
   a.raw_bytes = g.raw_bytes;
   // Slots in device memory with units of more than 1 KiB: the warp-specialised
   // kernel (planning off the decoders' path pays once a unit takes several vectors

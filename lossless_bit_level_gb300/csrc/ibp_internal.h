@@ -11,17 +11,20 @@ namespace ibp {
 // Row geometry, computed on the host from (row_elems, dtype, block_elems).
 // Kernels work on 32-bit "lane words": one FP32 element or two 16-bit elements.
 struct RowGeom {
-  int w;             // element width in bits (16 or 32)
+  int w;             // element width in bits (8, 16 or 32)
   int epw;           // elements per lane word (32 / w)
   int B;             // block size in elements
-  int lwb;           // lane words per block (B * w / 32): 16, 32 or 64
-  int nb;            // blocks per row
+  int lwb;           // lane words per block (B * w / 32): 8, 16, 32 or 64
+  int lwt;           // lane words of the last block (lwb, or fewer for a shorter tail)
+  int nb;            // blocks per row (ceil(row_elems / B))
   int raw_words;     // lane words per row
   int64_t row_elems; // elements per row
   int64_t raw_bytes; // bytes per raw row
 };
 
-inline int width_of(int dtype) { return dtype == IBP_FP32 ? 32 : 16; }
+inline int width_of(int dtype) {
+  return dtype == IBP_FP32 ? 32 : (dtype == IBP_W8 ? 8 : 16);
+}
 
 // Device properties the launchers size their grids with (cached per device).
 struct DeviceInfo {

@@ -10,8 +10,8 @@
 // (Harley-Seal: ones/twos/fours planes and a ripple counter of "eights"), so a
 // word costs a handful of bitwise operations instead of 32 bit tests; the planes
 // are flushed into 32 per-position totals every 255 steps, then reduced over the
-// warp and added into 32 64-bit global counters. 16-bit elements are counted as
-// halves of 32-bit words and folded in the finalize step.
+// warp and added into 32 64-bit global counters. 8- and 16-bit elements are
+// counted as parts of 32-bit words and folded in the finalize step.
 // meta_finalize_kernel: one warp applies the threshold in IEEE double and writes
 // the 16-byte ibp_meta.
 #include <algorithm>
@@ -130,8 +130,9 @@ __global__ void meta_finalize_kernel(const unsigned long long *counters, int64_t
                                      double T, uint32_t dtype, uint32_t block_elems,
                                      ibp_meta *meta) {
   const int j = threadIdx.x;  // one warp
-  unsigned long long c1 = 0;
-  if (j < w) c1 = (w == 32) ? counters[j] : counters[j] + counters[j + 16];
+  unsigned long long c1 = 0;  // element bit j: bits j, j + w, ... of the 32-bit words
+  if (j < w)
+    for (int q = j; q < 32; q += w) c1 += counters[q];
   const unsigned long long N = (unsigned long long)n_elems;
   const unsigned long long c0 = N - c1;
   const bool v = c1 > c0;  // a tie keeps 0

@@ -53,8 +53,9 @@ struct SelectScratch {
 
 __global__ void select_groups_kernel(SelectScratch *sc, int64_t n_elems, int w, double T) {
   const int j = threadIdx.x;  // one warp; lane j = bit position j
-  unsigned long long c1 = 0;
-  if (j < w) c1 = (w == 32) ? sc->counters[j] : sc->counters[j] + sc->counters[j + 16];
+  unsigned long long c1 = 0;  // element bit j: bits j, j + w, ... of the 32-bit words
+  if (j < w)
+    for (int q = j; q < 32; q += w) c1 += sc->counters[q];
   const unsigned long long N = (unsigned long long)n_elems;
   const unsigned long long c0 = N - c1;
   const bool v = c1 > c0;  // a tie keeps 0
@@ -94,13 +95,16 @@ struct ScoreArgs {
   int vpr;  // 16-byte vectors per row (raw_words / 4)
   int nb;
   int B;
+  int bt;   // elements of the last block (B, or fewer for a shorter tail)
   int w;
   int64_t raw_bytes;
   SelectScratch *sc;
 };
 
-// LWB = 32-bit words per block (16, 32 or 64): a block spans LWB/4 lanes of a
-// 128-word chunk, and a chunk holds 32/(LWB/4) whole blocks.
+// LWB = 32-bit words per block (8, 16, 32 or 64): a block spans LWB/4 lanes of a
+// 128-word chunk, and a chunk holds 32/(LWB/4) whole blocks. A shorter last block
+// spans fewer lanes; the lanes past the row's end load bitval, which adds no
+// mismatch bit, so the OR over the block's lane group is the last block's own.
 //
 // A block's level is the largest level[j] over its mismatch bits j (0 if none):
 // the block matches candidate k iff k >= level. It is read from four 256-entry
@@ -128,17 +132,20 @@ __global__ void __launch_bounds__(SEL_THREADS) select_score_kernel(const ScoreAr
   }
   if (threadIdx.x < 32) s_keep[threadIdx.x] = a.sc->keep[threadIdx.x];
   if (threadIdx.x == 0) {
-    const uint32_t k0 = a.sc->keep[0], bv = a.sc->bitval0;
-    s_M0 = (a.w == 16) ? (k0 | (k0 << 16)) : k0;
-    s_bv2 = (a.w == 16) ? (bv | (bv << 16)) : bv;
+    s_M0 = replicate(a.sc->keep[0], a.w);
+    s_bv2 = replicate(a.sc->bitval0, a.w);
   }
   __syncthreads();
   const uint32_t M0 = s_M0, bv2 = s_bv2;
   const int lane = threadIdx.x & 31;
-  const uint32_t wmask = (a.w == 16) ? 0xFFFFu : 0xFFFFFFFFu;
-  // bits of a matching / a raw block under candidate `lane`
-  const uint32_t bm = (uint32_t)a.B * (uint32_t)(a.w - __popc(s_keep[lane] & wmask));
+  const uint32_t wmask = low_mask((uint32_t)a.w);
+  // field width under candidate `lane`; bits of a matching / a raw full block, and
+  // of the last block matching / raw
+  const uint32_t mk = (uint32_t)(a.w - __popc(s_keep[lane] & wmask));
+  const uint32_t bm = (uint32_t)a.B * mk;
   const uint32_t br = (uint32_t)a.B * (uint32_t)a.w;
+  const uint32_t tm = (uint32_t)a.bt * mk;
+  const uint32_t tr = (uint32_t)a.bt * (uint32_t)a.w;
   const uint32_t raw = (uint32_t)a.raw_bytes;
   const uint32_t nb = (uint32_t)a.nb;
   const int cpr = (a.vpr + 31) / 32;  // chunks per row
@@ -149,7 +156,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_score_kernel(const ScoreAr
   int64_t r = wid * per;
   const int64_t r_end = min(a.n_rows, r + per);
   int c = 0;
-  uint32_t matched = 0;
+  uint32_t matched = 0;    // full blocks of the row matching candidate `lane`
+  bool tail_match = false;  // the row's last block matches it
   unsigned long long acc = 0;
   while (r < r_end) {
     uint4 x[SEL_UNROLL];
@@ -180,10 +188,12 @@ __global__ void __launch_bounds__(SEL_THREADS) select_score_kernel(const ScoreAr
 #pragma unroll
       for (int b = 0; b < BPC; ++b) {
         const int lb = __shfl_sync(FULL, lv, b * LPB);
-        matched += (blk0 + b < nb && lb <= lane) ? 1u : 0u;
+        const uint32_t blk = blk0 + b;
+        if (blk + 1 < nb) matched += (lb <= lane) ? 1u : 0u;
+        else if (blk + 1 == nb) tail_match = lb <= lane;
       }
       if (cc[u] == cpr - 1) {  // the row is complete
-        const uint32_t bits = nb + matched * bm + (nb - matched) * br;
+        const uint32_t bits = nb + matched * bm + (nb - 1 - matched) * br + (tail_match ? tm : tr);
         const uint32_t stored = ((bits + 31u) >> 5) << 2;
         acc += stored < raw ? stored : raw;
         matched = 0;
@@ -279,11 +289,13 @@ int launch_build_meta_select(const void *rows, int64_t n_rows, const RowGeom &g,
   a.vpr = g.raw_words / 4;
   a.nb = g.nb;
   a.B = g.B;
+  a.bt = g.lwt * 32 / g.w;
   a.w = g.w;
   a.raw_bytes = g.raw_bytes;
   a.sc = sc;
   int rc;
   switch (g.lwb) {
+    case 8: rc = launch_score<8>(a, dev, s); break;
     case 16: rc = launch_score<16>(a, dev, s); break;
     case 32: rc = launch_score<32>(a, dev, s); break;
     case 64: rc = launch_score<64>(a, dev, s); break;

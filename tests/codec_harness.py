@@ -8,7 +8,8 @@ import torch
 import lossless_bit_level_gb300 as ibp
 import oracle
 
-INT_VIEW = {np.dtype(np.uint32): (np.int32, torch.int32), np.dtype(np.uint16): (np.int16, torch.int16)}
+INT_VIEW = {np.dtype(np.uint32): (np.int32, torch.int32), np.dtype(np.uint16): (np.int16, torch.int16),
+            np.dtype(np.uint8): (np.uint8, torch.uint8)}
 
 
 def words_of(x: np.ndarray) -> np.ndarray:
@@ -16,7 +17,7 @@ def words_of(x: np.ndarray) -> np.ndarray:
         return x.view(np.uint32)
     if x.dtype == np.float16:
         return x.view(np.uint16)
-    assert x.dtype in (np.uint32, np.uint16), x.dtype
+    assert x.dtype in (np.uint32, np.uint16, np.uint8), x.dtype
     return x
 
 
@@ -79,7 +80,7 @@ def gpu_compress(words_t: torch.Tensor, meta: torch.Tensor, store: GpuStore) -> 
 def gpu_gather(store: GpuStore, meta: torch.Tensor, idx: np.ndarray,
                out: torch.Tensor | None = None) -> tuple[torch.Tensor, int]:
     idx_t = torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int64)).to("cuda")
-    wdt = torch.int32 if ibp.WIDTH[store.dtype] == 32 else torch.int16
+    wdt = {32: torch.int32, 16: torch.int16, 8: torch.uint8}[ibp.WIDTH[store.dtype]]
     if out is None:
         out = torch.zeros((idx.size, store.row_elems), dtype=wdt, device="cuda")
     status = torch.zeros((1,), dtype=torch.int32, device="cuda")

@@ -57,8 +57,13 @@ def test_argument_errors_before_cuda(lib):
     assert lib.ibp_build_meta(vp(16), 10, 128, ibp.FP32, 1.5, 32, vp(16), vp(16), None) == \
         ibp.ERR_ARG
     assert lib.ibp_build_meta(vp(16), 10, 128, 9, 0.9, 32, vp(16), vp(16), None) == ibp.ERR_DTYPE
-    assert lib.ibp_compress(None, 10, 128, ibp.FP32, 48, None, None, 512, None, None, None,
-                            None) == ibp.ERR_ARG  # 128 % 48 != 0
+    assert lib.ibp_compress(None, 10, 98, ibp.FP32, 32, None, None, 400, None, None, None,
+                            None) == ibp.ERR_ARG  # shorter last block, row not 16-byte whole
+    assert lib.ibp_compress(None, 10, 100, ibp.FP32, 32, None, None, 400, None, None, None,
+                            None) == ibp.ERR_ARG  # shorter last block allowed; null pointers
+    assert lib.ibp_compress(None, 10, 100, 7, 32, None, None, 400, None, None, None,
+                            None) == ibp.ERR_DTYPE
+    assert ibp.slot_bytes(40, ibp.W8) == 48
     assert lib.ibp_compress(None, 10, 128, ibp.FP32, 16, None, None, 512, None, None, None,
                             None) == ibp.ERR_UNSUPPORTED
     assert lib.ibp_compress(None, 10, 128, ibp.FP32, 32, None, None, 496, None, None, None,
@@ -98,7 +103,7 @@ def test_argument_errors_before_cuda(lib):
     assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 32, None, None,
                                             None, 3, None, None, None) == ibp.ERR_ARG
     assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 48, None, None,
-                                            None, 3, None, None, None) == ibp.ERR_ARG
+                                            None, 3, None, None, None) == ibp.ERR_UNSUPPORTED
     # contiguous ranges: inside the store, empty is a no-op
     assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, 4, 0, None, None,
                                     None) == ibp.OK

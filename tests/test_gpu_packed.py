@@ -17,7 +17,7 @@ from codec_harness import GpuStore, gpu_compress, gpu_meta, meta_tensor, oracle_
 
 pytestmark = pytest.mark.gpu
 
-FP32, FP16, BF16 = ibp.FP32, ibp.FP16, ibp.BF16
+FP32, FP16, BF16, W8 = ibp.FP32, ibp.FP16, ibp.BF16, ibp.W8
 
 
 class GpuPacked:
@@ -48,7 +48,7 @@ class GpuPacked:
 
 
 def packed_gather(p: GpuPacked, L: int, dtype_code: int, B: int, meta, idx: np.ndarray):
-    wdt = torch.int32 if ibp.WIDTH[dtype_code] == 32 else torch.int16
+    wdt = {32: torch.int32, 16: torch.int16, 8: torch.uint8}[ibp.WIDTH[dtype_code]]
     out = torch.zeros((idx.size, L), dtype=wdt, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ibp.decompress_gather_packed(p.packed, p.offsets, p.n, L, dtype_code, B, p.bitmask, meta,
@@ -123,7 +123,8 @@ def test_llm_down_rows_host():
 
 @pytest.mark.parametrize("dtype_code,np_dt,B,L", [
     (FP32, np.uint32, 32, 96), (FP16, np.uint16, 32, 224), (BF16, np.uint16, 64, 4160),
-    (FP32, np.uint32, 64, 1088)])
+    (FP32, np.uint32, 64, 1088), (FP32, np.uint32, 32, 100), (W8, np.uint8, 32, 48),
+    (W8, np.uint8, 64, 4112)])
 def test_shapes(dtype_code, np_dt, B, L):
     g = np.random.default_rng(L)
     w = 8 * np.dtype(np_dt).itemsize

@@ -15,7 +15,7 @@ from codec_harness import (GpuStore, bitmask_np, compare_slots, from_torch, gpu_
 
 pytestmark = pytest.mark.gpu
 
-FP32, FP16, BF16 = ibp.FP32, ibp.FP16, ibp.BF16
+FP32, FP16, BF16, W8 = ibp.FP32, ibp.FP16, ibp.BF16, ibp.W8
 
 
 def full_check(words: np.ndarray, dtype_code: int, T: float, B: int, idx: np.ndarray,
@@ -87,10 +87,17 @@ def test_llm_kv_rows():
 @pytest.mark.parametrize("dtype_code,np_dt,B,L", [
     (FP32, np.uint32, 32, 96), (FP32, np.uint32, 64, 192), (FP32, np.uint32, 32, 1056),
     (FP16, np.uint16, 32, 32), (FP16, np.uint16, 32, 224), (BF16, np.uint16, 64, 64),
-    (BF16, np.uint16, 32, 11008), (FP16, np.uint16, 64, 4160)])
+    (BF16, np.uint16, 32, 11008), (FP16, np.uint16, 64, 4160),
+    # rows ending in a shorter block (row length not a multiple of B)
+    (FP32, np.uint32, 32, 100), (FP32, np.uint32, 64, 1060), (FP16, np.uint16, 32, 72),
+    (BF16, np.uint16, 64, 4104), (FP32, np.uint32, 64, 4), (BF16, np.uint16, 32, 8),
+    # 8-bit element words (B = 32 is 8 lane words per block)
+    (W8, np.uint8, 32, 128), (W8, np.uint8, 64, 256), (W8, np.uint8, 32, 48),
+    (W8, np.uint8, 64, 4112), (W8, np.uint8, 32, 16), (W8, np.uint8, 64, 2048)])
 def test_shapes_and_ragged_tails(dtype_code, np_dt, B, L):
     """Several tiles, odd block counts (half-used last chunk for 16-bit B=32),
-    multi-segment rows, rows not a multiple of 32 blocks."""
+    multi-segment rows, rows not a multiple of 32 blocks, shorter last blocks
+    (down to a one-vector row), 8-bit words."""
     g = np.random.default_rng(L * 7 + B)
     w = 8 * np.dtype(np_dt).itemsize
     n = 333
@@ -153,14 +160,14 @@ def test_forced_masks_bf16(mask16):
     assert np.array_equal(from_torch(out, np.uint16), words[idx])
 
 
-@pytest.mark.parametrize("w", [32, 16])
+@pytest.mark.parametrize("w", [32, 16, 8])
 def test_special_values_round_trip(w):
     g = np.random.default_rng(w)
-    sp = np.array(pins.special_words(w), dtype=np.uint32 if w == 32 else np.uint16)
+    sp = np.array(pins.special_words(w), dtype={32: np.uint32, 16: np.uint16, 8: np.uint8}[w])
     n, L = 256, 128
     words = sp[g.integers(0, sp.size, size=(n, L))]
     words[: n // 2] = np.where(g.random(size=(n // 2, L)) < 0.97, sp[3], words[: n // 2])
-    dtype_code = FP32 if w == 32 else FP16
+    dtype_code = {32: FP32, 16: FP16, 8: W8}[w]
     for T in (0.0, 0.6, 0.95, 1.0):
         idx = g.integers(0, n, size=512)
         full_check(words, dtype_code, T, 32, idx)

@@ -18,7 +18,7 @@ from codec_harness import GpuStore, gpu_compress, gpu_gather, meta_values, to_to
 
 pytestmark = pytest.mark.gpu
 
-FP32, FP16, BF16 = ibp.FP32, ibp.FP16, ibp.BF16
+FP32, FP16, BF16, W8 = ibp.FP32, ibp.FP16, ibp.BF16, ibp.W8
 
 
 def gpu_select(rows_t: torch.Tensor, dtype_code: int, T: float, B: int):
@@ -79,7 +79,9 @@ def test_workload_prefixes(name):
 @pytest.mark.parametrize("T", [0.0, 0.5, 0.75, 0.9, 1.0])
 @pytest.mark.parametrize("dtype_code,np_dt,B,L", [
     (FP32, np.uint32, 32, 96), (FP32, np.uint32, 64, 1088), (FP16, np.uint16, 32, 224),
-    (BF16, np.uint16, 64, 64), (FP16, np.uint16, 32, 32)])
+    (BF16, np.uint16, 64, 64), (FP16, np.uint16, 32, 32),
+    (FP32, np.uint32, 32, 100), (BF16, np.uint16, 64, 4104), (W8, np.uint8, 32, 48),
+    (W8, np.uint8, 64, 256), (W8, np.uint8, 32, 4112)])
 def test_shapes_and_thresholds(T, dtype_code, np_dt, B, L):
     """Partial last chunk (96, 224 and 1088 words are not multiples of 128), one-block
     rows, many thresholds; exceptions in a high position spread one per block."""
