@@ -163,7 +163,18 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
   const uint32_t *tail = static_cast<const uint32_t *>(rows) + 4 * nvec;
   const int64_t npairs = (nvec + 1) / 2;
   const int64_t want = std::max<int64_t>(1, (npairs + META_THREADS - 1) / META_THREADS);
-  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * 8);
+  // one wave of resident CTAs (the loop is grid-strided; a partial second wave
+  // would run at a fraction of the occupancy)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, meta_count_kernel, META_THREADS, 0) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
   meta_count_kernel<<<grid, META_THREADS, 0, s>>>(static_cast<const uint4 *>(rows), nvec, tail,
                                                   ntail, counters);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
