@@ -540,19 +540,22 @@ def timed_gather(store, batches, out, steps, warmup, flush, barrier):
 def run_e2e(store, host_batches, steps, warmup, dev):
     """Through the public API with host buffers: pinned index batch -> device, gather,
     gathered rows -> pinned host, all inside the timed region of each step. Steps
-    alternate between two streams with their own buffers, so that the read-back of
-    step k (device -> host) overlaps the gather of step k+1 (host -> device); every
-    step still makes both copies."""
+    rotate over four streams with their own buffers, so that the read-back of one
+    step (device -> host) overlaps the gathers of the next ones (host -> device); every
+    step still makes both copies. (Measured: 1, 2, 3, 4 streams give 103, 138, 156,
+    160 GB/s on the dense GNN workload; the host link carries ~340 GB/s in both
+    directions at once.)"""
     n_idx = host_batches[0].numel()
-    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
-    idx_d = [torch.empty(n_idx, dtype=torch.int64, device=dev) for _ in range(2)]
-    out_d = [torch.empty((n_idx, store.L), dtype=store.word_dtype, device=dev) for _ in range(2)]
+    ns = 4
+    streams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
+    idx_d = [torch.empty(n_idx, dtype=torch.int64, device=dev) for _ in range(ns)]
+    out_d = [torch.empty((n_idx, store.L), dtype=store.word_dtype, device=dev) for _ in range(ns)]
     out_h = [torch.empty((n_idx, store.L), dtype=store.word_dtype, pin_memory=True)
-             for _ in range(2)]
+             for _ in range(ns)]
     main = torch.cuda.current_stream()
 
     def step(k):
-        j = k % 2
+        j = k % ns
         with torch.cuda.stream(streams[j]):
             idx_d[j].copy_(host_batches[k % len(host_batches)], non_blocking=True)
             store.gather(idx_d[j], out_d[j])
@@ -574,7 +577,7 @@ def run_e2e(store, host_batches, steps, warmup, dev):
     t = a.elapsed_time(b) * 1e-3 / steps
     return {"value": n_idx * store.raw_bytes / t / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": n_idx * 8, "d2h_bytes_per_step": n_idx * store.raw_bytes,
-            "ms_per_step": t * 1e3, "streams": 2}
+            "ms_per_step": t * 1e3, "streams": ns}
 
 
 # ----------------------------------------------------------------------------- oracle arm
