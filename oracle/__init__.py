@@ -63,6 +63,13 @@ class Oracle:
         lib.ibpo_select_meta.argtypes = [vp, i64, i64, i32, dbl, i64, ctypes.POINTER(u32),
                                          ctypes.POINTER(u32), vp, vp, ctypes.POINTER(i32)]
         lib.ibpo_select_meta.restype = i32
+        lib.ibpo_build_meta_positions.argtypes = [vp, i64, i64, i32, dbl, vp, vp]
+        lib.ibpo_build_meta_positions.restype = i32
+        lib.ibpo_compress_positions.argtypes = [vp, i64, i64, i32, i64, vp, vp, vp, i64, vp, vp]
+        lib.ibpo_compress_positions.restype = i32
+        lib.ibpo_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, i64, vp, vp, vp,
+                                                         vp, i64, vp]
+        lib.ibpo_decompress_gather_positions.restype = i32
         lib.ibpo_pack.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, i64, vp, vp, vp, vp]
         lib.ibpo_pack.restype = i32
         lib.ibpo_decompress_gather_packed.argtypes = [vp, vp, i64, i64, i32, i64, vp, u32, u32,
@@ -84,6 +91,58 @@ class Oracle:
         if rc != OK:
             raise ValueError(f"oracle build_meta rejected its arguments ({rc})")
         return mask.value, bitval.value
+
+    def build_meta_positions(self, rows: np.ndarray, T: float):
+        """Per-position (mask, bitval) arrays, one entry per element position."""
+        a = np.ascontiguousarray(rows)
+        if a.ndim != 2:
+            raise ValueError("rows must be 2-D")
+        w = _width(a)
+        n, L = a.shape
+        pm = np.zeros(L, dtype=np.uint32)
+        pb = np.zeros(L, dtype=np.uint32)
+        rc = self.lib.ibpo_build_meta_positions(_ptr(a), n, L, w, float(T), _ptr(pm), _ptr(pb))
+        if rc != OK:
+            raise ValueError(f"oracle build_meta_positions rejected its arguments ({rc})")
+        return pm, pb
+
+    def compress_positions(self, rows: np.ndarray, block_elems: int, pmask: np.ndarray,
+                           pbitval: np.ndarray, slot_bytes_: int | None = None):
+        a = np.ascontiguousarray(rows)
+        w = _width(a)
+        n, L = a.shape
+        pm = np.ascontiguousarray(pmask, dtype=np.uint32)
+        pb = np.ascontiguousarray(pbitval, dtype=np.uint32)
+        if pm.size != L or pb.size != L:
+            raise ValueError("one mask and bitval per element position")
+        sb = self.slot_bytes(L, w) if slot_bytes_ is None else int(slot_bytes_)
+        slots = np.zeros((n, sb), dtype=np.uint8)
+        bitmask = np.zeros(((n + 31) // 32,), dtype=np.uint32)
+        row_bits = np.zeros((n,), dtype=np.uint32)
+        rc = self.lib.ibpo_compress_positions(_ptr(a), n, L, w, int(block_elems), _ptr(pm),
+                                              _ptr(pb), _ptr(slots), sb, _ptr(bitmask),
+                                              _ptr(row_bits))
+        if rc != OK:
+            raise ValueError(f"oracle compress_positions rejected its arguments ({rc})")
+        return slots, bitmask, row_bits
+
+    def decompress_gather_positions(self, slots, n_rows, row_elems, dtype, block_elems, bitmask,
+                                    pmask, pbitval, idx, out=None):
+        dt = np.dtype(dtype)
+        w = 8 * dt.itemsize
+        s = np.ascontiguousarray(slots)
+        ix = np.ascontiguousarray(idx, dtype=np.int64)
+        bm = np.ascontiguousarray(bitmask, dtype=np.uint32)
+        pm = np.ascontiguousarray(pmask, dtype=np.uint32)
+        pb = np.ascontiguousarray(pbitval, dtype=np.uint32)
+        if out is None:
+            out = np.zeros((ix.size, row_elems), dtype=dt)
+        rc = self.lib.ibpo_decompress_gather_positions(_ptr(s), s.shape[1], n_rows, row_elems, w,
+                                                       int(block_elems), _ptr(bm), _ptr(pm),
+                                                       _ptr(pb), _ptr(ix), ix.size, _ptr(out))
+        if rc == BAD_ARG:
+            raise ValueError("oracle decompress_gather_positions rejected its arguments")
+        return out, rc
 
     def pack(self, slots: np.ndarray, row_elems: int, dtype, bitmask: np.ndarray,
              row_bits: np.ndarray, sel: np.ndarray | None = None):
@@ -227,6 +286,20 @@ def slot_bytes(row_elems: int, w_bits: int) -> int:
 
 def build_meta(elems: np.ndarray, T: float) -> tuple[int, int]:
     return default().build_meta(elems, T)
+
+
+def build_meta_positions(rows, T):
+    return default().build_meta_positions(rows, T)
+
+
+def compress_positions(rows, block_elems, pmask, pbitval, slot_bytes_=None):
+    return default().compress_positions(rows, block_elems, pmask, pbitval, slot_bytes_)
+
+
+def decompress_gather_positions(slots, n_rows, row_elems, dtype, block_elems, bitmask, pmask,
+                                pbitval, idx, out=None):
+    return default().decompress_gather_positions(slots, n_rows, row_elems, dtype, block_elems,
+                                                 bitmask, pmask, pbitval, idx, out)
 
 
 def pack(slots, row_elems, dtype, bitmask, row_bits, sel=None):

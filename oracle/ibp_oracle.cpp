@@ -166,24 +166,65 @@ extern "C" int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, d
   return IBPO_OK;
 }
 
-/* Compression: test each block against mask/bitval, record a participation bit
-   per block, strip the invariant bits of matching blocks and close the gaps,
-   keep failing blocks as they are; store the row in its fixed-size slot and flag
-   it in the bitmask when that saves space. */
-extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
-                             int64_t block_elems, uint32_t mask, uint32_t bitval, void *slots,
-                             int64_t slot_bytes, uint32_t *bitmask, uint32_t *row_bits) {
-  if (!rows || !slots || !bitmask || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) ||
-      block_elems <= 0 ||
-      slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
-    return IBPO_BAD_ARG;
-  mask &= width_mask(w_bits);
-  bitval &= mask;
+namespace {
+
+/* The code rows are compressed with: for every element position e of a row its
+   mask, bitval and field width m. The threshold metadata gives one pair shared by
+   all positions; the per-position variant one pair per position. The arrays run
+   one block past the row (mask 0, field width w) so that block loops never index
+   past them. */
+struct PosCode {
+  std::vector<uint32_t> mask, bitval;
+  std::vector<int> m;
+};
+
+PosCode make_code(const uint32_t *pmask, const uint32_t *pbitval, int shared, int64_t row_elems,
+                  int64_t block_elems, int w_bits) {
+  PosCode c;
+  const int64_t n = row_elems + block_elems;
+  c.mask.assign((size_t)n, 0u);
+  c.bitval.assign((size_t)n, 0u);
+  c.m.assign((size_t)n, w_bits);
+  for (int64_t e = 0; e < row_elems; ++e) {
+    uint32_t mk = (shared ? pmask[0] : pmask[e]) & width_mask(w_bits);
+    c.mask[e] = mk;
+    c.bitval[e] = (shared ? pbitval[0] : pbitval[e]) & mk;
+    c.m[e] = w_bits - popcount_w(mk, w_bits);
+  }
+  return c;
+}
+
+/* payload bits of block b: one field of m_e bits per element when the block
+   matches, the raw w-bit words otherwise */
+int64_t block_payload_bits(const PosCode &c, int64_t b, int64_t row_elems, int64_t block_elems,
+                           int w_bits, int match) {
+  const int64_t len = block_len(b, row_elems, block_elems);
+  int64_t s = 0;
+  for (int64_t i = 0; i < len; ++i) s += match ? c.m[b * block_elems + i] : w_bits;
+  return s;
+}
+
+/* block b matches when every element holds its position's bitval at its
+   position's mask */
+int block_matches(const PosCode &c, const unsigned char *row, int64_t b, int64_t row_elems,
+                  int64_t block_elems, int w_bits) {
+  int match = 1;
+  for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems); ++e)
+    if ((load_elem(row, e, w_bits) & c.mask[e]) != c.bitval[e]) match = 0;
+  return match;
+}
+
+/* Compression: test each block against the code, record a participation bit per
+   block, strip the invariant bits of matching blocks and close the gaps, keep
+   failing blocks as they are; store the row in its fixed-size slot and flag it in
+   the bitmask when that saves space. */
+int compress_rows(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                  int64_t block_elems, const PosCode &c, void *slots, int64_t slot_bytes,
+                  uint32_t *bitmask, uint32_t *row_bits) {
   const unsigned char *in = (const unsigned char *)rows;
   unsigned char *out = (unsigned char *)slots;
   const int64_t raw_bytes = row_elems * (w_bits / 8);
   const int64_t nb = (row_elems + block_elems - 1) / block_elems;
-  const int m = w_bits - popcount_w(mask, w_bits);
 
   for (int64_t q = 0; q < (n_rows + 31) / 32; ++q) bitmask[q] = 0;
 
@@ -194,13 +235,8 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
     /* participation bit per block */
     int64_t bits = 0;
     for (int64_t b = 0; b < nb; ++b) {
-      int match = 1;
-      for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
-           ++e) {
-        uint32_t x = load_elem(row, e, w_bits);
-        if ((x & mask) != bitval) match = 0;
-      }
-      bits += 1 + block_len(b, row_elems, block_elems) * (match ? m : w_bits);
+      int match = block_matches(c, row, b, row_elems, block_elems, w_bits);
+      bits += 1 + block_payload_bits(c, b, row_elems, block_elems, w_bits, match);
     }
     if (row_bits) row_bits[r] = (uint32_t)bits;
 
@@ -214,11 +250,7 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
     int64_t pos = 0;
     /* header: all participation bits first (R2) */
     for (int64_t b = 0; b < nb; ++b) {
-      int match = 1;
-      for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
-           ++e)
-        if ((load_elem(row, e, w_bits) & mask) != bitval) match = 0;
-      put_bit(slot, pos, match);
+      put_bit(slot, pos, block_matches(c, row, b, row_elems, block_elems, w_bits));
       pos += 1;
     }
     /* payloads, block by block */
@@ -227,7 +259,7 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
       for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
            ++e) {
         uint32_t x = load_elem(row, e, w_bits);
-        if (match) put_field(slot, &pos, extract_kept(x, mask, w_bits), m);
+        if (match) put_field(slot, &pos, extract_kept(x, c.mask[e], w_bits), c.m[e]);
         else put_field(slot, &pos, x, w_bits);
       }
     }
@@ -236,18 +268,43 @@ extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems
   return IBPO_OK;
 }
 
+}  // namespace
+
+extern "C" int ibpo_compress(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                             int64_t block_elems, uint32_t mask, uint32_t bitval, void *slots,
+                             int64_t slot_bytes, uint32_t *bitmask, uint32_t *row_bits) {
+  if (!rows || !slots || !bitmask || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) ||
+      block_elems <= 0 || slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+    return IBPO_BAD_ARG;
+  const PosCode c = make_code(&mask, &bitval, 1, row_elems, block_elems, w_bits);
+  return compress_rows(rows, n_rows, row_elems, w_bits, block_elems, c, slots, slot_bytes,
+                       bitmask, row_bits);
+}
+
+extern "C" int ibpo_compress_positions(const void *rows, int64_t n_rows, int64_t row_elems,
+                                       int w_bits, int64_t block_elems, const uint32_t *pmask,
+                                       const uint32_t *pbitval, void *slots, int64_t slot_bytes,
+                                       uint32_t *bitmask, uint32_t *row_bits) {
+  if (!rows || !slots || !bitmask || !pmask || !pbitval || n_rows < 0 || row_elems <= 0 ||
+      !valid_width(w_bits) || block_elems <= 0 || slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+    return IBPO_BAD_ARG;
+  const PosCode c = make_code(pmask, pbitval, 0, row_elems, block_elems, w_bits);
+  return compress_rows(rows, n_rows, row_elems, w_bits, block_elems, c, slots, slot_bytes,
+                       bitmask, row_bits);
+}
+
+namespace {
+
 /* Decompression of one row from its stored bytes (slot or packed entry, `avail`
    bytes of it readable): read the participation bits, walk the blocks in order
    (each block's start is the sum of the sizes of the blocks before it), and
    rebuild every element by putting the invariant bits back in place. Returns
    IBPO_OK, or IBPO_CORRUPT (orow untouched) when the stream the participation bits
    describe would not have been stored compressed or does not fit `avail`. */
-static int decode_row(const unsigned char *slot, int64_t avail, int compressed, int64_t row_elems,
-                      int w_bits, int64_t block_elems, uint32_t mask, uint32_t bitval,
-                      unsigned char *orow) {
+int decode_row(const unsigned char *slot, int64_t avail, int compressed, int64_t row_elems,
+               int w_bits, int64_t block_elems, const PosCode &c, unsigned char *orow) {
   const int64_t raw_bytes = row_elems * (w_bits / 8);
   const int64_t nb = (row_elems + block_elems - 1) / block_elems;
-  const int m = w_bits - popcount_w(mask, w_bits);
   if (!compressed) {
     if (avail < raw_bytes) return IBPO_CORRUPT;
     for (int64_t k = 0; k < raw_bytes; ++k) orow[k] = slot[k];
@@ -256,7 +313,7 @@ static int decode_row(const unsigned char *slot, int64_t avail, int compressed, 
   if (avail * 8 < nb) return IBPO_CORRUPT;
   int64_t bits = 0;
   for (int64_t b = 0; b < nb; ++b)
-    bits += 1 + block_len(b, row_elems, block_elems) * (get_bit(slot, b) ? m : w_bits);
+    bits += 1 + block_payload_bits(c, b, row_elems, block_elems, w_bits, get_bit(slot, b));
   if (4 * ((bits + 31) / 32) >= raw_bytes || 4 * ((bits + 31) / 32) > avail) return IBPO_CORRUPT;
   int64_t pos = nb; /* first payload bit */
   for (int64_t b = 0; b < nb; ++b) {
@@ -264,7 +321,7 @@ static int decode_row(const unsigned char *slot, int64_t avail, int compressed, 
     for (int64_t e = b * block_elems; e < b * block_elems + block_len(b, row_elems, block_elems);
          ++e) {
       uint32_t x;
-      if (match) x = reinsert(get_field(slot, &pos, m), mask, bitval, w_bits);
+      if (match) x = reinsert(get_field(slot, &pos, c.m[e]), c.mask[e], c.bitval[e], w_bits);
       else x = get_field(slot, &pos, w_bits);
       store_elem(orow, e, w_bits, x);
     }
@@ -272,18 +329,9 @@ static int decode_row(const unsigned char *slot, int64_t avail, int compressed, 
   return IBPO_OK;
 }
 
-/* Decompression-gather: rebuild each requested row from its slot. */
-extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
-                                      int64_t row_elems, int w_bits, int64_t block_elems,
-                                      const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
-                                      const int64_t *idx, int64_t n_idx, void *out) {
-  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
-      slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
-    return IBPO_BAD_ARG;
-  if (n_idx == 0) return IBPO_OK;
-  if (!slots || !bitmask || !idx || !out) return IBPO_BAD_ARG;
-  mask &= width_mask(w_bits);
-  bitval &= mask;
+int gather_rows(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems,
+                int w_bits, int64_t block_elems, const uint32_t *bitmask, const PosCode &c,
+                const int64_t *idx, int64_t n_idx, void *out) {
   const unsigned char *in = (const unsigned char *)slots;
   unsigned char *dst = (unsigned char *)out;
   const int64_t raw_bytes = row_elems * (w_bits / 8);
@@ -296,10 +344,63 @@ extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int
     }
     int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);
     int rc = decode_row(in + r * slot_bytes, slot_bytes, compressed, row_elems, w_bits,
-                        block_elems, mask, bitval, dst + i * raw_bytes);
+                        block_elems, c, dst + i * raw_bytes);
     if (rc != IBPO_OK && status == IBPO_OK) status = rc;
   }
   return status;
+}
+
+}  // namespace
+
+/* Decompression-gather: rebuild each requested row from its slot. */
+extern "C" int ibpo_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                      int64_t row_elems, int w_bits, int64_t block_elems,
+                                      const uint32_t *bitmask, uint32_t mask, uint32_t bitval,
+                                      const int64_t *idx, int64_t n_idx, void *out) {
+  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
+      slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+    return IBPO_BAD_ARG;
+  if (n_idx == 0) return IBPO_OK;
+  if (!slots || !bitmask || !idx || !out) return IBPO_BAD_ARG;
+  const PosCode c = make_code(&mask, &bitval, 1, row_elems, block_elems, w_bits);
+  return gather_rows(slots, slot_bytes, n_rows, row_elems, w_bits, block_elems, bitmask, c, idx,
+                     n_idx, out);
+}
+
+extern "C" int ibpo_decompress_gather_positions(const void *slots, int64_t slot_bytes,
+                                                int64_t n_rows, int64_t row_elems, int w_bits,
+                                                int64_t block_elems, const uint32_t *bitmask,
+                                                const uint32_t *pmask, const uint32_t *pbitval,
+                                                const int64_t *idx, int64_t n_idx, void *out) {
+  if (n_idx < 0 || n_rows < 0 || row_elems <= 0 || !valid_width(w_bits) || block_elems <= 0 ||
+      slot_bytes < ibpo_slot_bytes(row_elems, w_bits))
+    return IBPO_BAD_ARG;
+  if (n_idx == 0) return IBPO_OK;
+  if (!slots || !bitmask || !idx || !out || !pmask || !pbitval) return IBPO_BAD_ARG;
+  const PosCode c = make_code(pmask, pbitval, 0, row_elems, block_elems, w_bits);
+  return gather_rows(slots, slot_bytes, n_rows, row_elems, w_bits, block_elems, bitmask, c, idx,
+                     n_idx, out);
+}
+
+/* Per-position metadata: the preprocessing rule applied to each element position
+   of a row on its own (the sample of position e is element e of every row). */
+extern "C" int ibpo_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems,
+                                         int w_bits, double T, uint32_t *pmask_out,
+                                         uint32_t *pbitval_out) {
+  if (!rows || n_rows <= 0 || row_elems <= 0 || !valid_width(w_bits) || !pmask_out ||
+      !pbitval_out)
+    return IBPO_BAD_ARG;
+  const unsigned char *base = (const unsigned char *)rows;
+  const int nbytes = w_bits / 8;
+  std::vector<unsigned char> column((size_t)(n_rows * nbytes));
+  for (int64_t e = 0; e < row_elems; ++e) {
+    for (int64_t r = 0; r < n_rows; ++r)
+      for (int k = 0; k < nbytes; ++k)
+        column[(size_t)(r * nbytes + k)] = base[(r * row_elems + e) * nbytes + k];
+    int rc = ibpo_build_meta(column.data(), n_rows, w_bits, T, &pmask_out[e], &pbitval_out[e]);
+    if (rc != IBPO_OK) return rc;
+  }
+  return IBPO_OK;
 }
 
 /* Packed store: each selected row's used bytes, rounded up to 16, end to end. */
@@ -345,8 +446,7 @@ extern "C" int ibpo_decompress_gather_packed(const void *packed, const int64_t *
     return IBPO_BAD_ARG;
   if (n_idx == 0) return IBPO_OK;
   if (!packed || !offsets || !bitmask || !idx || !out) return IBPO_BAD_ARG;
-  mask &= width_mask(w_bits);
-  bitval &= mask;
+  const PosCode c = make_code(&mask, &bitval, 1, row_elems, block_elems, w_bits);
   const unsigned char *in = (const unsigned char *)packed;
   unsigned char *dst = (unsigned char *)out;
   const int64_t raw_bytes = row_elems * (w_bits / 8);
@@ -361,7 +461,7 @@ extern "C" int ibpo_decompress_gather_packed(const void *packed, const int64_t *
     int64_t avail = offsets[r + 1] - offsets[r];
     int rc = avail < 0 ? IBPO_CORRUPT
                        : decode_row(in + offsets[r], avail, compressed, row_elems, w_bits,
-                                    block_elems, mask, bitval, dst + i * raw_bytes);
+                                    block_elems, c, dst + i * raw_bytes);
     if (rc != IBPO_OK && status == IBPO_OK) status = rc;
   }
   return status;

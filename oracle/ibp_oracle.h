@@ -55,6 +55,27 @@ extern "C" {
 int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, double T,
                     uint32_t *mask_out, uint32_t *bitval_out);
 
+/* Per-position metadata (a variant of preprocessing: the "kilobyte-scale"
+ * metadata reading). Element position e of a row (0 <= e < row_elems) gets its own
+ * mask/bitval pair: the preprocessing rule of ibpo_build_meta applied to the
+ * sample made of element e of every row. pmask_out/pbitval_out: row_elems words. */
+int ibpo_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                              double T, uint32_t *pmask_out, uint32_t *pbitval_out);
+
+/* Compression and decompress-gather with per-position metadata: as ibpo_compress /
+ * ibpo_decompress_gather, except that element e of a block is tested against
+ * pmask[e]/pbitval[e] and, in a matching block, stored as a field of
+ * w - popcount(pmask[e]) bits (its non-invariant bits in ascending order). */
+int ibpo_compress_positions(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
+                            int64_t block_elems, const uint32_t *pmask, const uint32_t *pbitval,
+                            void *slots, int64_t slot_bytes, uint32_t *bitmask,
+                            uint32_t *row_bits);
+int ibpo_decompress_gather_positions(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                     int64_t row_elems, int w_bits, int64_t block_elems,
+                                     const uint32_t *bitmask, const uint32_t *pmask,
+                                     const uint32_t *pbitval, const int64_t *idx, int64_t n_idx,
+                                     void *out);
+
 /* Packed store (technical summary, "System integration": the compressed GPU
  * cache that raises the cache's effective capacity). Rows sel[0..n_sel) of a
  * slotted store (sel == NULL: rows 0..n_sel) are laid end to end: entry i holds the

@@ -23,6 +23,9 @@ Compression for ML -- Extended", technical summary, core algorithm):
     produced by the oracle);
   * 8-bit words and rows ending in a shorter block: a hand-worked example
     (tests/golden/hand_example_u8_tail.txt) and the size formula with tails;
+  * per-position metadata: a hand-worked example (tests/golden/positions_example_u8.txt),
+    the rule checked column by column against the brute-force count, sizes with
+    per-element field widths, and equal masks reproducing the shared-mask stream;
   * saving-aware mask selection: two hand-worked examples
     (tests/golden/select_examples.txt) and a threshold sweep (every distinct mask
     the threshold rule gives for thresholds at or above T, plus the empty mask,
@@ -63,6 +66,8 @@ def load_hand_example(name: str = "hand_example_fp16.txt", dtype=np.uint16):
                 d[key] = float(vals[0])
             elif key == "block":
                 d[key] = int(vals[0])
+            elif key in ("pmask", "pbitval"):
+                d[key] = [int(v, 16) for v in vals]
     d["rows"] = np.array(rows, dtype=dtype)
     d["streams"] = streams
     return d
@@ -234,6 +239,63 @@ def check_tail_blocks_and_bytes(o):
         idx = g.integers(0, n, size=100)
         out, rc = o.decompress_gather(slots, n, L, dt, B, bitmask, mask, bitval, idx)
         assert rc == 0 and np.array_equal(out, x[idx]), (w, B, L)
+
+
+def check_positions_hand_example(o):
+    """Per-position metadata on the hand-worked 8-bit rows (golden file)."""
+    d = load_hand_example("positions_example_u8.txt", np.uint8)
+    pm, pb = o.build_meta_positions(d["rows"], d["T"])
+    assert pm.tolist() == d["pmask"] and pb.tolist() == d["pbitval"], (pm, pb)
+    assert o.build_meta(d["rows"], d["T"]) == (0, 0)  # one shared mask finds nothing
+    slots, bitmask, row_bits = o.compress_positions(d["rows"], d["block"], pm, pb)
+    assert list(row_bits) == d["row_bits"]
+    assert int(bitmask[0]) == d["bitmask"]
+    for r, words in enumerate(d["streams"]):
+        assert slots[r, :4].view("<u4").tolist() == words, (r, slots[r, :4].view("<u4"))
+    typed = np.zeros_like(slots)
+    for r, words in enumerate(d["streams"]):
+        typed[r, :4] = np.array(words, dtype="<u4").view(np.uint8)
+    idx = np.array([3, 0, 2, 1, 1])
+    out, rc = o.decompress_gather_positions(typed, 4, 8, np.uint8, d["block"], bitmask,
+                                            np.array(d["pmask"]), np.array(d["pbitval"]), idx)
+    assert rc == 0 and np.array_equal(out, d["rows"][idx])
+
+
+def check_positions_meta_and_sizes(o):
+    """Per-position metadata equals the brute-force rule column by column; row sizes
+    follow the size formula with per-element field widths; equal masks at every
+    position reproduce the shared-mask stream byte for byte; round trips."""
+    g = np.random.default_rng(2024)
+    for dt, w, B, L in ((np.uint32, 32, 32, 64), (np.uint16, 16, 8, 40), (np.uint8, 8, 4, 22)):
+        n = 60
+        colconst = g.integers(0, 1 << w, size=L, dtype=np.uint64)
+        colhi = np.array([((1 << w) - 1) ^ ((1 << int(k)) - 1) for k in
+                          g.integers(1, w, size=L)], dtype=np.uint64)
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        flip = g.random(size=(n, L)) < 0.02
+        x = np.where(flip, base, (base & ~colhi) | (colconst & colhi)).astype(dt)
+        for T in (0.9, 1.0):
+            pm, pb = o.build_meta_positions(x, T)
+            for e in range(L):
+                assert (int(pm[e]), int(pb[e])) == brute_meta(x[:, e], T), (w, e)
+            slots, bitmask, row_bits = o.compress_positions(x, B, pm, pb)
+            m = w - np.array([bin(int(v)).count("1") for v in pm])
+            ok = (x.astype(np.uint64) & pm.astype(np.uint64)) == pb.astype(np.uint64)
+            bits = np.zeros(n, dtype=np.int64)
+            for b0 in range(0, L, B):
+                sl = slice(b0, min(b0 + B, L))
+                match = ok[:, sl].all(axis=1)
+                bits += 1 + np.where(match, m[sl].sum(), (sl.stop - sl.start) * w)
+            assert np.array_equal(row_bits.astype(np.int64), bits), (w, T)
+            idx = g.integers(0, n, size=80)
+            out, rc = o.decompress_gather_positions(slots, n, L, dt, B, bitmask, pm, pb, idx)
+            assert rc == 0 and np.array_equal(out, x[idx])
+        # one mask repeated at every position = the shared-mask code
+        mask, bitval = o.build_meta(x, 0.9)
+        s1, b1, r1 = o.compress(x, B, mask, bitval)
+        s2, b2, r2 = o.compress_positions(x, B, np.full(L, mask, np.uint32),
+                                          np.full(L, bitval, np.uint32))
+        assert np.array_equal(s1, s2) and np.array_equal(b1, b2) and np.array_equal(r1, r2)
 
 
 def check_size_formula(o):
@@ -509,4 +571,5 @@ ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_meta_closed_forms, check_size_formula, check_stream_layout,
               check_round_trip_specials, check_select_examples,
               check_select_threshold_sweep, check_pack_hand_example, check_pack_round_trip,
-              check_hand_example_u8_tail, check_tail_blocks_and_bytes]
+              check_hand_example_u8_tail, check_tail_blocks_and_bytes,
+              check_positions_hand_example, check_positions_meta_and_sizes]

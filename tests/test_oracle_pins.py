@@ -79,11 +79,11 @@ PLANTED = [
      "(double)cv > T * (double)n_elems"),
     ("tie picks 1", "int v = c1 > c0 ? 1 : 0;", "int v = c1 >= c0 ? 1 : 0;"),
     ("participation bit dropped from size",
-     "bits += 1 + block_len(b, row_elems, block_elems) * (match ? m : w_bits);",
-     "bits += block_len(b, row_elems, block_elems) * (match ? m : w_bits);"),
+     "bits += 1 + block_payload_bits(c, b, row_elems, block_elems, w_bits, match);",
+     "bits += block_payload_bits(c, b, row_elems, block_elems, w_bits, match);"),
     ("tail block sized as a full block",
-     "bits += 1 + block_len(b, row_elems, block_elems) * (match ? m : w_bits);",
-     "bits += 1 + block_elems * (match ? m : w_bits);"),
+     "const int64_t len = block_len(b, row_elems, block_elems);",
+     "const int64_t len = block_elems;"),
     ("kept bits taken from the mask", "    if (!bit_of(mask, j)) {\n      field",
      "    if (bit_of(mask, j)) {\n      field"),
     ("MSB-first bit order", "  int in_word = (int)(pos % 32);\n  int64_t byte = word * 4 + in_word / 8;\n  int in_byte = in_word % 8;\n  if (bit)",
@@ -108,6 +108,12 @@ PLANTED = [
     ("packed entry length not checked",
      "if (4 * ((bits + 31) / 32) >= raw_bytes || 4 * ((bits + 31) / 32) > avail) return IBPO_CORRUPT;",
      "if (4 * ((bits + 31) / 32) >= raw_bytes) return IBPO_CORRUPT;"),
+    ("positions use the first position's mask",
+     "uint32_t mk = (shared ? pmask[0] : pmask[e]) & width_mask(w_bits);",
+     "uint32_t mk = (shared ? pmask[0] : pmask[0]) & width_mask(w_bits);"),
+    ("positions metadata samples position 0 only",
+     "column[(size_t)(r * nbytes + k)] = base[(r * row_elems + e) * nbytes + k];",
+     "column[(size_t)(r * nbytes + k)] = base[(r * row_elems) * nbytes + k];"),
     ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
      "*bitval_out = bitval0;"),
 ]
