@@ -210,8 +210,28 @@ def measure_link(dev, nbytes=1 << 30, reps=10):
         b.record(s)
         b.synchronize()
         best_probe = max(best_probe, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    # both directions at once (two streams, half the buffer each way): the
+    # denominator of the end-to-end leg, whose steps move rows both ways
+    half = nbytes // 2
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    best_bidir = 0.0
+    for _ in range(reps):
+        a, b = event_pair(s)
+        a.record(s)
+        s1.wait_event(a)
+        s2.wait_event(a)
+        with torch.cuda.stream(s1):
+            d[:half].copy_(host[:half], non_blocking=True)
+        with torch.cuda.stream(s2):
+            host[half:].copy_(d[half:], non_blocking=True)
+        s.wait_stream(s1)
+        s.wait_stream(s2)
+        b.record(s)
+        b.synchronize()
+        best_bidir = max(best_bidir, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
     del host, d
     return {"h2d_memcpy_gbs": best_h2d, "d2h_memcpy_gbs": best_d2h,
+            "bidirectional_memcpy_gbs": best_bidir,
             "zero_copy_read_gbs": best_probe, "bytes": nbytes, "reps": reps}
 
 
@@ -833,6 +853,18 @@ def main():
                 "clocks": clk_h}
             del dstore
         extra["e2e"] = run_e2e(store, host_batches, max(20, steps // 10), warmup, dev)
+        if residency == "host":
+            # bytes over the link per step: the rows the gather reads (the ncu-measured
+            # link bytes when recorded, else the stored bytes), the index batch up,
+            # the rows back down
+            up = (rec["sysmem_read_bytes"] if rec else stored_per_step) + wl["batch"] * 8
+            both = up + out_bytes
+            t_e = extra["e2e"]["ms_per_step"] * 1e-3
+            extra["e2e"]["roofline"] = {
+                "bound": "host_link_both_directions", "achieved": both / t_e / 1e9,
+                "peak": link["bidirectional_memcpy_gbs"], "unit": "GB/s",
+                "frac": both / t_e / 1e9 / link["bidirectional_memcpy_gbs"],
+                "link_bytes_per_step": both}
         # preprocessing stages with rows and slots in HBM
         if residency == "host":
             dstore = Store.__new__(Store)

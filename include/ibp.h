@@ -256,6 +256,40 @@ int ibp_decompress_range(const void *slots, int64_t slot_bytes, int64_t n_rows, 
                          const ibp_meta *d_meta, int64_t row_begin, int64_t n_out, void *out,
                          int32_t *d_status, ibp_stream_t s);
 
+/* Per-position metadata (a variant of preprocessing: the "kilobyte-scale" metadata
+ * reading of "Core algorithm"; the paper fixes no layout, this one is the
+ * library's). Element position e of a row (0 <= e < row_elems) has its own
+ * mask/bitval pair, d_pmask[e] / d_pbitval[e] (w-bit values in uint32 words,
+ * device memory, row_elems entries each): the preprocessing rule of ibp_build_meta
+ * applied to the sample made of element e of every row. A block matches when each
+ * of its elements e satisfies (x & pmask[e]) == pbitval[e]; a matching element is
+ * stored as a field of w - popcount(pmask[e]) bits (its non-invariant bits,
+ * ascending). Participation bits, bit order, shorter last blocks and the store rule
+ * are those of the shared-mask format. Rows of at most 16 KiB (else
+ * IBP_ERR_UNSUPPORTED); the argument checks of the shared-mask calls apply.
+ * ibp_meta_positions_scratch_bytes: device scratch of ibp_build_meta_positions (8
+ * bytes per bit of a row). */
+int ibp_meta_positions_scratch_bytes(int64_t row_elems, int dtype, size_t *bytes);
+
+int ibp_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                             double T, uint32_t block_elems, uint32_t *d_pmask,
+                             uint32_t *d_pbitval, void *d_scratch, ibp_stream_t s);
+
+/* ibp_compress with per-position metadata (no *d_meta; no device-detected errors). */
+int ibp_compress_positions(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                           uint32_t block_elems, const uint32_t *d_pmask,
+                           const uint32_t *d_pbitval, void *slots, int64_t slot_bytes,
+                           uint32_t *d_row_bitmask, uint32_t *d_row_bits, ibp_stream_t s);
+
+/* ibp_decompress_gather with per-position metadata. Each requested row's slot is
+ * staged whole (its raw-size prefix). */
+int ibp_decompress_gather_positions(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                    int64_t row_elems, int dtype, uint32_t block_elems,
+                                    const uint32_t *d_row_bitmask, const uint32_t *d_pmask,
+                                    const uint32_t *d_pbitval, const int64_t *d_idx,
+                                    int64_t n_idx, void *out, int32_t *d_status,
+                                    ibp_stream_t s);
+
 /* Statistics of a store: reduces the bitmask and the per-row bit counts written
  * by ibp_compress into *d_stats (device memory), asynchronously on s. */
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,

@@ -50,7 +50,8 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_compress", "ibp_decompress_gather", "ibp_query", "ibp_probe_read",
            "ibp_build_meta_noalloc", "ibp_meta_select_scratch_bytes", "ibp_build_meta_select",
            "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed",
-           "ibp_decompress_range")
+           "ibp_decompress_range", "ibp_meta_positions_scratch_bytes", "ibp_build_meta_positions",
+           "ibp_compress_positions", "ibp_decompress_gather_positions")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -84,6 +85,11 @@ def load() -> ctypes.CDLL:
     lib.ibp_meta_select_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
     lib.ibp_build_meta_select.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
     u64 = ctypes.c_uint64
+    lib.ibp_meta_positions_scratch_bytes.argtypes = [i64, i32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.ibp_build_meta_positions.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
+    lib.ibp_compress_positions.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
+    lib.ibp_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp,
+                                                    i64, vp, vp, vp]
     lib.ibp_decompress_range.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, i64, i64, vp, vp, vp]
     lib.ibp_pack_scratch_bytes.argtypes = [i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.ibp_pack_offsets.argtypes = [vp, vp, i64, i64, i32, vp, i64, vp, vp, vp, vp]
@@ -268,6 +274,53 @@ def decompress_gather_packed(packed: torch.Tensor, offsets: torch.Tensor, n_rows
         _ptr(packed), packed.numel() * packed.element_size(), _ptr(offsets), int(n_rows),
         int(row_elems), int(dtype), int(block_elems), _ptr(bitmask), _ptr(meta), _ptr(idx),
         idx.numel(), _ptr(out), _ptr(status), _stream(stream)), "ibp_decompress_gather_packed")
+
+
+def meta_positions_scratch_bytes(row_elems: int, dtype: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().ibp_meta_positions_scratch_bytes(int(row_elems), int(dtype), ctypes.byref(out)),
+           "ibp_meta_positions_scratch_bytes")
+    return out.value
+
+
+def build_meta_positions(rows: torch.Tensor, T: float, block_elems: int, pmask: torch.Tensor,
+                         pbitval: torch.Tensor, scratch: torch.Tensor, dtype: int | None = None,
+                         stream=None) -> None:
+    """ibp_build_meta_positions: one mask/bitval per element position of a row."""
+    n, L = _rows_shape(rows)
+    _check(load().ibp_build_meta_positions(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
+                                           int(block_elems), _ptr(pmask), _ptr(pbitval),
+                                           _ptr(scratch), _stream(stream)),
+           "ibp_build_meta_positions")
+
+
+def compress_positions(rows: torch.Tensor, block_elems: int, pmask: torch.Tensor,
+                       pbitval: torch.Tensor, slots: torch.Tensor, bitmask: torch.Tensor,
+                       row_bits: torch.Tensor | None = None, dtype: int | None = None,
+                       stream=None) -> None:
+    """ibp_compress_positions: encode ``rows`` with per-position metadata."""
+    n, L = _rows_shape(rows)
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(n, 1)
+    _check(load().ibp_compress_positions(_ptr(rows), n, L, dtype_code(rows, dtype),
+                                         int(block_elems), _ptr(pmask), _ptr(pbitval),
+                                         _ptr(slots), sb, _ptr(bitmask), _ptr(row_bits),
+                                         _stream(stream)), "ibp_compress_positions")
+
+
+def decompress_gather_positions(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
+                                block_elems: int, bitmask: torch.Tensor, pmask: torch.Tensor,
+                                pbitval: torch.Tensor, idx: torch.Tensor, out: torch.Tensor,
+                                status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_decompress_gather_positions: rows ``idx`` rebuilt with per-position metadata."""
+    if idx.dtype != torch.int64:
+        raise ValueError("idx must be int64")
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(int(n_rows), 1)
+    _check(load().ibp_decompress_gather_positions(
+        _ptr(slots), sb, int(n_rows), int(row_elems), int(dtype), int(block_elems),
+        _ptr(bitmask), _ptr(pmask), _ptr(pbitval), _ptr(idx), idx.numel(), _ptr(out),
+        _ptr(status), _stream(stream)), "ibp_decompress_gather_positions")
 
 
 def decompress_range(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,

@@ -360,6 +360,74 @@ int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
                        in_device_memory(packed), reinterpret_cast<cudaStream_t>(s));
 }
 
+// Per-position variant: rows of at most 16 KiB (the per-lane-word tables and two
+// staged rows per warp live in shared memory).
+constexpr int64_t POS_MAX_ROW_BYTES = 16384;
+
+int ibp_meta_positions_scratch_bytes(int64_t row_elems, int dtype, size_t *bytes) {
+  if (!bytes) return IBP_ERR_ARG;
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (row_elems <= 0 || row_elems > MAX_ROW_ELEMS) return IBP_ERR_ARG;
+  // one 64-bit counter per bit of a row's 32-bit lane words
+  *bytes = (size_t)((row_elems * width_of(dtype) + 31) / 32) * 32 * 8;
+  return IBP_OK;
+}
+
+int ibp_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                             double T, uint32_t block_elems, uint32_t *d_pmask,
+                             uint32_t *d_pbitval, void *d_scratch, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (g.raw_bytes > POS_MAX_ROW_BYTES) return IBP_ERR_UNSUPPORTED;
+  if (n_rows <= 0 || !(T >= 0.0 && T <= 1.0)) return IBP_ERR_ARG;
+  if (!pointer_ok(rows, Where::device_or_host, 16) || !pointer_ok(d_pmask, Where::device_only, 4) ||
+      !pointer_ok(d_pbitval, Where::device_only, 4) ||
+      !pointer_ok(d_scratch, Where::device_only, 8))
+    return IBP_ERR_ARG;
+  return launch_build_meta_positions(rows, n_rows, g, T, d_pmask, d_pbitval, d_scratch,
+                                     reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_compress_positions(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                           uint32_t block_elems, const uint32_t *d_pmask,
+                           const uint32_t *d_pbitval, void *slots, int64_t slot_bytes,
+                           uint32_t *d_row_bitmask, uint32_t *d_row_bits, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (g.raw_bytes > POS_MAX_ROW_BYTES) return IBP_ERR_UNSUPPORTED;
+  if (n_rows < 0 || slot_bytes < slot_bytes_of(g) || slot_bytes % 16 != 0) return IBP_ERR_ARG;
+  if (n_rows == 0) return IBP_OK;
+  if (!pointer_ok(rows, Where::device_or_host, 16) || !pointer_ok(slots, Where::device_or_host, 16) ||
+      !pointer_ok(d_pmask, Where::device_only, 4) || !pointer_ok(d_pbitval, Where::device_only, 4) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      (d_row_bits && !pointer_ok(d_row_bits, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_compress_positions(rows, n_rows, g, d_pmask, d_pbitval, slots, slot_bytes,
+                                   d_row_bitmask, d_row_bits, reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_decompress_gather_positions(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                    int64_t row_elems, int dtype, uint32_t block_elems,
+                                    const uint32_t *d_row_bitmask, const uint32_t *d_pmask,
+                                    const uint32_t *d_pbitval, const int64_t *d_idx,
+                                    int64_t n_idx, void *out, int32_t *d_status,
+                                    ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (g.raw_bytes > POS_MAX_ROW_BYTES) return IBP_ERR_UNSUPPORTED;
+  if (n_rows < 0 || n_idx < 0 || slot_bytes < slot_bytes_of(g) || slot_bytes % 16 != 0)
+    return IBP_ERR_ARG;
+  if (n_idx == 0) return IBP_OK;
+  if (!pointer_ok(slots, Where::device_or_host, 16) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      !pointer_ok(d_pmask, Where::device_only, 4) || !pointer_ok(d_pbitval, Where::device_only, 4) ||
+      !pointer_ok(d_idx, Where::device_only, 8) || !pointer_ok(out, Where::device_only, 16) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_gather_positions(slots, slot_bytes, n_rows, g, d_row_bitmask, d_pmask, d_pbitval,
+                                 d_idx, n_idx, out, d_status, reinterpret_cast<cudaStream_t>(s));
+}
+
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
               int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s) {
   if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;

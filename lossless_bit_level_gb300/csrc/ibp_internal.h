@@ -58,6 +58,18 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
                   bool slots_in_device_memory, cudaStream_t s);
 size_t pack_scratch_bytes(int64_t n_sel);
+size_t pos_scratch_bytes(const RowGeom &g);
+int launch_build_meta_positions(const void *rows, int64_t n_rows, const RowGeom &g, double T,
+                                uint32_t *d_pmask, uint32_t *d_pbitval, void *d_scratch,
+                                cudaStream_t s);
+int launch_compress_positions(const void *rows, int64_t n_rows, const RowGeom &g,
+                              const uint32_t *d_pmask, const uint32_t *d_pbitval, void *slots,
+                              int64_t slot_bytes, uint32_t *d_bitmask, uint32_t *d_row_bits,
+                              cudaStream_t s);
+int launch_gather_positions(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                            const RowGeom &g, const uint32_t *d_bitmask, const uint32_t *d_pmask,
+                            const uint32_t *d_pbitval, const int64_t *d_idx, int64_t n_idx,
+                            void *out, int32_t *d_status, cudaStream_t s);
 int launch_pack_offsets(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
                         int64_t raw_bytes, const int64_t *d_sel, int64_t n_sel,
                         uint64_t *d_offsets, void *d_scratch, int32_t *d_status,

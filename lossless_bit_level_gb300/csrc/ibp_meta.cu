@@ -18,53 +18,12 @@
 
 #include "ibp_device.cuh"
 #include "ibp_internal.h"
+#include "ibp_popcount.cuh"
 
 namespace ibp {
 namespace {
 
 constexpr int META_THREADS = 256;
-
-__device__ __forceinline__ void csa(uint32_t &h, uint32_t &l, uint32_t a, uint32_t b, uint32_t c) {
-  const uint32_t u = a ^ b;
-  h = (a & b) | (u & c);
-  l = u ^ c;
-}
-
-struct Planes {
-  uint32_t ones = 0, twos = 0, fours = 0;
-  uint32_t eights[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // ripple counter of eights, bit-sliced
-  uint32_t tot[32];
-};
-
-__device__ __forceinline__ void add8(Planes &P, const uint4 &a, const uint4 &b) {
-  uint32_t twosA, twosB, foursA, foursB, eights;
-  csa(twosA, P.ones, P.ones, a.x, a.y);
-  csa(twosB, P.ones, P.ones, a.z, a.w);
-  csa(foursA, P.twos, P.twos, twosA, twosB);
-  csa(twosA, P.ones, P.ones, b.x, b.y);
-  csa(twosB, P.ones, P.ones, b.z, b.w);
-  csa(foursB, P.twos, P.twos, twosA, twosB);
-  csa(eights, P.fours, P.fours, foursA, foursB);
-  uint32_t carry = eights;
-#pragma unroll
-  for (int l = 0; l < 8; ++l) {
-    const uint32_t t = P.eights[l] & carry;
-    P.eights[l] ^= carry;
-    carry = t;
-  }
-}
-
-__device__ __forceinline__ void flush_eights(Planes &P) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int l = 0; l < 8; ++l) c |= ((P.eights[l] >> j) & 1u) << l;
-    P.tot[j] += 8u * c;
-  }
-#pragma unroll
-  for (int l = 0; l < 8; ++l) P.eights[l] = 0;
-}
 
 __global__ void __launch_bounds__(META_THREADS)
     meta_count_kernel(const uint4 *__restrict__ v, int64_t nvec, const uint32_t *tail, int ntail,

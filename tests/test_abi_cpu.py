@@ -43,6 +43,9 @@ def test_size_queries(lib):
     assert ibp.pack_scratch_bytes(0) == 8
     assert ibp.pack_scratch_bytes(4096) == 8
     assert ibp.pack_scratch_bytes(4097) == 16
+    assert ibp.meta_positions_scratch_bytes(128, ibp.FP32) == 128 * 256
+    assert ibp.meta_positions_scratch_bytes(4096, ibp.BF16) == 2048 * 256
+    assert ibp.meta_positions_scratch_bytes(64, ibp.W8) == 16 * 256
     with pytest.raises(ibp.IBPError):
         ibp.slot_bytes(0, ibp.FP32)
     with pytest.raises(ibp.IBPError) as e:
@@ -104,6 +107,17 @@ def test_argument_errors_before_cuda(lib):
                                             None, 3, None, None, None) == ibp.ERR_ARG
     assert lib.ibp_decompress_gather_packed(None, 0, None, 10, 128, ibp.FP32, 48, None, None,
                                             None, 3, None, None, None) == ibp.ERR_UNSUPPORTED
+    # per-position metadata: rows over 16 KiB are not handled; empty calls are no-ops
+    assert lib.ibp_compress_positions(None, 10, 8200, ibp.BF16, 64, None, None, None, 16400, None,
+                                      None, None) == ibp.ERR_UNSUPPORTED
+    assert lib.ibp_compress_positions(None, 0, 128, ibp.FP32, 32, None, None, None, 512, None,
+                                      None, None) == ibp.OK
+    assert lib.ibp_decompress_gather_positions(None, 512, 10, 128, ibp.FP32, 32, None, None, None,
+                                               None, 0, None, None, None) == ibp.OK
+    assert lib.ibp_decompress_gather_positions(None, 512, 10, 128, ibp.FP32, 32, None, None, None,
+                                               None, 2, None, None, None) == ibp.ERR_ARG
+    assert lib.ibp_build_meta_positions(None, 10, 128, ibp.FP32, 0.9, 32, None, None, None,
+                                        None) == ibp.ERR_ARG
     # contiguous ranges: inside the store, empty is a no-op
     assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, 4, 0, None, None,
                                     None) == ibp.OK
