@@ -440,6 +440,60 @@ def packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier, table_ra
     return res
 
 
+def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, table_raw,
+                  out_bytes, link, hbm_peak, dev, thresholds=(None, 0.99)):
+    """Per-position metadata (one mask/bitval per element position of a row): the
+    metadata build, the compression and the same gathers, at the workload's T and at
+    T = 0.99. Compresses into the store's slot buffer (the other legs are done)."""
+    n, L, dt, B = store.n, store.L, store.dtype, store.B
+    pm = torch.zeros(L, dtype=torch.int32, device=dev)
+    pb = torch.zeros(L, dtype=torch.int32, device=dev)
+    scratch = torch.empty(ibp.meta_positions_scratch_bytes(L, dt) // 8, dtype=torch.int64,
+                          device=dev)
+    bitmask = torch.zeros_like(store.bitmask)
+    row_bits = torch.zeros_like(store.row_bits)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {"metadata_bytes": 8 * L}
+    for T in thresholds:
+        T = wl["T"] if T is None else T
+
+        def meta():
+            ibp.build_meta_positions(store.rows, T, B, pm, pb, scratch, dtype=dt)
+
+        def comp():
+            ibp.compress_positions(store.rows, B, pm, pb, store.slots, bitmask, row_bits, dtype=dt)
+
+        mt, _ = time_stage(meta, reps, flush)
+        ct, _ = time_stage(comp, reps, flush)
+        torch.cuda.synchronize()
+        bits = row_bits.cpu().numpy().view(np.uint32).astype(np.int64)
+        bm = bitmask.cpu().numpy().view(np.uint32)
+        r = np.arange(n)
+        comp_flag = (bm[r // 32] >> (r % 32).astype(np.uint32)) & 1
+        stored = np.where(comp_flag == 1, 4 * ((bits + 31) // 32), store.raw_bytes)
+
+        class G:
+            def gather(self, idx, o, st=None):
+                ibp.decompress_gather_positions(store.slots, n, L, dt, B, bitmask, pm, pb, idx, o,
+                                                status)
+
+        per_step, clk = timed_gather(G(), batches, out, max(50, steps // 4), warmup, flush,
+                                     barrier)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ts = float(np.mean(per_step))
+        peak = link["h2d_memcpy_gbs"] if store.residency == "host" else hbm_peak
+        res[f"T={T}"] = {
+            "space_saving_pct": 100.0 * (1.0 - stored.sum() / table_raw),
+            "build_meta_ms": mt * 1e3, "build_meta_frac": table_raw / mt / 1e9 / peak,
+            "compress_ms": ct * 1e3,
+            "gather": {"value": out_bytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3,
+                       "clocks": clk, "frac_of_" + ("link" if store.residency == "host" else "hbm"):
+                       out_bytes / ts / 1e9 / peak if store.residency == "host" else
+                       (wl["batch"] * 8 + out_bytes + out_bytes) / ts / 1e9 / peak}}
+    return res
+
+
 def offload_leg(dev, n_steps=8, token_counts=(256, 4096)):
     """Overlapped offload pipeline on one LLaMA-7B-shaped decoder layer (q, k, v, o
     4096 x 4096; gate, up 11008 x 4096; down 4096 x 11008; BF16 N(0, 0.02)) kept
@@ -898,6 +952,8 @@ def main():
         extra["packed"] = packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier,
                                      table_raw, out_bytes, link, hbm_peak, dev)
         del sstore
+        extra["positions"] = positions_leg(store, wl, batches, out, steps, warmup, flush, barrier,
+                                           reps, table_raw, out_bytes, link, hbm_peak, dev)
         if args.workload == "gnn_dense":
             extra["offload"] = offload_leg(dev)
     line = {
