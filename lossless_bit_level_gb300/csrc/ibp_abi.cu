@@ -3,7 +3,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "ibp_device.cuh"
 #include "ibp_internal.h"
@@ -118,10 +120,10 @@ __global__ void probe_read_kernel(const uint4 *__restrict__ src, int64_t nvec,
 
 int device_info(DeviceInfo *out) {
   static DeviceInfo cache[64];
-  static bool have[64] = {false};
+  static std::atomic<bool> have[64];  // cache[d] is complete once have[d] is set
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return IBP_ERR_CUDA;
-  if (dev >= 0 && dev < 64 && have[dev]) {
+  if (dev >= 0 && dev < 64 && have[dev].load(std::memory_order_acquire)) {
     *out = cache[dev];
     return IBP_OK;
   }
@@ -131,9 +133,13 @@ int device_info(DeviceInfo *out) {
       cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
           cudaSuccess)
     return IBP_ERR_CUDA;
-  if (dev >= 0 && dev < 64) {
-    cache[dev] = d;
-    have[dev] = true;
+  if (dev >= 0 && dev < 64 && !have[dev].load(std::memory_order_acquire)) {
+    static std::mutex fill;
+    std::lock_guard<std::mutex> lock(fill);
+    if (!have[dev].load(std::memory_order_relaxed)) {
+      cache[dev] = d;
+      have[dev].store(true, std::memory_order_release);
+    }
   }
   *out = d;
   return IBP_OK;

@@ -21,6 +21,7 @@
 //   d. the stream (or the raw row) is written to the slot with 128-bit stores, and
 //      the row's bitmask bit is set or cleared with one atomic (one writer per bit).
 #include <algorithm>
+#include <atomic>
 
 #include "ibp_device.cuh"
 #include "ibp_internal.h"
@@ -46,7 +47,6 @@ struct CompressArgs {
   int warps;
   int warp_bytes;  // shared bytes per warp
   int hdr_words;   // header words reserved per warp (multiple of 4)
-  int64_t n_units; // ceil(n_rows / 32)
   int64_t raw_bytes;
 };
 
@@ -484,12 +484,12 @@ int ilog2(int x) {
 template <int LWB>
 int launch_lwb(const CompressArgs &a, const DeviceInfo &dev, int limit, size_t smem,
                cudaStream_t s) {
-  static int configured[64] = {0};
-  if (dev.device < 64 && !configured[dev.device]) {
+  static std::atomic<int> configured[64];  // the attribute is set once per device
+  if (dev.device >= 64 || !configured[dev.device].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(compress_kernel<LWB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              limit) != cudaSuccess)
       return IBP_ERR_CUDA;
-    configured[dev.device] = 1;
+    if (dev.device < 64) configured[dev.device].store(1, std::memory_order_release);
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<LWB>, a.warps * 32,
@@ -533,7 +533,6 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
   const int limit = std::min(COMPRESS_SMEM_BUDGET, dev.max_smem_optin - 2048);
   a.warps = std::min(COMPRESS_MAX_WARPS, limit / a.warp_bytes);
   if (a.warps < 1) return IBP_ERR_UNSUPPORTED;
-  a.n_units = (n_rows + 31) / 32;
   const int nspan = (g.raw_words + 127) / 128;
   if (nspan <= 4) {  // short rows: the register path
     a.warps = COMPRESS_MAX_WARPS;

@@ -30,6 +30,7 @@
 // issued before the current unit is decoded, and the index two units ahead is
 // prefetched, so header and body round trips overlap with decode.
 #include <algorithm>
+#include <atomic>
 
 #include "ibp_device.cuh"
 #include "ibp_internal.h"
@@ -645,12 +646,12 @@ int ilog2(int x) {
 template <int TL, int MINB, bool PACKED>
 int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const size_t smem = (size_t)GATHER_WARPS * team_warp_bytes(TL, a.unit_bytes);
-  static int configured[64] = {0};
-  if (dev.device < 64 && !configured[dev.device]) {
+  static std::atomic<int> configured[64];  // the attribute is set once per device
+  if (dev.device >= 64 || !configured[dev.device].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(gather_kernel<TL, MINB, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dev.max_smem_optin - (int)sizeof(SharedRuns) - 1024) != cudaSuccess)
       return IBP_ERR_CUDA;
-    configured[dev.device] = 1;
+    if (dev.device < 64) configured[dev.device].store(1, std::memory_order_release);
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL, MINB, PACKED>,
@@ -671,12 +672,12 @@ int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
 template <int TL>
 int launch_ws_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const size_t smem = (size_t)WS_DECODERS * 2 * (32 / TL) * a.unit_bytes;
-  static int configured[64] = {0};
-  if (dev.device < 64 && !configured[dev.device]) {
+  static std::atomic<int> configured[64];  // the attribute is set once per device
+  if (dev.device >= 64 || !configured[dev.device].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(gather_ws_kernel<TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dev.max_smem_optin - 16384) != cudaSuccess)
       return IBP_ERR_CUDA;
-    configured[dev.device] = 1;
+    if (dev.device < 64) configured[dev.device].store(1, std::memory_order_release);
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_ws_kernel<TL>, WS_THREADS,

@@ -15,6 +15,7 @@
 // meta_finalize_kernel: one warp applies the threshold in IEEE double and writes
 // the 16-byte ibp_meta.
 #include <algorithm>
+#include <atomic>
 
 #include "ibp_device.cuh"
 #include "ibp_internal.h"
@@ -124,7 +125,8 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
   const int64_t want = std::max<int64_t>(1, (npairs + META_THREADS - 1) / META_THREADS);
   // one wave of resident CTAs (the loop is grid-strided; a partial second wave
   // would run at a fraction of the occupancy)
-  static int per_sm = 0;
+  static std::atomic<int> occupancy{0};  // resident CTAs per SM, looked up once
+  int per_sm = occupancy.load(std::memory_order_relaxed);
   if (per_sm == 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, meta_count_kernel, META_THREADS, 0) !=
@@ -132,6 +134,7 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
         n < 1)
       n = 1;
     per_sm = n;
+    occupancy.store(n, std::memory_order_relaxed);
   }
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
   meta_count_kernel<<<grid, META_THREADS, 0, s>>>(static_cast<const uint4 *>(rows), nvec, tail,

@@ -29,6 +29,7 @@
 // 33rd candidate (all 32 positions in M0 with 32 distinct counts) is scored as
 // n_rows raw rows without a lane of its own.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 
 #include "ibp_device.cuh"
@@ -253,13 +254,15 @@ __global__ void select_finalize_kernel(const SelectScratch *sc, int64_t n_rows, 
 // partial wave would only lengthen the tail.
 template <int LWB>
 int launch_score(const ScoreArgs &a, const DeviceInfo &dev, cudaStream_t s) {
-  static int per_sm = 0;
+  static std::atomic<int> occupancy{0};  // resident CTAs per SM, looked up once
+  int per_sm = occupancy.load(std::memory_order_relaxed);
   if (per_sm == 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, select_score_kernel<LWB>, SEL_THREADS,
                                                       0) != cudaSuccess || n < 1)
       n = 1;
     per_sm = n;
+    occupancy.store(n, std::memory_order_relaxed);
   }
   const int64_t want = std::max<int64_t>(1, (a.n_rows + SEL_WARPS - 1) / SEL_WARPS);
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
