@@ -359,11 +359,23 @@ def mask_select_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps
                                  barrier)
     ts = float(np.mean(per_step))
     gathered = float(np.mean([stored[b.cpu().numpy()].sum() for b in batches]))
+
+    class Sized:  # the same store read through the sized gather (row sizes from row_bits)
+        def gather(self, idx, o, st=None):
+            ibp.decompress_gather_sized(sstore.slots, sstore.n, sstore.L, sstore.dtype, sstore.B,
+                                        sstore.bitmask, sstore.row_bits, sstore.meta, idx, o, st)
+
+    per_sized, clk_sized = timed_gather(Sized(), batches, out, max(50, steps // 4), warmup,
+                                        flush, barrier)
+    t_sized = float(np.mean(per_sized))
     peak = link["h2d_memcpy_gbs"] if residency == "host" else hbm_peak
     sel_frac = 2 * table_raw / sel_t / 1e9 / peak
     mask = int(sel.meta[0].item()) & 0xFFFFFFFF
     g = {"value": out_bytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3,
-         "stored_bytes_per_launch": gathered, "clocks": clk}
+         "stored_bytes_per_launch": gathered, "clocks": clk,
+         "sized": {"value": out_bytes / t_sized / 1e9, "unit": "GB/s",
+                   "ms_per_step": t_sized * 1e3, "clocks": clk_sized,
+                   "note": "ibp_decompress_gather_sized: each row's stored bytes only"}}
     if residency == "host":
         g["link_frac_algorithmic"] = gathered / ts / 1e9 / peak
     else:

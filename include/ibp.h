@@ -247,6 +247,18 @@ int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
                                  const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
                                  void *out, int32_t *d_status, ibp_stream_t s);
 
+/* ibp_decompress_gather given also the per-row bit counts ibp_compress wrote
+ * (d_row_bits, n_rows words, device memory). A row's stored length is then known
+ * from device memory before its slot is read, so exactly its used prefix (rounded
+ * up to 16 bytes) is staged, with no round trip through the slot's header: for
+ * slots in host memory only the stored bytes cross the link. A bit count that
+ * disagrees with the row's header is reported as IBP_ERR_CORRUPT. */
+int ibp_decompress_gather_sized(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                int64_t row_elems, int dtype, uint32_t block_elems,
+                                const uint32_t *d_row_bitmask, const uint32_t *d_row_bits,
+                                const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
+                                void *out, int32_t *d_status, ibp_stream_t s);
+
 /* Decompress a contiguous range of rows in order: out[i] = row row_begin + i for
  * i < n_out (row_begin + n_out <= n_rows). The same as ibp_decompress_gather with
  * d_idx = row_begin, row_begin + 1, ..., without an index array: for streaming

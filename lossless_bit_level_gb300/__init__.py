@@ -51,7 +51,8 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_build_meta_noalloc", "ibp_meta_select_scratch_bytes", "ibp_build_meta_select",
            "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed",
            "ibp_decompress_range", "ibp_meta_positions_scratch_bytes", "ibp_build_meta_positions",
-           "ibp_compress_positions", "ibp_decompress_gather_positions")
+           "ibp_compress_positions", "ibp_decompress_gather_positions",
+           "ibp_decompress_gather_sized")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -90,6 +91,8 @@ def load() -> ctypes.CDLL:
     lib.ibp_compress_positions.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
     lib.ibp_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp,
                                                     i64, vp, vp, vp]
+    lib.ibp_decompress_gather_sized.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, i64,
+                                                vp, vp, vp]
     lib.ibp_decompress_range.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, i64, i64, vp, vp, vp]
     lib.ibp_pack_scratch_bytes.argtypes = [i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.ibp_pack_offsets.argtypes = [vp, vp, i64, i64, i32, vp, i64, vp, vp, vp, vp]
@@ -321,6 +324,22 @@ def decompress_gather_positions(slots: torch.Tensor, n_rows: int, row_elems: int
         _ptr(slots), sb, int(n_rows), int(row_elems), int(dtype), int(block_elems),
         _ptr(bitmask), _ptr(pmask), _ptr(pbitval), _ptr(idx), idx.numel(), _ptr(out),
         _ptr(status), _stream(stream)), "ibp_decompress_gather_positions")
+
+
+def decompress_gather_sized(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
+                            block_elems: int, bitmask: torch.Tensor, row_bits: torch.Tensor,
+                            meta: torch.Tensor, idx: torch.Tensor, out: torch.Tensor,
+                            status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_decompress_gather_sized: as decompress_gather, staging only each row's
+    stored bytes (known from ``row_bits``)."""
+    if idx.dtype != torch.int64:
+        raise ValueError("idx must be int64")
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(int(n_rows), 1)
+    _check(load().ibp_decompress_gather_sized(
+        _ptr(slots), sb, int(n_rows), int(row_elems), int(dtype), int(block_elems),
+        _ptr(bitmask), _ptr(row_bits), _ptr(meta), _ptr(idx), idx.numel(), _ptr(out),
+        _ptr(status), _stream(stream)), "ibp_decompress_gather_sized")
 
 
 def decompress_range(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,

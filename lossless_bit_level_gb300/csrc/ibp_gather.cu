@@ -46,7 +46,8 @@ struct GatherArgs {
   const uint8_t *slots;      // slotted store, or the packed store's bytes
   int64_t slot_bytes;        // slotted store only
   const uint64_t *offsets;   // packed store: entry offsets [n_rows + 1]; null if slotted
-  uint64_t packed_bytes;     // packed store: size of the buffer at slots
+  const uint32_t *row_bits;  // slotted store with known row sizes (sized gather), or null
+  uint64_t packed_bytes;     // packed or sized: bytes of the buffer at slots
   int64_t n_rows;
   const uint32_t *bitmask;
   const ibp_meta *meta;
@@ -96,22 +97,34 @@ __device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u) {
   return a.idx ? __ldg(a.idx + i) : a.row0 + i;
 }
 
-// Offsets of a packed store's entry r (both 0 for a slotted store or a bad index).
+// The bytes of row r to stage, [o0, o1) of the buffer at slots: a packed store's
+// entry, or (sized gather) the used prefix of the row's slot from its bitmask bit
+// and bit count, rounded up to 16 bytes. Both 0 for a bad index.
 struct EntrySpan {
   uint64_t o0, o1;
 };
 
 __device__ __forceinline__ EntrySpan load_span(const GatherArgs &a, int64_t r) {
   EntrySpan e{0, 0};
-  if (a.offsets && r >= 0 && r < a.n_rows) {
+  if (r < 0 || r >= a.n_rows) return e;
+  if (a.offsets) {
     e.o0 = __ldg(a.offsets + r);
     e.o1 = __ldg(a.offsets + r + 1);
+  } else if (a.row_bits) {
+    const uint32_t bits = __ldg(a.row_bits + r);
+    const bool comp = (__ldg(a.bitmask + (r >> 5)) >> (r & 31)) & 1u;
+    const uint64_t used = comp ? 4ull * (((uint64_t)bits + 31) >> 5) : (uint64_t)a.raw_bytes;
+    const uint64_t len = (used + 15) & ~(uint64_t)15;
+    const uint64_t slot = (uint64_t)a.slot_bytes;
+    e.o0 = (uint64_t)r * slot;
+    e.o1 = e.o0 + (len < slot ? len : slot);
   }
   return e;
 }
 
-// PACKED: a packed store (a.offsets set); span: the entry's offsets, loaded ahead
-// by the caller. A slotted store's instantiation carries none of it.
+// PACKED: the bytes to stage come with the row (a packed store's entry, or a sized
+// gather's used slot prefix); span: those bytes, loaded ahead by the caller. The
+// plain slotted instantiation carries none of it.
 template <bool PACKED>
 __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, int64_t u,
                                           int64_t r, bool leader, EntrySpan span) {
@@ -489,8 +502,9 @@ __device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64
     r_next = k + step < count ? load_index(a, u0 + k + step) : -1;  // prefetch
     bool ok = true;
     if (have) {
-      const Unit un = a.offsets ? plan_unit<true>(a, shrink, u0 + k, r, true, load_span(a, r))
-                                : plan_unit<false>(a, shrink, u0 + k, r, true, EntrySpan{0, 0});
+      const Unit un = (a.offsets || a.row_bits)
+                          ? plan_unit<true>(a, shrink, u0 + k, r, true, load_span(a, r))
+                          : plan_unit<false>(a, shrink, u0 + k, r, true, EntrySpan{0, 0});
       const int slot = (int)(k % PLAN_SLOTS);
       ok = mbar_wait(&freed[slot], (uint32_t)((k / PLAN_SLOTS) & 1) ^ 1u, abort);
       if (ok) {
@@ -582,7 +596,8 @@ __device__ void ws_decode(const GatherArgs &a, const Code &code, const SharedRun
     cp_async_commit();
     cp_async_wait<1>();
     __syncwarp();
-    if (a.offsets) decode_unit<NR, TL, true>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
+    if (a.offsets || a.row_bits)
+      decode_unit<NR, TL, true>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
     else decode_unit<NR, TL, false>(a, code, runs, sruns, cur, buf0 + b * buf_step, tl);
     __syncwarp();
     cur = nxt;
@@ -734,7 +749,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
-                  bool slots_in_device_memory, cudaStream_t s) {
+                  bool slots_in_device_memory, cudaStream_t s, const uint32_t *d_row_bits) {
   if (n_idx == 0) return IBP_OK;
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
@@ -742,7 +757,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.slots = static_cast<const uint8_t *>(slots);
   a.slot_bytes = slot_bytes;
   a.offsets = d_offsets;
-  a.packed_bytes = packed_bytes;
+  a.row_bits = d_offsets ? nullptr : d_row_bits;
+  a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
   a.n_rows = n_rows;
   a.bitmask = d_bitmask;
   a.meta = d_meta;
@@ -778,7 +794,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   const int nvec = a.seg_blocks * g.lwb / 4;
   int tl = 4;
   while (tl < 32 && tl * 4 < nvec) tl *= 2;
-  if (d_offsets) return launch_team<true>(a, tl, slots_in_device_memory, dev, s);
+  if (d_offsets || a.row_bits) return launch_team<true>(a, tl, slots_in_device_memory, dev, s);
   return launch_team<false>(a, tl, slots_in_device_memory, dev, s);
 }
 

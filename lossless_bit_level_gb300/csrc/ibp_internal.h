@@ -50,13 +50,16 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
 // slots_in_device_memory selects the warp-specialised bulk-copy kernel (device
 // memory) or the cp.async kernel (page-locked host memory read zero-copy).
 // d_idx null: the rows row0 .. row0 + n_idx - 1 in order.
+// d_row_bits non-null (slotted stores): each row's used slot prefix is known from
+// device memory before the slot is read, and only that prefix is staged.
 // d_offsets non-null: a packed store (entry r at slots + d_offsets[r], packed_bytes
 // long in all); otherwise slot r at slots + r * slot_bytes.
 int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
                   uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
-                  bool slots_in_device_memory, cudaStream_t s);
+                  bool slots_in_device_memory, cudaStream_t s,
+                  const uint32_t *d_row_bits = nullptr);
 size_t pack_scratch_bytes(int64_t n_sel);
 size_t pos_scratch_bytes(const RowGeom &g);
 int launch_build_meta_positions(const void *rows, int64_t n_rows, const RowGeom &g, double T,

@@ -299,3 +299,97 @@ def test_gather_in_cuda_graph(where):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         assert np.array_equal(out.cpu().numpy().view(np.uint32), words[ix])
+
+
+def test_concurrent_host_threads():
+    """Four host threads, each with its own stream, gather from one store at once
+    (the library keeps only per-device lookups that are filled once, under a lock)."""
+    import threading
+    words = words_of(gen.gnn_dense(6000))
+    n, L = words.shape
+    rows_t = to_torch(words, "device")
+    meta = gpu_meta(rows_t, FP32, 0.9, 32)
+    store = GpuStore(n, L, FP32, 32, "host")
+    gpu_compress(rows_t, meta, store)
+    torch.cuda.synchronize()
+    errors = []
+
+    def work(k):
+        try:
+            s = torch.cuda.Stream()
+            g = np.random.default_rng(100 + k)
+            for _ in range(20):
+                ix = g.integers(0, n, size=777)
+                idx = torch.from_numpy(ix).cuda()
+                out = torch.zeros((ix.size, L), dtype=torch.int32, device="cuda")
+                st = torch.zeros(1, dtype=torch.int32, device="cuda")
+                torch.cuda.current_stream().synchronize()
+                ibp.decompress_gather(store.slots, n, L, FP32, 32, store.bitmask, meta, idx, out,
+                                      st, stream=s)
+                s.synchronize()
+                assert int(st.item()) == 0
+                assert np.array_equal(out.cpu().numpy().view(np.uint32), words[ix])
+        except Exception as e:  # collected and re-raised in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[0]
+
+
+@pytest.mark.parametrize("where", ["host", "device"])
+@pytest.mark.parametrize("name", ["dense", "sparse", "kv", "w8_tail"])
+def test_sized_gather(where, name):
+    """The sized gather (row sizes from row_bits, only the used prefix staged)
+    against the oracle and the original rows; a row size that disagrees with the
+    row's header is reported as corrupt and the row left untouched."""
+    if name == "dense":
+        words, code, T, B = words_of(gen.gnn_dense(8000)), FP32, 0.9, 32
+    elif name == "sparse":
+        words, code, T, B = words_of(gen.gnn_sparse(3000)), FP32, 0.9, 32
+    elif name == "kv":
+        words, code, T, B = gen.llm_kv(2, 1, n_rows=600), BF16, 0.9, 64
+    else:
+        g = np.random.default_rng(8)
+        base = g.integers(0, 256, size=(700, 4112), dtype=np.uint64)
+        words = np.where(g.random(size=base.shape) < 0.003, base,
+                         (base & np.uint64(0x1F)) | np.uint64(0x40)).astype(np.uint8)
+        code, T, B = W8, 0.9, 64
+    n, L = words.shape
+    mask, bitval, o_slots, o_bitmask, o_row_bits = oracle_store(words, T, B)
+    rows_t = to_torch(words, where)
+    meta = gpu_meta(rows_t, code, T, B)
+    store = GpuStore(n, L, code, B, where)
+    gpu_compress(rows_t, meta, store)
+    g = np.random.default_rng(n)
+    ix = np.concatenate([g.integers(0, n, size=2000), [0, n - 1]]).astype(np.int64)
+    wdt = {4: torch.int32, 2: torch.int16, 1: torch.uint8}[words.dtype.itemsize]
+    out = torch.zeros((ix.size, L), dtype=wdt, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ibp.decompress_gather_sized(store.slots, n, L, code, B, store.bitmask, store.row_bits, meta,
+                                torch.from_numpy(ix).cuda(), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = from_torch(out, words.dtype)
+    o_out, rc = oracle.decompress_gather(o_slots, n, L, words.dtype, B, o_bitmask, mask, bitval, ix)
+    assert rc == 0 and np.array_equal(got, o_out) and np.array_equal(got, words[ix])
+    # a compressed row whose recorded size is cut below its stream is corrupt
+    comp_rows = [r for r in range(n) if (o_bitmask[r // 32] >> (r % 32)) & 1
+                 and o_row_bits[r] > 160]
+    if comp_rows:
+        r = comp_rows[0]
+        other = (r + 1) % n
+        bad_bits = store.row_bits.clone()
+        bad_bits[r] = 64  # 8 bytes: rounds to one 16-byte piece
+        sentinel = torch.full((2, L), 5, dtype=wdt, device="cuda")
+        st.zero_()
+        ibp.decompress_gather_sized(store.slots, n, L, code, B, store.bitmask, bad_bits, meta,
+                                    torch.tensor([r, other], dtype=torch.int64, device="cuda"),
+                                    sentinel, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == ibp.ERR_CORRUPT
+        res = from_torch(sentinel, words.dtype)
+        assert np.all(res[0] == 5) and np.array_equal(res[1], words[other])
