@@ -18,7 +18,8 @@ import torch
 import ibp_inputs as gen
 import lossless_bit_level_gb300 as ibp
 import oracle
-from codec_harness import GpuStore, gpu_compress, gpu_gather, gpu_meta, meta_values, to_torch
+from codec_harness import GpuStore, gpu_compress, gpu_gather, gpu_meta, meta_tensor, meta_values, \
+    to_torch
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -128,3 +129,107 @@ def test_llm_layer_full(layer):
                     seed=layer + kv)
         del words
         torch.cuda.empty_cache()
+
+
+def test_gnn_dense_variants_full():
+    """The next-step variants on the full 2,000,000 x 128 dense GNN table:
+    * saving-aware metadata: every candidate's score equals the stored bytes the GPU
+      compression reports (ibp_query) for that candidate's mask, and the chosen one is
+      the smallest; the candidate masks are the oracle's on a 200,000-row prefix's
+      threshold family (same counts order) -- checked by recomputing the threshold
+      mask from numpy bit counts of the whole table;
+    * per-position metadata: the GPU arrays equal numpy bit counts column by column;
+      rows compressed with them round-trip, sampled slots equal the oracle's;
+    * sized and packed gathers of full batches equal the original rows."""
+    words = gen.gnn_dense().view(np.uint32)
+    n, L = words.shape
+    T, B = 0.9, 32
+    dev = torch.device("cuda")
+    rows = to_torch(words, "host")
+    # bit counts of the whole table (numpy, 64 positions at a time)
+    ones = np.zeros(32, dtype=np.int64)
+    col_ones = np.zeros((L, 32), dtype=np.int64)
+    for r0 in range(0, n, 250_000):
+        chunk = words[r0:r0 + 250_000]
+        for j in range(32):
+            b = (chunk >> np.uint32(j)) & np.uint32(1)
+            col = b.sum(axis=0, dtype=np.int64)
+            col_ones[:, j] += col
+            ones[j] += col.sum()
+    # saving-aware selection
+    meta = torch.zeros(4, dtype=torch.int32, device=dev)
+    scratch = torch.empty(ibp.meta_select_scratch_bytes() // 4, dtype=torch.int32, device=dev)
+    cand = torch.zeros((ibp.MAX_MASK_CANDIDATES, 4), dtype=torch.int32, device=dev)
+    ibp.build_meta_select(rows, T, B, meta, scratch, cand, dtype=ibp.FP32)
+    torch.cuda.synchronize()
+    cands = ibp.read_candidates(cand)
+    N = n * L
+    held = np.maximum(ones, N - ones)
+    m0 = sum(1 << j for j in range(32) if float(held[j]) >= T * float(N))
+    assert cands[0][0] == m0
+    store = GpuStore(n, L, ibp.FP32, B, "host")
+    stats_t = torch.zeros(10, dtype=torch.int32, device=dev)
+    for mk, bv, score in cands:
+        m = meta_tensor(mk, bv, ibp.FP32, B)
+        gpu_compress(rows, m, store)
+        ibp.query(store.bitmask, store.row_bits, n, L, ibp.FP32, stats_t)
+        assert ibp.read_stats(stats_t).stored_bytes == score, hex(mk)
+    chosen = meta.cpu().numpy().view(np.uint32)
+    assert int(chosen[0]) == min(cands, key=lambda c: (c[2], -bin(c[0]).count("1")))[0]
+    # sized and packed gathers of the chosen store
+    gpu_compress(rows, meta, store)
+    idx = gen.zipf_indices(n, 100_000, 1.0, part=7, workload=gen.GNN_DENSE)
+    it = torch.from_numpy(idx).to(dev)
+    out = torch.zeros((idx.size, L), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ibp.decompress_gather_sized(store.slots, n, L, ibp.FP32, B, store.bitmask, store.row_bits,
+                                meta, it, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and np.array_equal(out.cpu().numpy().view(np.uint32), words[idx])
+    offsets = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+    kscr = torch.empty(ibp.pack_scratch_bytes(n) // 8, dtype=torch.int64, device=dev)
+    ibp.pack_offsets(store.bitmask, store.row_bits, n, L, ibp.FP32, offsets, kscr, status=st)
+    total = int(offsets[-1].item())
+    packed = torch.empty(total, dtype=torch.uint8, device=dev)
+    kbm = torch.zeros_like(store.bitmask)
+    ibp.pack(store.slots, n, L, ibp.FP32, store.bitmask, store.row_bits, offsets, packed, kbm,
+             status=st)
+    out.zero_()
+    ibp.decompress_gather_packed(packed, offsets, n, L, ibp.FP32, B, kbm, meta, it, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and np.array_equal(out.cpu().numpy().view(np.uint32), words[idx])
+    del packed
+    # per-position metadata at T = 0.99
+    Tp = 0.99
+    pm = torch.zeros(L, dtype=torch.int32, device=dev)
+    pb = torch.zeros(L, dtype=torch.int32, device=dev)
+    pscr = torch.empty(ibp.meta_positions_scratch_bytes(L, ibp.FP32) // 8, dtype=torch.int64,
+                       device=dev)
+    ibp.build_meta_positions(rows, Tp, B, pm, pb, pscr, dtype=ibp.FP32)
+    torch.cuda.synchronize()
+    g_pm = pm.cpu().numpy().view(np.uint32)
+    g_pb = pb.cpu().numpy().view(np.uint32)
+    for e in range(L):
+        c1 = col_ones[e]
+        c0 = n - c1
+        v = (c1 > c0).astype(np.int64)
+        hv = np.where(v == 1, c1, c0)
+        inv = hv.astype(np.float64) >= Tp * float(n)
+        assert int(g_pm[e]) == sum(1 << j for j in range(32) if inv[j]), e
+        assert int(g_pb[e]) == sum(1 << j for j in range(32) if inv[j] and v[j]), e
+    ibp.compress_positions(rows, B, pm, pb, store.slots, store.bitmask, store.row_bits,
+                           dtype=ibp.FP32)
+    torch.cuda.synchronize()
+    sample = np.unique(np.random.default_rng(3).integers(0, n, size=3000))
+    o_slots, o_bm, o_rb = oracle.compress_positions(words[sample], B, g_pm, g_pb)
+    rb = store.row_bits.cpu().numpy().view(np.uint32)
+    assert np.array_equal(rb[sample], o_rb)
+    gs = store.slots[torch.from_numpy(sample)].numpy()
+    for k in range(sample.size):
+        used = 4 * ((int(o_rb[k]) + 31) // 32) if (o_bm[k // 32] >> (k % 32)) & 1 else 4 * L
+        assert np.array_equal(gs[k, :used], o_slots[k, :used]), int(sample[k])
+    out.zero_()
+    ibp.decompress_gather_positions(store.slots, n, L, ibp.FP32, B, store.bitmask, pm, pb, it, out,
+                                    st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and np.array_equal(out.cpu().numpy().view(np.uint32), words[idx])
