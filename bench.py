@@ -506,6 +506,70 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
     return res
 
 
+def dlrm_batched_leg(dev, flush, barrier, steps, warmup, hbm_peak, n_tables=26,
+                     lookups=65_536):
+    """All 26 DLRM tables (1,000,000 x 128 FP32 each, per-table metadata T = 0.95,
+    B = 32, slots in HBM) and one Zipf(1.05) lookup batch of 65,536 rows per table:
+    26 separate gathers per step against one batched gather of all 26 jobs."""
+    L, T, B = 128, 0.95, 32
+    stores, jobs, outs = [], [], []
+    stored_total = 0
+    for t in range(n_tables):
+        words = gen.dlrm_table(t).view(np.uint32)
+        n = words.shape[0]
+        rows = torch.from_numpy(words.view(np.int32)).to(dev)
+        meta = torch.zeros(4, dtype=torch.int32, device=dev)
+        scr = torch.empty(ibp.meta_scratch_bytes() // 4, dtype=torch.int32, device=dev)
+        ibp.build_meta(rows, T, B, meta, scr, dtype=ibp.FP32)
+        slots = torch.empty((n, ibp.slot_bytes(L, ibp.FP32)), dtype=torch.uint8, device=dev)
+        bm = torch.zeros(((n + 31) // 32,), dtype=torch.int32, device=dev)
+        rb = torch.zeros((n,), dtype=torch.int32, device=dev)
+        ibp.compress(rows, B, meta, slots, bm, rb, None, dtype=ibp.FP32)
+        ix = gen.zipf_indices(n, lookups, 1.05, part=t, workload=gen.DLRM)
+        bits = rb.cpu().numpy().view(np.uint32).astype(np.int64)
+        comp = (bm.cpu().numpy().view(np.uint32)[np.arange(n) // 32] >>
+                (np.arange(n) % 32).astype(np.uint32)) & 1
+        stored = np.where(comp == 1, 4 * ((bits + 31) // 32), 4 * L)
+        stored_total += int(stored[ix].sum())
+        out = torch.empty((lookups, L), dtype=torch.int32, device=dev)
+        stores.append((slots, n, bm, meta))
+        jobs.append((slots, n, bm, meta, torch.from_numpy(ix).to(dev), out))
+        outs.append(out)
+        del rows, words
+    torch.cuda.synchronize()
+    out_bytes = n_tables * lookups * 4 * L
+    alg = n_tables * lookups * 8 + stored_total + out_bytes
+    s = torch.cuda.current_stream()
+
+    def separate():
+        for slots, n, bm, meta, ix, out in jobs:
+            ibp.decompress_gather(slots, n, L, ibp.FP32, B, bm, meta, ix, out)
+
+    def batched():
+        ibp.decompress_gather_batched(jobs, L, ibp.FP32, B)
+
+    res = {"workload": f"{n_tables} DLRM tables 1,000,000 x 128 FP32 in HBM, {lookups} "
+                       "Zipf(1.05) lookups per table per step", "output_bytes_per_step": out_bytes,
+           "algorithmic_bytes_per_step": alg}
+    for name, fn in (("separate_calls", separate), ("batched_call", batched)):
+        class G:
+            def gather(self, idx, o, st=None):
+                fn()
+        per_step, clk = timed_gather(G(), [None], None, max(20, steps // 10), warmup, flush,
+                                     barrier)
+        t = float(np.mean(per_step))
+        res[name] = {"value": out_bytes / t / 1e9, "unit": "GB/s", "ms_per_step": t * 1e3,
+                     "hbm_frac": alg / t / 1e9 / hbm_peak, "clocks": clk}
+    # every table's rows come back exactly
+    for (slots, n, bm, meta, ix, out), t in zip(jobs, range(n_tables)):
+        if t % 9 == 0:
+            words = gen.dlrm_table(t).view(np.uint32)
+            assert np.array_equal(out.cpu().numpy().view(np.uint32), words[ix.cpu().numpy()])
+    del stores, jobs, outs
+    torch.cuda.empty_cache()
+    return res
+
+
 def offload_leg(dev, n_steps=8, token_counts=(256, 4096)):
     """Overlapped offload pipeline on one LLaMA-7B-shaped decoder layer (q, k, v, o
     4096 x 4096; gate, up 11008 x 4096; down 4096 x 11008; BF16 N(0, 0.02)) kept
@@ -968,6 +1032,9 @@ def main():
                                            reps, table_raw, out_bytes, link, hbm_peak, dev)
         if args.workload == "gnn_dense":
             extra["offload"] = offload_leg(dev)
+        if args.workload == "dlrm_table":
+            extra["dlrm_26_tables"] = dlrm_batched_leg(dev, flush, barrier, steps, warmup,
+                                                       hbm_peak)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,

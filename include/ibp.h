@@ -259,6 +259,29 @@ int ibp_decompress_gather_sized(const void *slots, int64_t slot_bytes, int64_t n
                                 const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
                                 void *out, int32_t *d_status, ibp_stream_t s);
 
+/* One gather of a batch: a store (slots, slot_bytes, n_rows, its bitmask and
+ * metadata) and the indices to read from it into out, as in ibp_decompress_gather. */
+typedef struct {
+  const void *slots;              /* device or registered host memory, 16-byte aligned */
+  int64_t slot_bytes;
+  int64_t n_rows;
+  const uint32_t *d_row_bitmask;  /* device */
+  const ibp_meta *d_meta;         /* device */
+  const int64_t *d_idx;           /* device */
+  int64_t n_idx;
+  void *out;                      /* device, n_idx x row_elems words, 16-byte aligned */
+} ibp_gather_job;
+
+/* Several decompress-gathers with one row geometry (row_elems, dtype, block_elems)
+ * in one launch per 64 jobs: e.g. one lookup batch per embedding table of a model.
+ * jobs: host array of n_jobs descriptions (read during the call; the structs need
+ * not outlive it). Each job gets CTAs in proportion to its indices, so the fixed
+ * cost of a launch is paid once for the batch. Per-job checks, results and device
+ * errors are those of ibp_decompress_gather (*d_status is shared by all jobs). */
+int ibp_decompress_gather_batched(const ibp_gather_job *jobs, int n_jobs, int64_t row_elems,
+                                  int dtype, uint32_t block_elems, int32_t *d_status,
+                                  ibp_stream_t s);
+
 /* Decompress a contiguous range of rows in order: out[i] = row row_begin + i for
  * i < n_out (row_begin + n_out <= n_rows). The same as ibp_decompress_gather with
  * d_idx = row_begin, row_begin + 1, ..., without an index array: for streaming

@@ -40,6 +40,14 @@ class IBPError(RuntimeError):
         super().__init__(f"{call}: {status_string(code)} ({code})")
 
 
+class GatherJob(ctypes.Structure):
+    """ibp_gather_job: one gather of a batch."""
+    _fields_ = [("slots", ctypes.c_void_p), ("slot_bytes", ctypes.c_int64),
+                ("n_rows", ctypes.c_int64), ("d_row_bitmask", ctypes.c_void_p),
+                ("d_meta", ctypes.c_void_p), ("d_idx", ctypes.c_void_p),
+                ("n_idx", ctypes.c_int64), ("out", ctypes.c_void_p)]
+
+
 class Stats(ctypes.Structure):
     _fields_ = [("n_rows", ctypes.c_int64), ("n_compressed", ctypes.c_int64),
                 ("raw_bytes", ctypes.c_int64), ("stored_bytes", ctypes.c_int64),
@@ -52,7 +60,7 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed",
            "ibp_decompress_range", "ibp_meta_positions_scratch_bytes", "ibp_build_meta_positions",
            "ibp_compress_positions", "ibp_decompress_gather_positions",
-           "ibp_decompress_gather_sized")
+           "ibp_decompress_gather_sized", "ibp_decompress_gather_batched")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -91,6 +99,7 @@ def load() -> ctypes.CDLL:
     lib.ibp_compress_positions.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
     lib.ibp_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp,
                                                     i64, vp, vp, vp]
+    lib.ibp_decompress_gather_batched.argtypes = [vp, i32, i64, i32, u32, vp, vp]
     lib.ibp_decompress_gather_sized.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, i64,
                                                 vp, vp, vp]
     lib.ibp_decompress_range.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, i64, i64, vp, vp, vp]
@@ -340,6 +349,24 @@ def decompress_gather_sized(slots: torch.Tensor, n_rows: int, row_elems: int, dt
         _ptr(slots), sb, int(n_rows), int(row_elems), int(dtype), int(block_elems),
         _ptr(bitmask), _ptr(row_bits), _ptr(meta), _ptr(idx), idx.numel(), _ptr(out),
         _ptr(status), _stream(stream)), "ibp_decompress_gather_sized")
+
+
+def decompress_gather_batched(jobs, row_elems: int, dtype: int, block_elems: int,
+                              status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_decompress_gather_batched: ``jobs`` is a list of (slots, n_rows, bitmask, meta,
+    idx, out) tuples sharing one row geometry; one launch per 64 jobs."""
+    arr = (GatherJob * max(len(jobs), 1))()
+    for k, (slots, n_rows, bitmask, meta, idx, out) in enumerate(jobs):
+        if idx.dtype != torch.int64:
+            raise ValueError("idx must be int64")
+        sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+            slots.element_size() // max(int(n_rows), 1)
+        arr[k] = GatherJob(slots.data_ptr(), sb, int(n_rows), bitmask.data_ptr(), meta.data_ptr(),
+                           idx.data_ptr(), idx.numel(), out.data_ptr())
+    _check(load().ibp_decompress_gather_batched(ctypes.cast(arr, ctypes.c_void_p), len(jobs),
+                                                int(row_elems), int(dtype), int(block_elems),
+                                                _ptr(status), _stream(stream)),
+           "ibp_decompress_gather_batched")
 
 
 def decompress_range(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,

@@ -5,7 +5,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <memory>
 #include <mutex>
+#include <vector>
 
 #include "ibp_device.cuh"
 #include "ibp_internal.h"
@@ -15,6 +17,7 @@ namespace ibp {
 namespace {
 
 constexpr int64_t MAX_ROW_ELEMS = int64_t(1) << 20;
+constexpr int BATCH_JOBS_MAX_CHECK = 256;  // job flags kept on the stack up to this many
 
 enum class Where { device_only, device_or_host };
 
@@ -296,6 +299,45 @@ int ibp_decompress_gather_sized(const void *slots, int64_t slot_bytes, int64_t n
   return launch_gather(slots, slot_bytes, nullptr, 0, n_rows, g, (uint32_t)dtype, d_row_bitmask,
                        d_meta, d_idx, 0, n_idx, out, d_status, in_device_memory(slots),
                        reinterpret_cast<cudaStream_t>(s), d_row_bits);
+}
+
+int ibp_decompress_gather_batched(const ibp_gather_job *jobs, int n_jobs, int64_t row_elems,
+                                  int dtype, uint32_t block_elems, int32_t *d_status,
+                                  ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_jobs < 0 || (n_jobs > 0 && !jobs)) return IBP_ERR_ARG;
+  int64_t total_idx = 0;
+  for (int j = 0; j < n_jobs; ++j) total_idx += jobs[j].n_idx > 0 ? jobs[j].n_idx : 0;
+  if (total_idx == 0) {  // nothing to gather (negative counts are still refused)
+    for (int j = 0; j < n_jobs; ++j)
+      if (jobs[j].n_idx < 0) return IBP_ERR_ARG;
+    return IBP_OK;
+  }
+  if (d_status && !pointer_ok(d_status, Where::device_only, 4)) return IBP_ERR_ARG;
+  bool in_dev[BATCH_JOBS_MAX_CHECK];
+  bool *in_device = in_dev;
+  std::unique_ptr<bool[]> heap;
+  if (n_jobs > BATCH_JOBS_MAX_CHECK) {
+    heap.reset(new bool[(size_t)n_jobs]);
+    in_device = heap.get();
+  }
+  for (int j = 0; j < n_jobs; ++j) {
+    const ibp_gather_job &jb = jobs[j];
+    if (jb.n_rows < 0 || jb.n_idx < 0 || jb.slot_bytes < slot_bytes_of(g) ||
+        jb.slot_bytes % 16 != 0)
+      return IBP_ERR_ARG;
+    in_device[j] = false;
+    if (jb.n_idx == 0) continue;
+    if (!pointer_ok(jb.slots, Where::device_or_host, 16) ||
+        !pointer_ok(jb.d_row_bitmask, Where::device_only, 4) ||
+        !pointer_ok(jb.d_meta, Where::device_only, 16) ||
+        !pointer_ok(jb.d_idx, Where::device_only, 8) || !pointer_ok(jb.out, Where::device_only, 16))
+      return IBP_ERR_ARG;
+    in_device[j] = in_device_memory(jb.slots);
+  }
+  return launch_gather_batched(jobs, n_jobs, g, (uint32_t)dtype, d_status, in_device,
+                               reinterpret_cast<cudaStream_t>(s));
 }
 
 int ibp_decompress_range(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems,

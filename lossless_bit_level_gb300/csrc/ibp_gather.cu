@@ -63,6 +63,7 @@ struct GatherArgs {
   int unit_bytes;  // shared staging bytes per unit (one buffer)
   int64_t n_units;
   int64_t raw_bytes;
+  int cta0, ncta;  // the CTAs [cta0, cta0 + ncta) of the grid work on this gather
 };
 
 // The plan of one unit (identical in every lane of its team).
@@ -330,8 +331,8 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
   const int tl = lane % TL;
   const bool leader = tl == 0;
   const uint32_t shrink = 32u - (uint32_t)code.fc;
-  const int64_t warp_gid = (int64_t)blockIdx.x * GATHER_WARPS + (threadIdx.x >> 5);
-  const int64_t stride = (int64_t)gridDim.x * GATHER_WARPS * TPW;  // between a team's units
+  const int64_t warp_gid = (int64_t)(blockIdx.x - a.cta0) * GATHER_WARPS + (threadIdx.x >> 5);
+  const int64_t stride = (int64_t)a.ncta * GATHER_WARPS * TPW;  // between a team's units
   uint8_t *const bufs = warp_smem + team * a.unit_bytes;  // buffer k at bufs + k * buf_step
   const int buf_step = TPW * a.unit_bytes;
   StagedMeta *const metas = warp_meta + team;  // meta k at metas[k * TPW]
@@ -430,13 +431,12 @@ __host__ __device__ inline size_t team_warp_bytes(int tl, int unit_bytes) {
 
 // MINB: resident CTAs per SM the register budget is sized for (4 for slots in
 // device memory, 3 for host memory; measured best for each).
-template <int TL, int MINB, bool PACKED>
-__global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ SharedRuns sruns;
+template <int TL, bool PACKED>
+__device__ __forceinline__ void team_gather(const GatherArgs &a, uint8_t *smem,
+                                            SharedRuns &sruns) {
   const ibp_meta m = load_meta(a.meta);
   if (m.dtype != a.dtype || m.block_elems != a.block_elems) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, IBP_ERR_META);
+    if ((int)blockIdx.x == a.cta0 && threadIdx.x == 0) report(a.status, IBP_ERR_META);
     return;
   }
   const Code code = make_code(m);
@@ -446,6 +446,62 @@ __global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherA
   StagedMeta *warp_meta = reinterpret_cast<StagedMeta *>(
       warp_smem + (size_t)GATHER_NBUF * (32 / TL) * a.unit_bytes);
   dispatch_runs<TL, PACKED>(a, code, sruns, warp_smem, warp_meta);
+}
+
+template <int TL, int MINB, bool PACKED>
+__global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ SharedRuns sruns;
+  team_gather<TL, PACKED>(a, smem, sruns);
+}
+
+// Several gathers with one row geometry in one launch (e.g. one lookup batch per
+// embedding table): each job has its own store, metadata, indices and output, and
+// owns a contiguous range of the grid's CTAs, which run the team loop above on it.
+// One launch instead of one per job removes the per-launch fixed cost (the first
+// round trips of every CTA and the drain) from all jobs but one.
+constexpr int BATCH_MAX_JOBS = 64;
+
+struct BatchJob {
+  const uint8_t *slots;
+  int64_t slot_bytes;
+  int64_t n_rows;
+  const uint32_t *bitmask;
+  const ibp_meta *meta;
+  const int64_t *idx;
+  int64_t n_idx;
+  uint32_t *out;
+  int cta0, ncta;
+};
+
+struct BatchArgs {
+  GatherArgs common;  // geometry, status; the per-job fields are filled per CTA
+  int n_jobs;
+  BatchJob jobs[BATCH_MAX_JOBS];
+};
+
+template <int TL, int MINB>
+__global__ void __launch_bounds__(GATHER_WARPS * 32, MINB)
+    gather_batched_kernel(const __grid_constant__ BatchArgs b) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ SharedRuns sruns;
+  int j = 0;
+  while (j + 1 < b.n_jobs && (int)blockIdx.x >= b.jobs[j + 1].cta0) ++j;
+  const BatchJob &job = b.jobs[j];
+  GatherArgs a = b.common;
+  a.slots = job.slots;
+  a.slot_bytes = job.slot_bytes;
+  a.n_rows = job.n_rows;
+  a.bitmask = job.bitmask;
+  a.meta = job.meta;
+  a.idx = job.idx;
+  a.n_idx = job.n_idx;
+  a.out = job.out;
+  a.n_units = job.n_idx * a.nseg;
+  a.cta0 = job.cta0;
+  a.ncta = job.ncta;
+  if (a.n_units == 0) return;
+  team_gather<TL, false>(a, smem, sruns);
 }
 
 // ---------------------------------------------------------------------------
@@ -680,7 +736,10 @@ int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   // left over lets a consumer's kernels run beside a streaming decode.
   const int ctas_per_sm = MINB == 3 ? std::min(per_sm, 2) : per_sm;
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * ctas_per_sm);
-  gather_kernel<TL, MINB, PACKED><<<grid, GATHER_WARPS * 32, smem, s>>>(a);
+  GatherArgs g = a;
+  g.cta0 = 0;
+  g.ncta = grid;
+  gather_kernel<TL, MINB, PACKED><<<grid, GATHER_WARPS * 32, smem, s>>>(g);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
@@ -756,6 +815,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   GatherArgs a;
   a.slots = static_cast<const uint8_t *>(slots);
   a.slot_bytes = slot_bytes;
+  a.cta0 = 0;
+  a.ncta = 0;
   a.offsets = d_offsets;
   a.row_bits = d_offsets ? nullptr : d_row_bits;
   a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
@@ -796,6 +857,112 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   while (tl < 32 && tl * 4 < nvec) tl *= 2;
   if (d_offsets || a.row_bits) return launch_team<true>(a, tl, slots_in_device_memory, dev, s);
   return launch_team<false>(a, tl, slots_in_device_memory, dev, s);
+}
+
+int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom &g,
+                          uint32_t dtype, int32_t *d_status, const bool *in_device,
+                          cudaStream_t s) {
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  BatchArgs b;
+  GatherArgs &a = b.common;
+  a = GatherArgs{};
+  a.status = d_status;
+  a.dtype = dtype;
+  a.block_elems = (uint32_t)g.B;
+  a.lwb = g.lwb;
+  a.lwb_shift = ilog2(g.lwb);
+  a.nb = g.nb;
+  a.raw_words = g.raw_words;
+  a.lwt = g.lwt;
+  a.raw_bytes = g.raw_bytes;
+  const int block_bytes = g.lwb * 4;
+  a.seg_blocks = std::max(1, std::min({g.nb, 32, SEG_TARGET_BYTES / block_bytes}));
+  a.nseg = (g.nb + a.seg_blocks - 1) / a.seg_blocks;
+  a.unit_bytes = ((a.seg_blocks * block_bytes + 64 + 127) / 128) * 128 + 32;
+  const int nvec = a.seg_blocks * g.lwb / 4;
+  int tl = 4;
+  while (tl < 32 && tl * 4 < nvec) tl *= 2;
+  for (int j0 = 0; j0 < n_jobs; j0 += BATCH_MAX_JOBS) {
+    const int nj = std::min(BATCH_MAX_JOBS, n_jobs - j0);
+    bool all_device = true;
+    int64_t total_units = 0;
+    for (int j = 0; j < nj; ++j) {
+      all_device = all_device && in_device[j0 + j];
+      total_units += jobs[j0 + j].n_idx * a.nseg;
+    }
+    if (total_units == 0) continue;
+    const int minb = all_device ? 4 : 3;
+    // CTAs in proportion to each job's units, at least one per job with work
+    int per_sm = 0;
+    const size_t smem = (size_t)GATHER_WARPS * team_warp_bytes(tl, a.unit_bytes);
+    const void *kern = nullptr;
+#define IBP_BATCH_KERNEL(T, M) reinterpret_cast<const void *>(gather_batched_kernel<T, M>)
+    switch (tl) {
+      case 4: kern = minb == 4 ? IBP_BATCH_KERNEL(4, 4) : IBP_BATCH_KERNEL(4, 3); break;
+      case 8: kern = minb == 4 ? IBP_BATCH_KERNEL(8, 4) : IBP_BATCH_KERNEL(8, 3); break;
+      case 16: kern = minb == 4 ? IBP_BATCH_KERNEL(16, 4) : IBP_BATCH_KERNEL(16, 3); break;
+      default: kern = minb == 4 ? IBP_BATCH_KERNEL(32, 4) : IBP_BATCH_KERNEL(32, 3); break;
+    }
+#undef IBP_BATCH_KERNEL
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.max_smem_optin - (int)sizeof(SharedRuns) - 1024) != cudaSuccess)
+      return IBP_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, GATHER_WARPS * 32, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      return IBP_ERR_CUDA;
+    const int ctas_per_sm = minb == 3 ? std::min(per_sm, 2) : per_sm;
+    const int64_t budget = (int64_t)dev.sm_count * ctas_per_sm;
+    const int64_t units_per_cta = (int64_t)GATHER_WARPS * (32 / tl);
+    int cta = 0;
+    int used = 0;
+    for (int j = 0; j < nj; ++j) {
+      const ibp_gather_job &src = jobs[j0 + j];
+      const int64_t units = src.n_idx * a.nseg;
+      int64_t n = 0;
+      if (units > 0) {
+        const int64_t want = (units + units_per_cta - 1) / units_per_cta;
+        const int64_t share = std::max<int64_t>(1, budget * units / total_units);
+        n = std::min(want, share);
+      }
+      BatchJob &d = b.jobs[used];
+      if (units == 0) continue;
+      d.slots = static_cast<const uint8_t *>(src.slots);
+      d.slot_bytes = src.slot_bytes;
+      d.n_rows = src.n_rows;
+      d.bitmask = src.d_row_bitmask;
+      d.meta = src.d_meta;
+      d.idx = src.d_idx;
+      d.n_idx = src.n_idx;
+      d.out = static_cast<uint32_t *>(src.out);
+      d.cta0 = cta;
+      d.ncta = (int)n;
+      cta += (int)n;
+      ++used;
+    }
+    b.n_jobs = used;
+    switch (tl) {
+      case 4:
+        if (minb == 4) gather_batched_kernel<4, 4><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        else gather_batched_kernel<4, 3><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        break;
+      case 8:
+        if (minb == 4) gather_batched_kernel<8, 4><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        else gather_batched_kernel<8, 3><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        break;
+      case 16:
+        if (minb == 4) gather_batched_kernel<16, 4><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        else gather_batched_kernel<16, 3><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        break;
+      default:
+        if (minb == 4) gather_batched_kernel<32, 4><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        else gather_batched_kernel<32, 3><<<cta, GATHER_WARPS * 32, smem, s>>>(b);
+        break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return IBP_ERR_CUDA;
+  }
+  return IBP_OK;
 }
 
 }  // namespace ibp

@@ -60,6 +60,11 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
                   bool slots_in_device_memory, cudaStream_t s,
                   const uint32_t *d_row_bits = nullptr);
+// Several slotted gathers with one row geometry in one launch per 64 jobs; in_device[j]:
+// job j's slots are in device memory.
+int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom &g,
+                          uint32_t dtype, int32_t *d_status, const bool *in_device,
+                          cudaStream_t s);
 size_t pack_scratch_bytes(int64_t n_sel);
 size_t pos_scratch_bytes(const RowGeom &g);
 int launch_build_meta_positions(const void *rows, int64_t n_rows, const RowGeom &g, double T,

@@ -118,6 +118,10 @@ def test_argument_errors_before_cuda(lib):
                                                None, 2, None, None, None) == ibp.ERR_ARG
     assert lib.ibp_build_meta_positions(None, 10, 128, ibp.FP32, 0.9, 32, None, None, None,
                                         None) == ibp.ERR_ARG
+    # batched gathers: empty batch is a no-op; a null job array with jobs is refused
+    assert lib.ibp_decompress_gather_batched(None, 0, 128, ibp.FP32, 32, None, None) == ibp.OK
+    assert lib.ibp_decompress_gather_batched(None, 3, 128, ibp.FP32, 32, None, None) == ibp.ERR_ARG
+    assert ctypes.sizeof(ibp.GatherJob) == 64
     # contiguous ranges: inside the store, empty is a no-op
     assert lib.ibp_decompress_range(None, 512, 10, 128, ibp.FP32, 32, None, None, 4, 0, None, None,
                                     None) == ibp.OK

@@ -393,3 +393,40 @@ def test_sized_gather(where, name):
         assert int(st.item()) == ibp.ERR_CORRUPT
         res = from_torch(sentinel, words.dtype)
         assert np.all(res[0] == 5) and np.array_equal(res[1], words[other])
+
+
+@pytest.mark.parametrize("n_tables", [5, 70])
+def test_batched_gather_tables(n_tables):
+    """One call gathering from many tables (each its own store, metadata, indices and
+    output; some host-resident, one job with no indices, one with a bad index), more
+    than 64 jobs split into launches; every job against the oracle."""
+    g = np.random.default_rng(n_tables)
+    L, B, T = 128, 32, 0.95
+    jobs, expect, bad_job = [], [], None
+    for t in range(n_tables):
+        words = words_of(gen.dlrm_table(t % 26, 2000 + 37 * t))
+        n = words.shape[0]
+        where = "host" if t % 3 == 0 else "device"
+        rows_t = to_torch(words, where)
+        meta = gpu_meta(rows_t, FP32, T, B)
+        store = GpuStore(n, L, FP32, B, where)
+        gpu_compress(rows_t, meta, store)
+        k = 0 if t == 1 else int(g.integers(1, 900))
+        ix = g.integers(0, n, size=k).astype(np.int64)
+        if t == 2:
+            ix[0] = n + 5  # out of range: skipped, reported
+            bad_job = t
+        out = torch.full((max(k, 1), L), 9, dtype=torch.int32, device="cuda")
+        jobs.append((store.slots, n, store.bitmask, meta, torch.from_numpy(ix).cuda(), out, store))
+        expect.append((words, ix))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ibp.decompress_gather_batched([j[:6] for j in jobs], L, FP32, B, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == ibp.ERR_INDEX
+    for t, ((words, ix), job) in enumerate(zip(expect, jobs)):
+        got = job[5].cpu().numpy().view(np.uint32)[: ix.size]
+        if t == bad_job:
+            assert np.all(got[0] == 9)
+            assert np.array_equal(got[1:], words[ix[1:]])
+        else:
+            assert np.array_equal(got, words[ix]), t
