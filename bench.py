@@ -507,7 +507,7 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
 
 
 def dlrm_batched_leg(dev, flush, barrier, steps, warmup, hbm_peak, n_tables=26,
-                     lookups=65_536):
+                     lookups=65_536, n_rows=1_000_000):
     """All 26 DLRM tables (1,000,000 x 128 FP32 each, per-table metadata T = 0.95,
     B = 32, slots in HBM) and one Zipf(1.05) lookup batch of 65,536 rows per table:
     26 separate gathers per step against one batched gather of all 26 jobs."""
@@ -515,7 +515,7 @@ def dlrm_batched_leg(dev, flush, barrier, steps, warmup, hbm_peak, n_tables=26,
     stores, jobs, outs = [], [], []
     stored_total = 0
     for t in range(n_tables):
-        words = gen.dlrm_table(t).view(np.uint32)
+        words = gen.dlrm_table(t, n_rows).view(np.uint32)
         n = words.shape[0]
         rows = torch.from_numpy(words.view(np.int32)).to(dev)
         meta = torch.zeros(4, dtype=torch.int32, device=dev)
@@ -548,7 +548,7 @@ def dlrm_batched_leg(dev, flush, barrier, steps, warmup, hbm_peak, n_tables=26,
     def batched():
         ibp.decompress_gather_batched(jobs, L, ibp.FP32, B)
 
-    res = {"workload": f"{n_tables} DLRM tables 1,000,000 x 128 FP32 in HBM, {lookups} "
+    res = {"workload": f"{n_tables} DLRM tables {n_rows:,} x 128 FP32 in HBM, {lookups} "
                        "Zipf(1.05) lookups per table per step", "output_bytes_per_step": out_bytes,
            "algorithmic_bytes_per_step": alg}
     for name, fn in (("separate_calls", separate), ("batched_call", batched)):
@@ -563,7 +563,7 @@ def dlrm_batched_leg(dev, flush, barrier, steps, warmup, hbm_peak, n_tables=26,
     # every table's rows come back exactly
     for (slots, n, bm, meta, ix, out), t in zip(jobs, range(n_tables)):
         if t % 9 == 0:
-            words = gen.dlrm_table(t).view(np.uint32)
+            words = gen.dlrm_table(t, n_rows).view(np.uint32)
             assert np.array_equal(out.cpu().numpy().view(np.uint32), words[ix.cpu().numpy()])
     del stores, jobs, outs
     torch.cuda.empty_cache()
@@ -848,6 +848,8 @@ def main():
                     help="override where slots and rows live (default: the workload's)")
     ap.add_argument("--indices", choices=["zipf", "uniform"], default=None,
                     help="override the workload's index distribution")
+    ap.add_argument("--tables", type=int, default=26,
+                    help="DLRM workload: tables in the batched-gather leg")
     ap.add_argument("--rows", type=int, default=None,
                     help="use only the first ROWS rows of the table (smaller profiling cases)")
     args = ap.parse_args()
@@ -1034,7 +1036,8 @@ def main():
             extra["offload"] = offload_leg(dev)
         if args.workload == "dlrm_table":
             extra["dlrm_26_tables"] = dlrm_batched_leg(dev, flush, barrier, steps, warmup,
-                                                       hbm_peak)
+                                                       hbm_peak, n_tables=args.tables,
+                                                       n_rows=args.rows or 1_000_000)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
