@@ -294,9 +294,17 @@ class Store:
         self.row_bits = torch.zeros((self.n,), dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stats_t = torch.zeros(10, dtype=torch.int32, device=dev)
+        # under several ranks the metadata is that of every rank's rows together:
+        # local bit counts, one all-reduce of 33 int64 values, then the threshold
+        self.sharded = False
+        self.counters = torch.zeros(32, dtype=torch.int64, device=dev)
 
     def build_meta(self):
-        ibp.build_meta(self.rows, self.T, self.B, self.meta, self.scratch, dtype=self.dtype)
+        if self.sharded:
+            from lossless_bit_level_gb300.sharded import sharded_meta
+            sharded_meta(self.rows, self.T, self.B, self.meta, self.counters, dtype=self.dtype)
+        else:
+            ibp.build_meta(self.rows, self.T, self.B, self.meta, self.scratch, dtype=self.dtype)
 
     def compress(self):
         ibp.compress(self.rows, self.B, self.meta, self.slots, self.bitmask, self.row_bits,
@@ -896,6 +904,7 @@ def main():
     words = rows_np.view(np.uint32) if rows_np.dtype == np.float32 else rows_np
     del rows_np
     store = Store(words, wl["dtype"], wl["T"], wl["B"], wl["residency"], dev)
+    store.sharded = world > 1
     n, L = store.n, store.L
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
@@ -1045,7 +1054,9 @@ def main():
         "config": {"workload": wl["desc"], "rows": n, "row_elems": L, "T": wl["T"],
                    "block_elems": wl["B"], "batch": wl["batch"], "residency": residency,
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then read)",
-                   "parallelism": f"{world} independent replica(s)"},
+                   "parallelism": f"{world} independent replica(s)",
+                   "meta_exchange": ("all-reduce of 32 bit counters + element count"
+                                     if world > 1 else None)},
         "space_saving_pct": 100.0 * (1.0 - st.stored_bytes / st.raw_bytes),
         "space_saving_gathered_pct": 100.0 * (1.0 - stored_per_step / out_bytes),
         "bit_saving_pct": 100.0 * (1.0 - st.total_bits / (8.0 * st.raw_bytes)),

@@ -117,6 +117,20 @@ int ibp_meta_scratch_bytes(size_t *bytes);
 int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtype, double T,
                    uint32_t block_elems, ibp_meta *d_meta, void *d_scratch, ibp_stream_t s);
 
+/* Preprocessing in two steps, for rows held in several places (shards of a table on
+ * several GPUs, or batches streamed one after another): bit counts are additive.
+ * ibp_meta_count overwrites d_counters (32 uint64 words, device memory, 256 bytes)
+ * with the number of 1s at each bit position of the rows' 32-bit words; the holders'
+ * counters are summed (e.g. an all-reduce of the 32 words across GPUs, or an
+ * elementwise add); ibp_meta_finalize applies the threshold rule of ibp_build_meta to
+ * the summed counters, n_elems being the total number of elements counted, and
+ * writes *d_meta. With one holder the pair equals ibp_build_meta. The rows of a
+ * count must be a whole number of 32-bit words. */
+int ibp_meta_count(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                   uint64_t *d_counters, ibp_stream_t s);
+int ibp_meta_finalize(const uint64_t *d_counters, int64_t n_elems, int dtype, double T,
+                      uint32_t block_elems, ibp_meta *d_meta, ibp_stream_t s);
+
 /* ibp_build_meta for callers that cannot allocate device memory (the paper has no
  * counterpart; this is a library convenience). Same arguments, checks and result
  * as ibp_build_meta, except that the counters live in a 256-byte array built into

@@ -60,7 +60,8 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_pack_scratch_bytes", "ibp_pack_offsets", "ibp_pack", "ibp_decompress_gather_packed",
            "ibp_decompress_range", "ibp_meta_positions_scratch_bytes", "ibp_build_meta_positions",
            "ibp_compress_positions", "ibp_decompress_gather_positions",
-           "ibp_decompress_gather_sized", "ibp_decompress_gather_batched")
+           "ibp_decompress_gather_sized", "ibp_decompress_gather_batched", "ibp_meta_count",
+           "ibp_meta_finalize")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -99,6 +100,8 @@ def load() -> ctypes.CDLL:
     lib.ibp_compress_positions.argtypes = [vp, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
     lib.ibp_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp,
                                                     i64, vp, vp, vp]
+    lib.ibp_meta_count.argtypes = [vp, i64, i64, i32, vp, vp]
+    lib.ibp_meta_finalize.argtypes = [vp, i64, i32, dbl, u32, vp, vp]
     lib.ibp_decompress_gather_batched.argtypes = [vp, i32, i64, i32, u32, vp, vp]
     lib.ibp_decompress_gather_sized.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, i64,
                                                 vp, vp, vp]
@@ -169,6 +172,23 @@ def build_meta(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Tenso
     _check(load().ibp_build_meta(_ptr(rows), n, L, dtype_code(rows, dtype), float(T),
                                  int(block_elems), _ptr(meta), _ptr(scratch), _stream(stream)),
            "ibp_build_meta")
+
+
+def meta_count(rows: torch.Tensor, counters: torch.Tensor, dtype: int | None = None,
+               stream=None) -> None:
+    """ibp_meta_count: per-bit 1-counts of ``rows`` into ``counters`` (32 x int64 on
+    the device, overwritten); counters of several row sets add up."""
+    n, L = _rows_shape(rows)
+    _check(load().ibp_meta_count(_ptr(rows), n, L, dtype_code(rows, dtype), _ptr(counters),
+                                 _stream(stream)), "ibp_meta_count")
+
+
+def meta_finalize(counters: torch.Tensor, n_elems: int, dtype: int, T: float, block_elems: int,
+                  meta: torch.Tensor, stream=None) -> None:
+    """ibp_meta_finalize: the threshold rule applied to (summed) ``counters``."""
+    _check(load().ibp_meta_finalize(_ptr(counters), int(n_elems), int(dtype), float(T),
+                                    int(block_elems), _ptr(meta), _stream(stream)),
+           "ibp_meta_finalize")
 
 
 def build_meta_noalloc(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Tensor,

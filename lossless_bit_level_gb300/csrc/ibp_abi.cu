@@ -220,6 +220,29 @@ int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtyp
                            reinterpret_cast<cudaStream_t>(s));
 }
 
+int ibp_meta_count(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
+                   uint64_t *d_counters, ibp_stream_t s) {
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (n_rows < 0 || row_elems <= 0 || row_elems > MAX_ROW_ELEMS) return IBP_ERR_ARG;
+  const int64_t bits = n_rows * row_elems * width_of(dtype);
+  if (bits % 32 != 0) return IBP_ERR_ARG;  // whole 32-bit words
+  if (!pointer_ok(d_counters, Where::device_only, 8)) return IBP_ERR_ARG;
+  if (n_rows > 0 && !pointer_ok(rows, Where::device_or_host, 16)) return IBP_ERR_ARG;
+  return launch_meta_count(rows, bits / 32, reinterpret_cast<unsigned long long *>(d_counters),
+                           reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_meta_finalize(const uint64_t *d_counters, int64_t n_elems, int dtype, double T,
+                      uint32_t block_elems, ibp_meta *d_meta, ibp_stream_t s) {
+  if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
+  if (n_elems <= 0 || !(T >= 0.0 && T <= 1.0)) return IBP_ERR_ARG;
+  if (block_elems != 32 && block_elems != 64) return IBP_ERR_UNSUPPORTED;
+  if (!pointer_ok(d_counters, Where::device_only, 8) || !pointer_ok(d_meta, Where::device_only, 16))
+    return IBP_ERR_ARG;
+  return launch_meta_finalize(reinterpret_cast<const unsigned long long *>(d_counters), n_elems,
+                              dtype, T, block_elems, d_meta, reinterpret_cast<cudaStream_t>(s));
+}
+
 int ibp_meta_select_scratch_bytes(size_t *bytes) {
   if (!bytes) return IBP_ERR_ARG;
   *bytes = select_scratch_bytes();

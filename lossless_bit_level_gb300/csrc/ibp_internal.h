@@ -40,6 +40,8 @@ int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, ui
 // 64-bit counters, then adds every n_words 32-bit word into them.
 int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *counters,
                       cudaStream_t s);
+int launch_meta_finalize(const unsigned long long *counters, int64_t n_elems, int dtype, double T,
+                         uint32_t block_elems, ibp_meta *d_meta, cudaStream_t s);
 int launch_build_meta_select(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                              double T, ibp_meta *d_meta, ibp_mask_candidate *d_candidates,
                              void *d_scratch, cudaStream_t s);

@@ -142,13 +142,18 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
+int launch_meta_finalize(const unsigned long long *counters, int64_t n_elems, int dtype, double T,
+                         uint32_t block_elems, ibp_meta *d_meta, cudaStream_t s) {
+  meta_finalize_kernel<<<1, 32, 0, s>>>(counters, n_elems, width_of(dtype), T, (uint32_t)dtype,
+                                        block_elems, d_meta);
+  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+}
+
 int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, uint32_t block_elems,
                       int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s) {
   unsigned long long *counters = static_cast<unsigned long long *>(d_scratch);
   if (int rc = launch_meta_count(rows, n_words, counters, s)) return rc;
-  meta_finalize_kernel<<<1, 32, 0, s>>>(counters, n_elems, width_of(dtype), T, (uint32_t)dtype,
-                                        block_elems, d_meta);
-  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
+  return launch_meta_finalize(counters, n_elems, dtype, T, block_elems, d_meta, s);
 }
 
 }  // namespace ibp

@@ -118,6 +118,11 @@ def test_argument_errors_before_cuda(lib):
                                                None, 2, None, None, None) == ibp.ERR_ARG
     assert lib.ibp_build_meta_positions(None, 10, 128, ibp.FP32, 0.9, 32, None, None, None,
                                         None) == ibp.ERR_ARG
+    # split preprocessing: counts of rows not whole 32-bit words, bad T, bad block
+    assert lib.ibp_meta_count(vp(16), 3, 3, ibp.W8, vp(16), None) == ibp.ERR_ARG
+    assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 1.2, 32, vp(16), None) == ibp.ERR_ARG
+    assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 0.9, 48, vp(16), None) == \
+        ibp.ERR_UNSUPPORTED
     # batched gathers: empty batch is a no-op; a null job array with jobs is refused
     assert lib.ibp_decompress_gather_batched(None, 0, 128, ibp.FP32, 32, None, None) == ibp.OK
     assert lib.ibp_decompress_gather_batched(None, 3, 128, ibp.FP32, 32, None, None) == ibp.ERR_ARG

@@ -50,3 +50,53 @@ def test_job_throughput_single_process():
     import bench
     t, gbs = bench.job_throughput(0.004, 2e9)
     assert t == 0.004 and gbs == pytest.approx(500.0)
+
+
+def _counts_worker(rank, world, port, q):
+    """Each rank holds a ragged shard of a seeded table (rank 2 none), counts its
+    words' bits on the host and sums the counts through allreduce_counts."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import numpy as np
+
+    import ibp_inputs as gen
+    from lossless_bit_level_gb300.sharded import allreduce_counts
+    words = gen.gnn_dense(1000).view(np.uint32)
+    bounds = [0, 377, 1000, 1000]
+    mine = words[bounds[rank]:bounds[rank + 1]]
+    w32 = mine.ravel()
+    counts = torch.tensor([int(((w32 >> np.uint32(j)) & np.uint32(1)).sum()) for j in range(32)],
+                          dtype=torch.int64)
+    total = allreduce_counts(counts, mine.size)
+    q.put((rank, total, counts.tolist()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_allreduce_counts_three_ranks():
+    """The metadata exchange over gloo: summed counters equal the counts of the
+    whole table and the element total is the table's, with one rank holding no rows."""
+    import numpy as np
+
+    import ibp_inputs as gen
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_counts_worker, args=(r, 3, port, q)) for r in range(3)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    words = gen.gnn_dense(1000).view(np.uint32).ravel()
+    want = [int(((words >> np.uint32(j)) & np.uint32(1)).sum()) for j in range(32)]
+    for rank, total, counts in res:
+        assert total == words.size
+        assert counts == want
+
+
+def test_allreduce_counts_rejects_bad_buffer():
+    from lossless_bit_level_gb300.sharded import allreduce_counts
+    with pytest.raises(ValueError):
+        allreduce_counts(torch.zeros(32, dtype=torch.int32), 1)
