@@ -70,6 +70,19 @@ WORKLOADS = {
         residency="host",
         desc="one DLRM embedding table 1,000,000 x 128 FP32 U(-1e-3,1e-3), T=0.95, B=32; "
              "gather 65,536 Zipf(1.05) lookups per step from pinned host slots (zero-copy)"),
+    "llm_kv": dict(
+        rows=lambda: gen.llm_kv(0, 0), dtype=ibp.BF16, T=0.9, B=64, batch=32_768,
+        index=lambda n, k, part: np.arange(k, dtype=np.int64) % n,
+        residency="host",
+        desc="LLM K cache of one layer, 8 x 4096 tokens x (32 heads x 128) BF16 N(0,1) with 41 "
+             "channels x10, T=0.9, B=64; every row streamed in order per step from pinned "
+             "host slots (zero-copy)"),
+    "llm_down": dict(
+        rows=lambda: gen.llm_weight(0, "down"), dtype=ibp.BF16, T=0.9, B=64, batch=4096,
+        index=lambda n, k, part: np.arange(k, dtype=np.int64) % n,
+        residency="host",
+        desc="LLM FFN down-projection weight 4096 x 11008 BF16 N(0,0.02), T=0.9, B=64; every "
+             "row streamed in order per step from pinned host slots (zero-copy)"),
 }
 
 
@@ -785,6 +798,12 @@ def workload_table(name):
     elif name == "tiny":
         wl["rows_prefix"] = lambda n: gen.tiny_fp32(min(n, 4096))
         wl["index_desc"] = "uniform"
+    elif name == "llm_kv":
+        wl["rows_prefix"] = lambda n: gen.llm_kv(0, 0, n_rows=min(n, 32_768))
+        wl["index_desc"] = "in-order"
+    elif name == "llm_down":
+        wl["rows_prefix"] = lambda n: gen.llm_weight(0, "down", n_rows=min(n, 4096))
+        wl["index_desc"] = "in-order"
     else:
         wl["rows_prefix"] = lambda n: gen.dlrm_table(0, min(n, 1_000_000))
         wl["index_desc"] = "Zipf(1.05)"
@@ -833,7 +852,8 @@ def run_reference(args, wl):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": f"u{8 * words.dtype.itemsize}",
+        "data": "synthetic",
         "config": {"workload": wl["desc"]},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -1039,8 +1059,10 @@ def main():
         extra["packed"] = packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier,
                                      table_raw, out_bytes, link, hbm_peak, dev)
         del sstore
-        extra["positions"] = positions_leg(store, wl, batches, out, steps, warmup, flush, barrier,
-                                           reps, table_raw, out_bytes, link, hbm_peak, dev)
+        if store.raw_bytes <= 16384:  # per-position tables are built for rows up to 16 KiB
+            extra["positions"] = positions_leg(store, wl, batches, out, steps, warmup, flush,
+                                               barrier, reps, table_raw, out_bytes, link,
+                                               hbm_peak, dev)
         if args.workload == "gnn_dense":
             extra["offload"] = offload_leg(dev)
         if args.workload == "dlrm_table":
@@ -1050,7 +1072,8 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": f"u{8 * words.dtype.itemsize}",
+        "data": "synthetic",
         "config": {"workload": wl["desc"], "rows": n, "row_elems": L, "T": wl["T"],
                    "block_elems": wl["B"], "batch": wl["batch"], "residency": residency,
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, then read)",

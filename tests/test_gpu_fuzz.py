@@ -21,18 +21,20 @@ pytestmark = pytest.mark.gpu
 WIDTHS = {8: (np.uint8, ibp.W8), 16: (np.uint16, ibp.BF16), 32: (np.uint32, ibp.FP32)}
 
 
-def draw_case(seed: int):
-    g = np.random.default_rng(seed)
+def draw_case(seed: int, long_rows: bool = False):
+    g = np.random.default_rng([seed, 1] if long_rows else seed)
     w = int(g.choice([8, 16, 32]))
     np_dt, code = WIDTHS[w]
     B = int(g.choice([32, 64]))
     step = 128 // w  # elements per 16 bytes: keeps shorter last blocks legal
-    if g.random() < 0.5:
+    if long_rows:  # rows of 2 KiB + 16 bytes to 40 KiB
+        L = step * int(g.integers(129, 2561))
+    elif g.random() < 0.5:
         L = B * int(g.integers(1, 12))
     else:
         L = step * int(g.integers(1, 4 * B // step * 3))
         L = max(L, step)
-    n = int(g.integers(1, 700))
+    n = int(g.integers(1, 120 if long_rows else 700))
     T = float(g.choice([0.5, 0.8, 0.9, 0.97, 1.0]))
     colhi = np.array([((1 << w) - 1) ^ ((1 << int(k)) - 1) for k in g.integers(1, w, size=L)],
                      dtype=np.uint64)
@@ -50,7 +52,16 @@ def draw_case(seed: int):
 
 @pytest.mark.parametrize("seed", range(120))
 def test_random_case(seed):
-    words, code, B, T, g = draw_case(seed)
+    run_case(seed, *draw_case(seed))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_long_rows(seed):
+    """Rows over 2 KiB (one CTA per row up to 32 KiB, one warp per row beyond)."""
+    run_case(seed, *draw_case(seed, long_rows=True))
+
+
+def run_case(seed, words, code, B, T, g):
     n, L = words.shape
     raw = L * words.dtype.itemsize
     wdt = {4: torch.int32, 2: torch.int16, 1: torch.uint8}[words.dtype.itemsize]

@@ -93,7 +93,9 @@ def test_llm_kv_rows():
     (BF16, np.uint16, 64, 4104), (FP32, np.uint32, 64, 4), (BF16, np.uint16, 32, 8),
     # 8-bit element words (B = 32 is 8 lane words per block)
     (W8, np.uint8, 32, 128), (W8, np.uint8, 64, 256), (W8, np.uint8, 32, 48),
-    (W8, np.uint8, 64, 4112), (W8, np.uint8, 32, 16), (W8, np.uint8, 64, 2048)])
+    (W8, np.uint8, 64, 4112), (W8, np.uint8, 32, 16), (W8, np.uint8, 64, 2048),
+    # 32 KiB rows (the longest one CTA encodes) and just past it
+    (FP32, np.uint32, 32, 8192), (FP32, np.uint32, 64, 8196), (BF16, np.uint16, 64, 16400)])
 def test_shapes_and_ragged_tails(dtype_code, np_dt, B, L):
     """Several tiles, odd block counts (half-used last chunk for 16-bit B=32),
     multi-segment rows, rows not a multiple of 32 blocks, shorter last blocks
@@ -116,10 +118,12 @@ def test_shapes_and_ragged_tails(dtype_code, np_dt, B, L):
     (0x0F0F0F0F, 0x0A0B0C0D & 0x0F0F0F0F),  # 4 runs
     (0x7F800000, 0x3F800000),
 ])
-def test_forced_masks_fp32(mask, bitval):
-    """Meta written directly (any mask is a valid code): compress + gather vs oracle."""
+@pytest.mark.parametrize("L", [128, 1600])
+def test_forced_masks_fp32(mask, bitval, L):
+    """Meta written directly (any mask is a valid code): compress + gather vs oracle,
+    on short rows and on 6.4 KB rows (one CTA per row)."""
     g = np.random.default_rng(mask & 0xFFFF)
-    n, L, B = 200, 128, 32
+    n, B = 200, 32
     rnd = g.integers(0, 1 << 32, size=(n, L), dtype=np.uint64).astype(np.uint32)
     keep = g.random(size=(n, L)) < 0.995
     words = np.where(keep, (rnd & ~np.uint32(mask)) | np.uint32(bitval), rnd).astype(np.uint32)
