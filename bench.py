@@ -263,6 +263,25 @@ def measure_hbm_copy(dev, nbytes=1 << 30, reps=10):
     return best
 
 
+def measure_launch_floor(dev, flush, reps=20):
+    """CUDA-event time of a one-element kernel right after the L2 flush, the way a
+    gather step is timed: the floor that any single-launch step pays (launch,
+    dispatch and the two event records), in seconds (mean after 3 warm-ups)."""
+    tiny = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream()
+    ts = []
+    for k in range(reps + 3):
+        flush()
+        a, b = event_pair(s)
+        a.record(s)
+        tiny.add_(1)
+        b.record(s)
+        b.synchronize()
+        if k >= 3:
+            ts.append(a.elapsed_time(b) * 1e-3)
+    return float(np.mean(ts))
+
+
 def job_throughput(t_local: float, bytes_per_step_local: float, dist=None, device=None):
     """Whole-job throughput of independent replicas: every rank processed
     bytes_per_step_local per step; the job's step time is the slowest rank's, so the
@@ -936,6 +955,7 @@ def main():
 
     link = measure_link(dev)
     hbm_copy_now = measure_hbm_copy(dev)
+    launch_floor = measure_launch_floor(dev, flush)
     torch.cuda.empty_cache()
 
     # preprocessing stages (timed with CUDA events; raw input bytes per second)
@@ -1097,6 +1117,9 @@ def main():
                          "residency": residency},
         },
         "link": link, "hbm_copy_gbs_this_run": hbm_copy_now,
+        "launch_floor_us": {"value": launch_floor * 1e6,
+                            "what": "CUDA-event time of a one-element kernel after the L2 "
+                                    "flush, timed like a gather step"},
         "e2e": extra.pop("e2e", None),
     }
     line.update(extra)
