@@ -64,6 +64,12 @@ struct GatherArgs {
   int64_t n_units;
   int64_t raw_bytes;
   int cta0, ncta;  // the CTAs [cta0, cta0 + ncta) of the grid work on this gather
+  // Sized gather: the staged prefix of a slot ends on a multiple of this many bytes
+  // of the address space (within the slot). Packed store: the staged bytes start and
+  // end on such multiples (within the store and the staging buffer) around the entry.
+  // 128 for host memory, where a partly read 128-byte line costs the link about as
+  // much as a whole one; 16 for HBM.
+  uint32_t span_align;
 };
 
 // The plan of one unit (identical in every lane of its team).
@@ -76,6 +82,8 @@ struct Unit {
   uint32_t segp;       // participation bits of the segment's blocks (0 for raw rows);
                        // the row index when lsb == PARSE_HEADER
   uint32_t bmw;        // bitmask word of the row (only when lsb == PARSE_HEADER)
+  uint32_t echunk;     // packed entry or sized span: its 16-byte chunks (checks)
+  uint32_t lead;       // staged bytes in front of the entry (whole-line staging)
 };
 
 // Unit.lsb value telling the decoder to take the participation bits from the
@@ -100,7 +108,8 @@ __device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u) {
 
 // The bytes of row r to stage, [o0, o1) of the buffer at slots: a packed store's
 // entry, or (sized gather) the used prefix of the row's slot from its bitmask bit
-// and bit count, rounded up to 16 bytes. Both 0 for a bad index.
+// and bit count, extended to an address that is a multiple of span_align (16 or
+// 128) and cut at the slot's end. Both 0 for a bad index.
 struct EntrySpan {
   uint64_t o0, o1;
 };
@@ -115,9 +124,11 @@ __device__ __forceinline__ EntrySpan load_span(const GatherArgs &a, int64_t r) {
     const uint32_t bits = __ldg(a.row_bits + r);
     const bool comp = (__ldg(a.bitmask + (r >> 5)) >> (r & 31)) & 1u;
     const uint64_t used = comp ? 4ull * (((uint64_t)bits + 31) >> 5) : (uint64_t)a.raw_bytes;
-    const uint64_t len = (used + 15) & ~(uint64_t)15;
     const uint64_t slot = (uint64_t)a.slot_bytes;
     e.o0 = (uint64_t)r * slot;
+    const uint64_t base = (uint64_t)(uintptr_t)a.slots;
+    const uint64_t al = a.span_align;
+    const uint64_t len = ((base + e.o0 + used + al - 1) & ~(al - 1)) - (base + e.o0);
     e.o1 = e.o0 + (len < slot ? len : slot);
   }
   return e;
@@ -137,6 +148,8 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   un.lsb = 0;
   un.segp = 0;
   un.bmw = 0;
+  un.echunk = 0;
+  un.lead = 0;
   if (u >= a.n_units) return un;
   int64_t i = u;
   int s = 0;
@@ -174,9 +187,29 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
     // later, off the critical path
     un.src = slot;
     un.nchunk = PACKED ? (uint32_t)min((int64_t)nvec, avail >> 4) : nvec;
+    un.echunk = un.nchunk;
     un.nvec = nvec;
     un.lsb = PARSE_HEADER;
     un.segp = (uint32_t)r;
+    if (PACKED && a.offsets && a.span_align > 16) {
+      // whole lines around the entry: from the line it starts in to the end of the
+      // line it ends in, inside the store and leaving the staging buffer room for
+      // the decoder's look-ahead word
+      const uint64_t al = a.span_align;
+      const uint64_t base = (uint64_t)(uintptr_t)a.slots;
+      const uint64_t e0 = base + span.o0;
+      uint64_t s0 = e0 & ~(al - 1);
+      if (s0 < base) s0 = base;
+      uint64_t s1 = (base + span.o1 + al - 1) & ~(al - 1);
+      if (s1 > base + a.packed_bytes) s1 = base + a.packed_bytes;
+      const uint64_t cap = (uint64_t)a.unit_bytes - 16;
+      if (e0 - s0 + 16ull * un.echunk <= cap) {
+        if (s1 - s0 > cap) s1 = s0 + cap;
+        un.src = a.slots + (s0 - base);
+        un.lead = (uint32_t)(e0 - s0);
+        un.nchunk = (uint32_t)((s1 - s0) >> 4);
+      }
+    }
     return un;
   }
   if (!((__ldg(a.bitmask + (r >> 5)) >> (r & 31)) & 1u)) {  // stored raw
@@ -251,8 +284,10 @@ template <int NR, int TL, bool PACKED>
 __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &code,
                                             const RegRuns<NR> &runs, const SharedRuns &sruns,
                                             const Unit &un, const uint8_t *buf, int tl) {
+  // the staged bytes start un.lead bytes before the entry (whole-line staging)
   const uint32_t fc = (uint32_t)code.fc;
   const uint32_t shrink = 32u - fc;
+  buf += un.lead;
   const uint32_t *S = reinterpret_cast<const uint32_t *>(buf);
   uint4 *dst = reinterpret_cast<uint4 *>(a.out + un.out_word);
   uint32_t segp = un.segp, lsb = un.lsb, nvec = un.nvec;
@@ -260,19 +295,19 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
     if (!((un.bmw >> (segp & 31)) & 1u)) {  // stored raw: the slot prefix is the row
       segp = 0;
       lsb = 0;
-      if (PACKED && un.nchunk < nvec) {  // a packed entry shorter than the raw row
+      if (PACKED && un.echunk < nvec) {  // a packed entry shorter than the raw row
         if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
         nvec = 0;
       }
     } else {  // participation bits are S[0] (one segment, nb <= 32)
-      segp = (!PACKED || un.nchunk) ? (S[0] & low_mask((uint32_t)a.nb)) : 0u;
+      segp = (!PACKED || un.echunk) ? (S[0] & low_mask((uint32_t)a.nb)) : 0u;
       lsb = (uint32_t)a.nb;
       const uint32_t p_last = (segp >> (a.nb - 1)) & 1u;
       const uint32_t total =
           (uint32_t)a.nb + 32u * (uint32_t)a.raw_words -
           shrink * ((uint32_t)a.lwb * __popc(segp) - (uint32_t)(a.lwb - a.lwt) * p_last);
       const int64_t used = (int64_t)((total + 31) >> 5) * 4;
-      if (used >= a.raw_bytes || (PACKED && used > 16 * (int64_t)un.nchunk)) {
+      if (used >= a.raw_bytes || (PACKED && used > 16 * (int64_t)un.echunk)) {
         if (tl == 0) report(a.status, IBP_ERR_CORRUPT);
         nvec = 0;
       }
@@ -318,7 +353,7 @@ __device__ __forceinline__ void decode_unit(const GatherArgs &a, const Code &cod
 // Decode-time fields of a staged unit, kept in shared memory next to its buffer.
 struct __align__(16) StagedMeta {
   int64_t out_word;
-  uint32_t lsb, segp, nvec, bmw, nchunk;
+  uint32_t lsb, segp, nvec, bmw, nchunk, lead;  // nchunk, lead: Unit.echunk, Unit.lead
 };
 
 template <int NR, int TL, bool PACKED>
@@ -370,7 +405,8 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
       m.segp = un.segp;
       m.nvec = un.nvec;
       m.bmw = 0;
-      m.nchunk = PACKED ? un.nchunk : 0u;
+      m.nchunk = PACKED ? un.echunk : 0u;
+      m.lead = PACKED ? un.lead : 0u;
       metas[k_plan * TPW] = m;
     }
     stage_unit<TL>(un, bufs + k_plan * buf_step, tl);
@@ -396,7 +432,9 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     const StagedMeta m = metas[k_dec * TPW];
     Unit un;
     un.src = nullptr;
-    un.nchunk = PACKED ? m.nchunk : 0u;
+    un.nchunk = 0u;
+    un.echunk = PACKED ? m.nchunk : 0u;
+    un.lead = PACKED ? m.lead : 0u;
     un.out_word = m.out_word;
     un.lsb = m.lsb;
     un.segp = m.segp;
@@ -592,6 +630,8 @@ __device__ __forceinline__ Unit ws_take(const GatherArgs &a, int64_t k, int64_t 
   un.lsb = 0;
   un.segp = 0;
   un.bmw = 0;
+  un.echunk = 0;
+  un.lead = 0;  // slots in device memory: spans are staged exactly
   *ok = true;
   if (k >= count) return un;
   const int slot = (int)(k % PLAN_SLOTS);
@@ -601,6 +641,7 @@ __device__ __forceinline__ Unit ws_take(const GatherArgs &a, int64_t k, int64_t 
     un.src = p.src;
     un.out_word = p.out_word;
     un.nchunk = p.nchunk;
+    un.echunk = p.nchunk;
     un.lsb = p.lsb;
     un.segp = p.segp;
     un.nvec = p.nvec;
@@ -787,10 +828,11 @@ int launch_ws(GatherArgs a, const RowGeom &g, const DeviceInfo &dev, cudaStream_
 template <bool PACKED>
 int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const DeviceInfo &dev,
                 cudaStream_t s) {
-  // units of at most 1 KiB in device memory: team size 4 or 8, 4 CTAs per SM (3 for
-  // packed stores, whose extra span registers would spill at 4)
+  // units of at most 1 KiB in device memory: team size 4 or 8, 4 CTAs per SM. The
+  // packed and sized instantiations spill 32 bytes at that register budget and are
+  // still 10% faster than at 3 CTAs per SM (measured on a packed store in HBM).
   if (slots_in_device_memory) {
-    constexpr int MINB = PACKED ? 3 : 4;
+    constexpr int MINB = 4;
     if (tl == 4) return launch_tl<4, MINB, PACKED>(a, dev, s);
     return launch_tl<8, MINB, PACKED>(a, dev, s);
   }
@@ -819,6 +861,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.ncta = 0;
   a.offsets = d_offsets;
   a.row_bits = d_offsets ? nullptr : d_row_bits;
+  a.span_align = slots_in_device_memory ? 16u : 128u;
   a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
   a.n_rows = n_rows;
   a.bitmask = d_bitmask;
@@ -867,6 +910,7 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
   BatchArgs b;
   GatherArgs &a = b.common;
   a = GatherArgs{};
+  a.span_align = 16u;
   a.status = d_status;
   a.dtype = dtype;
   a.block_elems = (uint32_t)g.B;
