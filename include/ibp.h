@@ -117,15 +117,21 @@ int ibp_meta_scratch_bytes(size_t *bytes);
 int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtype, double T,
                    uint32_t block_elems, ibp_meta *d_meta, void *d_scratch, ibp_stream_t s);
 
-/* Preprocessing in two steps, for rows held in several places (shards of a table on
- * several GPUs, or batches streamed one after another): bit counts are additive.
- * ibp_meta_count overwrites d_counters (32 uint64 words, device memory, 256 bytes)
- * with the number of 1s at each bit position of the rows' 32-bit words; the holders'
- * counters are summed (e.g. an all-reduce of the 32 words across GPUs, or an
- * elementwise add); ibp_meta_finalize applies the threshold rule of ibp_build_meta to
- * the summed counters, n_elems being the total number of elements counted, and
- * writes *d_meta. With one holder the pair equals ibp_build_meta. The rows of a
- * count must be a whole number of 32-bit words. */
+/* Preprocessing ("Core algorithm", preprocessing) in two steps, for rows held in
+ * several places (shards of a table on several GPUs, or batches streamed one after
+ * another): the per-position counts of disjoint row sets add up.
+ * ibp_meta_count: rows as for ibp_build_meta (device or registered host memory, a
+ * whole number of 32-bit words, 16-byte aligned; n_rows may be 0). Overwrites
+ * d_counters (32 uint64 words = 256 bytes of device memory, 8-byte aligned) with the
+ * number of 1s at each bit position of the rows' 32-bit words (8- and 16-bit elements
+ * are folded into their element positions by the finalize step).
+ * The holders' counters are then summed by the caller (an all-reduce of the 32 words
+ * across GPUs, or an elementwise add on one GPU).
+ * ibp_meta_finalize: applies the threshold rule of ibp_build_meta to the summed
+ * counters, n_elems (> 0) being the total number of elements counted, and writes
+ * *d_meta. T outside [0, 1] or n_elems <= 0: IBP_ERR_ARG; block_elems not 32 or 64:
+ * IBP_ERR_UNSUPPORTED. With one holder the pair equals ibp_build_meta. Both calls are
+ * asynchronous on s and allocate nothing. */
 int ibp_meta_count(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
                    uint64_t *d_counters, ibp_stream_t s);
 int ibp_meta_finalize(const uint64_t *d_counters, int64_t n_elems, int dtype, double T,
