@@ -64,6 +64,8 @@ class Oracle:
                                          ctypes.POINTER(u32), vp, vp, ctypes.POINTER(i32)]
         lib.ibpo_select_meta.restype = i32
         lib.ibpo_build_meta_positions.argtypes = [vp, i64, i64, i32, dbl, vp, vp]
+        lib.ibpo_build_meta_block_positions.argtypes = [vp, i64, i64, i32, dbl, i64, vp, vp]
+        lib.ibpo_build_meta_block_positions.restype = ctypes.c_int
         lib.ibpo_build_meta_positions.restype = i32
         lib.ibpo_compress_positions.argtypes = [vp, i64, i64, i32, i64, vp, vp, vp, i64, vp, vp]
         lib.ibpo_compress_positions.restype = i32
@@ -104,6 +106,22 @@ class Oracle:
         rc = self.lib.ibpo_build_meta_positions(_ptr(a), n, L, w, float(T), _ptr(pm), _ptr(pb))
         if rc != OK:
             raise ValueError(f"oracle build_meta_positions rejected its arguments ({rc})")
+        return pm, pb
+
+    def build_meta_block_positions(self, rows: np.ndarray, T: float, block_elems: int):
+        """Block-position (mask, bitval) arrays, written one entry per element
+        position (entry e holds the pair of block position e % block_elems)."""
+        a = np.ascontiguousarray(rows)
+        if a.ndim != 2:
+            raise ValueError("rows must be 2-D")
+        w = _width(a)
+        n, L = a.shape
+        pm = np.zeros(L, dtype=np.uint32)
+        pb = np.zeros(L, dtype=np.uint32)
+        rc = self.lib.ibpo_build_meta_block_positions(_ptr(a), n, L, w, float(T),
+                                                      int(block_elems), _ptr(pm), _ptr(pb))
+        if rc != OK:
+            raise ValueError(f"oracle build_meta_block_positions rejected its arguments ({rc})")
         return pm, pb
 
     def compress_positions(self, rows: np.ndarray, block_elems: int, pmask: np.ndarray,
@@ -290,6 +308,10 @@ def build_meta(elems: np.ndarray, T: float) -> tuple[int, int]:
 
 def build_meta_positions(rows, T):
     return default().build_meta_positions(rows, T)
+
+
+def build_meta_block_positions(rows, T, block_elems):
+    return default().build_meta_block_positions(rows, T, block_elems)
 
 
 def compress_positions(rows, block_elems, pmask, pbitval, slot_bytes_=None):

@@ -403,6 +403,38 @@ extern "C" int ibpo_build_meta_positions(const void *rows, int64_t n_rows, int64
   return IBPO_OK;
 }
 
+/* Block-position metadata: one mask/bitval per position q within a block, from the
+ * sample made of the element at position q of every block of every row (a shorter
+ * last block adds only the positions it has); element e of a row takes the pair of
+ * its position e % block_elems. */
+extern "C" int ibpo_build_meta_block_positions(const void *rows, int64_t n_rows,
+                                               int64_t row_elems, int w_bits, double T,
+                                               int64_t block_elems, uint32_t *pmask_out,
+                                               uint32_t *pbitval_out) {
+  if (!rows || n_rows <= 0 || row_elems <= 0 || block_elems <= 0 || !valid_width(w_bits) ||
+      !pmask_out || !pbitval_out)
+    return IBPO_BAD_ARG;
+  const unsigned char *base = (const unsigned char *)rows;
+  const int nbytes = w_bits / 8;
+  const int64_t npos = block_elems < row_elems ? block_elems : row_elems;
+  std::vector<unsigned char> sample;
+  for (int64_t q = 0; q < npos; ++q) {
+    sample.clear();
+    for (int64_t r = 0; r < n_rows; ++r)
+      for (int64_t e = q; e < row_elems; e += block_elems)
+        for (int k = 0; k < nbytes; ++k) sample.push_back(base[(r * row_elems + e) * nbytes + k]);
+    uint32_t mask = 0, bitval = 0;
+    int rc = ibpo_build_meta(sample.data(), (int64_t)(sample.size() / nbytes), w_bits, T, &mask,
+                             &bitval);
+    if (rc != IBPO_OK) return rc;
+    for (int64_t e = q; e < row_elems; e += block_elems) {
+      pmask_out[e] = mask;
+      pbitval_out[e] = bitval;
+    }
+  }
+  return IBPO_OK;
+}
+
 /* Packed store: each selected row's used bytes, rounded up to 16, end to end. */
 extern "C" int ibpo_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t row_elems,
                          int w_bits, const uint32_t *bitmask, const uint32_t *row_bits,

@@ -62,6 +62,17 @@ int ibpo_build_meta(const void *elems, int64_t n_elems, int w_bits, double T,
 int ibpo_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems, int w_bits,
                               double T, uint32_t *pmask_out, uint32_t *pbitval_out);
 
+/* Block-position metadata (a variant of preprocessing: the block-sized reading of the
+ * "kilobyte-scale" metadata). Position q of a block (0 <= q < block_elems) gets its
+ * own mask/bitval pair: the rule of ibpo_build_meta applied to the sample made of
+ * the element at position q of every block of every row (a shorter last block adds
+ * only the positions it has). Written row-sized, like ibpo_build_meta_positions:
+ * element e of a row gets the pair of position e % block_elems, so the per-position
+ * compression and gather take the result as it is. */
+int ibpo_build_meta_block_positions(const void *rows, int64_t n_rows, int64_t row_elems,
+                                    int w_bits, double T, int64_t block_elems,
+                                    uint32_t *pmask_out, uint32_t *pbitval_out);
+
 /* Compression and decompress-gather with per-position metadata: as ibpo_compress /
  * ibpo_decompress_gather, except that element e of a block is tested against
  * pmask[e]/pbitval[e] and, in a matching block, stored as a field of

@@ -567,9 +567,56 @@ def check_pack_round_trip(o):
         assert rc == -6 and np.array_equal(out, sentinel)
 
 
+def check_block_positions_hand_example(o):
+    """Block-position metadata on the hand-worked 8-bit rows with a shorter last
+    block (golden file), and compression with the tiled tables."""
+    d = load_hand_example("block_positions_example_u8.txt", np.uint8)
+    pm, pb = o.build_meta_block_positions(d["rows"], d["T"], d["block"])
+    assert pm.tolist() == d["pmask"] and pb.tolist() == d["pbitval"], (pm, pb)
+    slots, bitmask, row_bits = o.compress_positions(d["rows"], d["block"], pm, pb)
+    assert list(row_bits) == d["row_bits"]
+    assert int(bitmask[0]) == d["bitmask"]
+    for r, words in enumerate(d["streams"]):
+        assert slots[r, :4].view("<u4").tolist() == words, (r, slots[r, :4].view("<u4"))
+    out, rc = o.decompress_gather_positions(slots, 2, 6, np.uint8, d["block"], bitmask, pm, pb,
+                                            np.array([1, 0, 1]))
+    assert rc == 0 and np.array_equal(out, d["rows"][[1, 0, 1]])
+
+
+def check_block_positions_reductions(o):
+    """Block-position metadata: position q is the brute-force rule over the
+    elements q, q + B, q + 2B, ... of every row, and every element takes its
+    position's pair; with B = 1 it is the shared mask, with B >= L the per-element
+    metadata. Rows with and without a shorter last block."""
+    g = np.random.default_rng(77)
+    for dt, w, B, L in ((np.uint32, 32, 8, 40), (np.uint16, 16, 16, 56), (np.uint8, 8, 4, 22),
+                        (np.uint8, 8, 32, 32)):
+        n = 50
+        colconst = g.integers(0, 1 << w, size=B, dtype=np.uint64)
+        colhi = np.array([((1 << w) - 1) ^ ((1 << int(k)) - 1) for k in
+                          g.integers(1, w, size=B)], dtype=np.uint64)
+        base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+        q_of = np.arange(L) % B
+        flip = g.random(size=(n, L)) < 0.05
+        x = np.where(flip, base, (base & ~colhi[q_of]) | (colconst[q_of] & colhi[q_of]))
+        x = x.astype(dt)
+        for T in (0.8, 0.95, 1.0):
+            pm, pb = o.build_meta_block_positions(x, T, B)
+            for q in range(min(B, L)):
+                want = brute_meta(x[:, q::B], T)
+                assert all((int(pm[e]), int(pb[e])) == want for e in range(q, L, B)), (w, q)
+            assert (o.build_meta_block_positions(x, T, 1)[0] == o.build_meta(x, T)[0]).all()
+            assert (o.build_meta_block_positions(x, T, 1)[1] == o.build_meta(x, T)[1]).all()
+            for BB in (L, L + 5):
+                a = o.build_meta_block_positions(x, T, BB)
+                b = o.build_meta_positions(x, T)
+                assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_meta_closed_forms, check_size_formula, check_stream_layout,
               check_round_trip_specials, check_select_examples,
               check_select_threshold_sweep, check_pack_hand_example, check_pack_round_trip,
               check_hand_example_u8_tail, check_tail_blocks_and_bytes,
-              check_positions_hand_example, check_positions_meta_and_sizes]
+              check_positions_hand_example, check_positions_meta_and_sizes,
+              check_block_positions_hand_example, check_block_positions_reductions]

@@ -114,6 +114,15 @@ PLANTED = [
     ("positions metadata samples position 0 only",
      "column[(size_t)(r * nbytes + k)] = base[(r * row_elems + e) * nbytes + k];",
      "column[(size_t)(r * nbytes + k)] = base[(r * row_elems) * nbytes + k];"),
+    ("block positions sample only the first block",
+     "      for (int64_t e = q; e < row_elems; e += block_elems)\n        for (int k = 0; k < nbytes; ++k) sample",
+     "      for (int64_t e = q; e < row_elems && e < block_elems; e += block_elems)\n        for (int k = 0; k < nbytes; ++k) sample"),
+    ("block positions tiled by block index",
+     "    for (int64_t e = q; e < row_elems; e += block_elems) {\n      pmask_out[e] = mask;",
+     "    for (int64_t e = q * block_elems; e < row_elems && e < (q + 1) * block_elems; ++e) {\n      pmask_out[e] = mask;"),
+    ("block positions count a shorter last block as full",
+     "    int rc = ibpo_build_meta(sample.data(), (int64_t)(sample.size() / nbytes), w_bits, T, &mask,",
+     "    while ((int64_t)(sample.size() / nbytes) < n_rows * ((row_elems + block_elems - 1) / block_elems))\n      for (int k = 0; k < nbytes; ++k) sample.push_back(0);\n    int rc = ibpo_build_meta(sample.data(), (int64_t)(sample.size() / nbytes), w_bits, T, &mask,"),
     ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
      "*bitval_out = bitval0;"),
 ]
