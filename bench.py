@@ -496,7 +496,9 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
                   out_bytes, link, hbm_peak, dev, thresholds=(None, 0.99)):
     """Per-position metadata (one mask/bitval per element position of a row): the
     metadata build, the compression and the same gathers, at the workload's T and at
-    T = 0.99. Compresses into the store's slot buffer (the other legs are done)."""
+    T = 0.99; then block-position metadata (one pair per position within a block) at
+    the workload's T. Compresses into the store's slot buffer (the other legs are
+    done)."""
     n, L, dt, B = store.n, store.L, store.dtype, store.B
     pm = torch.zeros(L, dtype=torch.int32, device=dev)
     pb = torch.zeros(L, dtype=torch.int32, device=dev)
@@ -505,12 +507,15 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
     bitmask = torch.zeros_like(store.bitmask)
     row_bits = torch.zeros_like(store.row_bits)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    res = {"metadata_bytes": 8 * L}
-    for T in thresholds:
-        T = wl["T"] if T is None else T
+    res = {"metadata_bytes": 8 * L, "block_positions_metadata_bytes": 8 * B}
+    modes = [(f"T={wl['T'] if T is None else T}", wl["T"] if T is None else T, False)
+             for T in thresholds]
+    modes.append((f"block_positions T={wl['T']}", wl["T"], True))
+    for key, T, per_block in modes:
+        build = ibp.build_meta_block_positions if per_block else ibp.build_meta_positions
 
         def meta():
-            ibp.build_meta_positions(store.rows, T, B, pm, pb, scratch, dtype=dt)
+            build(store.rows, T, B, pm, pb, scratch, dtype=dt)
 
         def comp():
             ibp.compress_positions(store.rows, B, pm, pb, store.slots, bitmask, row_bits, dtype=dt)
@@ -535,7 +540,7 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
         assert int(status.item()) == 0
         ts = float(np.mean(per_step))
         peak = link["h2d_memcpy_gbs"] if store.residency == "host" else hbm_peak
-        res[f"T={T}"] = {
+        res[key] = {
             "space_saving_pct": 100.0 * (1.0 - stored.sum() / table_raw),
             "build_meta_ms": mt * 1e3, "build_meta_frac": table_raw / mt / 1e9 / peak,
             "compress_ms": ct * 1e3,

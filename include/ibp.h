@@ -330,6 +330,22 @@ int ibp_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems
                              double T, uint32_t block_elems, uint32_t *d_pmask,
                              uint32_t *d_pbitval, void *d_scratch, ibp_stream_t s);
 
+/* Block-position metadata (the block-sized reading of the "kilobyte-scale" metadata
+ * of "Core algorithm", preprocessing; the layout is the library's). Position q of a
+ * block (0 <= q < block_elems) gets one mask/bitval pair: the preprocessing rule of
+ * ibp_build_meta applied to the sample made of the element at position q of every
+ * block of every row (a shorter last block adds only the positions it has, so the
+ * sample of position q has n_rows * ceil((row_elems - q) / block_elems) elements).
+ * The result is written row-sized, like ibp_build_meta_positions: d_pmask[e] and
+ * d_pbitval[e] (row_elems entries each, device memory) hold the pair of position
+ * e % block_elems, so ibp_compress_positions and ibp_decompress_gather_positions
+ * take them as they are. Same arguments, limits, scratch
+ * (ibp_meta_positions_scratch_bytes) and errors as ibp_build_meta_positions;
+ * asynchronous on s. */
+int ibp_build_meta_block_positions(const void *rows, int64_t n_rows, int64_t row_elems,
+                                   int dtype, double T, uint32_t block_elems, uint32_t *d_pmask,
+                                   uint32_t *d_pbitval, void *d_scratch, ibp_stream_t s);
+
 /* ibp_compress with per-position metadata (no *d_meta; no device-detected errors). */
 int ibp_compress_positions(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
                            uint32_t block_elems, const uint32_t *d_pmask,

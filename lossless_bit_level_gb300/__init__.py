@@ -61,7 +61,7 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_decompress_range", "ibp_meta_positions_scratch_bytes", "ibp_build_meta_positions",
            "ibp_compress_positions", "ibp_decompress_gather_positions",
            "ibp_decompress_gather_sized", "ibp_decompress_gather_batched", "ibp_meta_count",
-           "ibp_meta_finalize")
+           "ibp_meta_finalize", "ibp_build_meta_block_positions")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -101,6 +101,7 @@ def load() -> ctypes.CDLL:
     lib.ibp_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp,
                                                     i64, vp, vp, vp]
     lib.ibp_meta_count.argtypes = [vp, i64, i64, i32, vp, vp]
+    lib.ibp_build_meta_block_positions.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
     lib.ibp_meta_finalize.argtypes = [vp, i64, i32, dbl, u32, vp, vp]
     lib.ibp_decompress_gather_batched.argtypes = [vp, i32, i64, i32, u32, vp, vp]
     lib.ibp_decompress_gather_sized.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, i64,
@@ -313,6 +314,18 @@ def meta_positions_scratch_bytes(row_elems: int, dtype: int) -> int:
     _check(load().ibp_meta_positions_scratch_bytes(int(row_elems), int(dtype), ctypes.byref(out)),
            "ibp_meta_positions_scratch_bytes")
     return out.value
+
+
+def build_meta_block_positions(rows: torch.Tensor, T: float, block_elems: int,
+                               pmask: torch.Tensor, pbitval: torch.Tensor, scratch: torch.Tensor,
+                               dtype: int | None = None, stream=None) -> None:
+    """ibp_build_meta_block_positions: one mask/bitval per position within a block,
+    written row-sized (entry e holds the pair of position e % block_elems)."""
+    n, L = _rows_shape(rows)
+    _check(load().ibp_build_meta_block_positions(_ptr(rows), n, L, dtype_code(rows, dtype),
+                                                 float(T), int(block_elems), _ptr(pmask),
+                                                 _ptr(pbitval), _ptr(scratch), _stream(stream)),
+           "ibp_build_meta_block_positions")
 
 
 def build_meta_positions(rows: torch.Tensor, T: float, block_elems: int, pmask: torch.Tensor,

@@ -481,6 +481,21 @@ int ibp_build_meta_positions(const void *rows, int64_t n_rows, int64_t row_elems
                                      reinterpret_cast<cudaStream_t>(s));
 }
 
+int ibp_build_meta_block_positions(const void *rows, int64_t n_rows, int64_t row_elems,
+                                   int dtype, double T, uint32_t block_elems, uint32_t *d_pmask,
+                                   uint32_t *d_pbitval, void *d_scratch, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (g.raw_bytes > POS_MAX_ROW_BYTES) return IBP_ERR_UNSUPPORTED;
+  if (n_rows <= 0 || !(T >= 0.0 && T <= 1.0)) return IBP_ERR_ARG;
+  if (!pointer_ok(rows, Where::device_or_host, 16) || !pointer_ok(d_pmask, Where::device_only, 4) ||
+      !pointer_ok(d_pbitval, Where::device_only, 4) ||
+      !pointer_ok(d_scratch, Where::device_only, 8))
+    return IBP_ERR_ARG;
+  return launch_build_meta_positions(rows, n_rows, g, T, d_pmask, d_pbitval, d_scratch,
+                                     reinterpret_cast<cudaStream_t>(s), true);
+}
+
 int ibp_compress_positions(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
                            uint32_t block_elems, const uint32_t *d_pmask,
                            const uint32_t *d_pbitval, void *slots, int64_t slot_bytes,

@@ -76,9 +76,10 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
                           cudaStream_t s);
 size_t pack_scratch_bytes(int64_t n_sel);
 size_t pos_scratch_bytes(const RowGeom &g);
+// per_block_position: one pair per position within a block, written row-sized.
 int launch_build_meta_positions(const void *rows, int64_t n_rows, const RowGeom &g, double T,
                                 uint32_t *d_pmask, uint32_t *d_pbitval, void *d_scratch,
-                                cudaStream_t s);
+                                cudaStream_t s, bool per_block_position = false);
 int launch_compress_positions(const void *rows, int64_t n_rows, const RowGeom &g,
                               const uint32_t *d_pmask, const uint32_t *d_pbitval, void *slots,
                               int64_t slot_bytes, uint32_t *d_bitmask, uint32_t *d_row_bits,

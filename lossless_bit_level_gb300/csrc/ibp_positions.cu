@@ -193,6 +193,42 @@ __global__ void pos_finalize_kernel(const unsigned long long *counters, int64_t 
   pbitval[p] = bitval;
 }
 
+// Block-position metadata: position q of a block takes the rule over the counts of
+// every element position e with e % B == q (the element at position q of every
+// block of every row; a shorter last block contributes only the positions it has),
+// then every element position gets its block position's pair. One CTA.
+__global__ void pos_block_finalize_kernel(const unsigned long long *counters, int64_t n_rows,
+                                          int row_elems, int w, int B, double T,
+                                          uint32_t *pmask, uint32_t *pbitval) {
+  __shared__ uint32_t qmask[64], qbitval[64];
+  const int q = threadIdx.x;
+  const int epw = 32 / w;
+  if (q < B && q < row_elems) {
+    const int64_t copies = (row_elems - q + B - 1) / B;  // blocks that have position q
+    const unsigned long long N = (unsigned long long)(n_rows * copies);
+    uint32_t mask = 0, bitval = 0;
+    for (int j = 0; j < w; ++j) {
+      unsigned long long c1 = 0;
+      for (int e = q; e < row_elems; e += B)
+        c1 += counters[(int64_t)(e / epw) * 32 + (e % epw) * w + j];
+      const unsigned long long c0 = N - c1;
+      const bool v = c1 > c0;  // a tie keeps 0
+      const unsigned long long held = v ? c1 : c0;
+      if ((double)held >= T * (double)N) {
+        mask |= 1u << j;
+        bitval |= (uint32_t)v << j;
+      }
+    }
+    qmask[q] = mask;
+    qbitval[q] = bitval;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < row_elems; e += blockDim.x) {
+    pmask[e] = qmask[e % B];
+    pbitval[e] = qbitval[e % B];
+  }
+}
+
 // ---------------------------------------------------------------- compress
 struct PosCompressArgs {
   const uint8_t *rows;
@@ -539,7 +575,7 @@ size_t pos_scratch_bytes(const RowGeom &g) { return (size_t)g.raw_words * 32 * 8
 
 int launch_build_meta_positions(const void *rows, int64_t n_rows, const RowGeom &g, double T,
                                 uint32_t *d_pmask, uint32_t *d_pbitval, void *d_scratch,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool per_block_position) {
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
   unsigned long long *counters = static_cast<unsigned long long *>(d_scratch);
@@ -554,8 +590,12 @@ int launch_build_meta_positions(const void *rows, int64_t n_rows, const RowGeom 
       static_cast<const uint32_t *>(rows), n_rows, g.raw_words, rows_per_chunk, n_chunks,
       counters);
   if (cudaGetLastError() != cudaSuccess) return IBP_ERR_CUDA;
-  pos_finalize_kernel<<<(unsigned)((g.row_elems + 127) / 128), 128, 0, s>>>(
-      counters, n_rows, (int)g.row_elems, g.w, T, d_pmask, d_pbitval);
+  if (per_block_position)
+    pos_block_finalize_kernel<<<1, 256, 0, s>>>(counters, n_rows, (int)g.row_elems, g.w, g.B, T,
+                                                d_pmask, d_pbitval);
+  else
+    pos_finalize_kernel<<<(unsigned)((g.row_elems + 127) / 128), 128, 0, s>>>(
+        counters, n_rows, (int)g.row_elems, g.w, T, d_pmask, d_pbitval);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 

@@ -21,14 +21,16 @@ pytestmark = pytest.mark.gpu
 FP32, FP16, BF16, W8 = ibp.FP32, ibp.FP16, ibp.BF16, ibp.W8
 
 
-def gpu_positions(words: np.ndarray, dtype_code: int, T: float, B: int, where: str = "device"):
+def gpu_positions(words: np.ndarray, dtype_code: int, T: float, B: int, where: str = "device",
+                  block_positions: bool = False):
     n, L = words.shape
     rows_t = to_torch(words, where)
     pm = torch.zeros(L, dtype=torch.int32, device="cuda")
     pb = torch.zeros(L, dtype=torch.int32, device="cuda")
     scratch = torch.empty(ibp.meta_positions_scratch_bytes(L, dtype_code) // 8, dtype=torch.int64,
                           device="cuda")
-    ibp.build_meta_positions(rows_t, T, B, pm, pb, scratch, dtype=dtype_code)
+    build = ibp.build_meta_block_positions if block_positions else ibp.build_meta_positions
+    build(rows_t, T, B, pm, pb, scratch, dtype=dtype_code)
     sb = ibp.slot_bytes(L, dtype_code)
     if where == "device":
         slots = torch.zeros((n, sb), dtype=torch.uint8, device="cuda")
@@ -41,11 +43,16 @@ def gpu_positions(words: np.ndarray, dtype_code: int, T: float, B: int, where: s
     return pm, pb, slots, bitmask, row_bits
 
 
-def check(words: np.ndarray, dtype_code: int, T: float, B: int, where: str = "device"):
+def check(words: np.ndarray, dtype_code: int, T: float, B: int, where: str = "device",
+          block_positions: bool = False):
     n, L = words.shape
-    o_pm, o_pb = oracle.build_meta_positions(words, T)
+    if block_positions:
+        o_pm, o_pb = oracle.build_meta_block_positions(words, T, B)
+    else:
+        o_pm, o_pb = oracle.build_meta_positions(words, T)
     o_slots, o_bm, o_rb = oracle.compress_positions(words, B, o_pm, o_pb)
-    pm, pb, slots, bitmask, row_bits = gpu_positions(words, dtype_code, T, B, where)
+    pm, pb, slots, bitmask, row_bits = gpu_positions(words, dtype_code, T, B, where,
+                                                     block_positions)
     assert np.array_equal(pm.cpu().numpy().view(np.uint32), o_pm)
     assert np.array_equal(pb.cpu().numpy().view(np.uint32), o_pb)
     gbm = bitmask.cpu().numpy().view(np.uint32)
@@ -147,3 +154,43 @@ def test_bad_index_and_row_limit():
         ibp.compress_positions(big, 64, pm, pb, torch.zeros((4, 16400), dtype=torch.uint8,
                                                             device="cuda"), bitmask, dtype=BF16)
     assert e.value.code == ibp.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype_code,np_dt,B,L", [
+    (FP32, np.uint32, 32, 96), (FP32, np.uint32, 64, 1060), (FP16, np.uint16, 32, 72),
+    (BF16, np.uint16, 64, 4104), (W8, np.uint8, 32, 48), (W8, np.uint8, 64, 4112),
+    (FP32, np.uint32, 32, 4), (BF16, np.uint16, 64, 8192)])
+@pytest.mark.parametrize("T", [0.75, 0.97])
+def test_block_positions_shapes_and_tails(dtype_code, np_dt, B, L, T):
+    """Block-position metadata: each position within a block has its own constant
+    high bits (the same in every block), rare exceptions, rows stored raw, shorter
+    last blocks (whose positions are counted only where they exist), 8-bit words."""
+    g = np.random.default_rng(L * 5 + int(T * 100))
+    w = 8 * np.dtype(np_dt).itemsize
+    n = 300
+    q_of = np.arange(L) % B
+    colconst = g.integers(0, 1 << w, size=B, dtype=np.uint64)[q_of]
+    colhi = np.array([((1 << w) - 1) ^ ((1 << int(k)) - 1) for k in g.integers(1, w, size=B)],
+                     dtype=np.uint64)[q_of]
+    base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+    flip = g.random(size=(n, L)) < 0.01
+    words = np.where(flip, base, (base & ~colhi) | (colconst & colhi)).astype(np_dt)
+    words[::11] = base[::11].astype(np_dt)
+    check(words, dtype_code, T, B, block_positions=True)
+
+
+@pytest.mark.parametrize("where", ["device", "host"])
+@pytest.mark.parametrize("name,dt,T,B", [("kv", BF16, 0.9, 64), ("dlrm", FP32, 0.95, 32),
+                                          ("sparse", FP32, 0.9, 32)])
+def test_block_positions_workloads(where, name, dt, T, B):
+    x = {"sparse": lambda: gen.gnn_sparse(1500), "dlrm": lambda: gen.dlrm_table(3, 20_000),
+         "kv": lambda: gen.llm_kv(0, 1, n_rows=600)}[name]()
+    check(words_of(x), dt, T, B, where, block_positions=True)
+
+
+def test_block_positions_equal_positions_for_one_block_rows():
+    """With one block per row the block positions are the element positions."""
+    words = words_of(gen.dlrm_table(1, 5000, row_elems=32))
+    a = gpu_positions(words, FP32, 0.9, 32, block_positions=True)
+    b = gpu_positions(words, FP32, 0.9, 32)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
