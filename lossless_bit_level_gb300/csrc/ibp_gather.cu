@@ -837,9 +837,9 @@ int launch_ws(GatherArgs a, const RowGeom &g, const DeviceInfo &dev, cudaStream_
 template <bool PACKED>
 int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const DeviceInfo &dev,
                 cudaStream_t s) {
-  // units of at most 1 KiB in device memory: team size 4 or 8, 4 CTAs per SM. The
-  // packed and sized instantiations spill 32 bytes at that register budget and are
-  // still 10% faster than at 3 CTAs per SM (measured on a packed store in HBM).
+  // units of at most 1 KiB in device memory: team size 4 or 8, 4 CTAs per SM (for
+  // the packed and sized instantiations too: measured 10% faster than 3 on a packed
+  // store in HBM).
   if (slots_in_device_memory) {
     constexpr int MINB = 4;
     if (tl == 4) return launch_tl<4, MINB, PACKED>(a, dev, s);
