@@ -551,6 +551,45 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
     return res
 
 
+def dedup_leg(store, wl, batches, out, steps, warmup, flush, barrier, out_bytes, link, hbm_peak,
+              dev):
+    """The same gathers through ibp_decompress_gather_dedup: each distinct row of a batch
+    read and decoded once, then copied to every position that names it. The link
+    bytes it needs are the stored bytes of the distinct rows."""
+    scratch = torch.empty(ibp.gather_dedup_scratch_bytes(wl["batch"], store.L, store.dtype,
+                                                         store.B),
+                          dtype=torch.uint8, device=dev)
+
+    class Dedup:
+        def gather(self, idx, o, st=None):
+            ibp.decompress_gather_dedup(store.slots, store.n, store.L, store.dtype, store.B,
+                                        store.bitmask, store.meta, idx, o, scratch, st)
+
+    per_step, clk = timed_gather(Dedup(), batches, out, max(50, steps // 4), warmup, flush,
+                                 barrier)
+    ts = float(np.mean(per_step))
+    stored = store.stored_per_row()
+    host_idx = [b.cpu().numpy() for b in batches]
+    distinct = float(np.mean([np.unique(b).size / b.size for b in host_idx]))
+    distinct_bytes = float(np.mean([stored[np.unique(b)].sum() for b in host_idx]))
+    # the output matches the plain gather's
+    check = torch.empty_like(out)
+    store.gather(batches[0], check)
+    Dedup().gather(batches[0], out)
+    torch.cuda.synchronize()
+    assert torch.equal(check, out)
+    del scratch, check
+    torch.cuda.empty_cache()
+    r = {"value": out_bytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3, "clocks": clk,
+         "distinct_fraction": distinct, "distinct_stored_bytes_per_launch": distinct_bytes,
+         "launches_per_call": 4}
+    if store.residency == "host":
+        r["link_frac_distinct_bytes"] = distinct_bytes / ts / 1e9 / link["h2d_memcpy_gbs"]
+    else:
+        r["hbm_frac"] = (wl["batch"] * 8 + distinct_bytes + 2 * out_bytes) / ts / 1e9 / hbm_peak
+    return r
+
+
 def dlrm_batched_leg(dev, flush, barrier, steps, warmup, hbm_peak, n_tables=26,
                      lookups=65_536, n_rows=1_000_000):
     """All 26 DLRM tables (1,000,000 x 128 FP32 each, per-table metadata T = 0.95,
@@ -1078,6 +1117,9 @@ def main():
                                       "reads_rows": 2}}
             del dstore, sel_d
             torch.cuda.empty_cache()
+        # before the mask-selection leg, which recompresses into the store's slots
+        extra["dedup"] = dedup_leg(store, wl, batches, out, steps, warmup, flush, barrier,
+                                   out_bytes, link, hbm_peak, dev)
         sstore, extra["mask_select"] = mask_select_leg(store, wl, batches, out, steps, warmup,
                                                        flush, barrier, reps, table_raw,
                                                        out_bytes, residency, link, hbm_peak)

@@ -267,6 +267,26 @@ int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
                                  const ibp_meta *d_meta, const int64_t *d_idx, int64_t n_idx,
                                  void *out, int32_t *d_status, ibp_stream_t s);
 
+/* De-duplicated decompress-gather ("Core algorithm", decompression; "System
+ * integration", rows in host memory moved over the host link). Same arguments and
+ * result as ibp_decompress_gather: out[i] (n_idx x row_elems words, device memory)
+ * is row d_idx[i]; an index outside [0, n_rows) records IBP_ERR_INDEX in *d_status
+ * and leaves its output row untouched. Each distinct row of d_idx is read from its
+ * slot and decoded once, into d_scratch, then copied to every position that names
+ * it: for skewed index lists a row crosses the host link once instead of once per
+ * request. d_scratch: device memory of scratch_bytes >= the size
+ * ibp_gather_dedup_scratch_bytes reports (about n_idx * raw row bytes plus 16 bytes
+ * per index and a hash table of 16 bytes per index), 16-byte aligned, overwritten;
+ * scratch_bytes too small: IBP_ERR_ARG. n_idx up to 2^24 - 1 and n_rows below 2^40,
+ * else IBP_ERR_UNSUPPORTED. Asynchronous on s (four launches); allocates nothing. */
+int ibp_gather_dedup_scratch_bytes(int64_t n_idx, int64_t row_elems, int dtype,
+                                   uint32_t block_elems, size_t *bytes);
+int ibp_decompress_gather_dedup(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                int64_t row_elems, int dtype, uint32_t block_elems,
+                                const uint32_t *d_row_bitmask, const ibp_meta *d_meta,
+                                const int64_t *d_idx, int64_t n_idx, void *out, void *d_scratch,
+                                size_t scratch_bytes, int32_t *d_status, ibp_stream_t s);
+
 /* ibp_decompress_gather given also the per-row bit counts ibp_compress wrote
  * (d_row_bits, n_rows words, device memory). A row's stored length is then known
  * from device memory before its slot is read, so exactly its used prefix (rounded

@@ -61,7 +61,8 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_decompress_range", "ibp_meta_positions_scratch_bytes", "ibp_build_meta_positions",
            "ibp_compress_positions", "ibp_decompress_gather_positions",
            "ibp_decompress_gather_sized", "ibp_decompress_gather_batched", "ibp_meta_count",
-           "ibp_meta_finalize", "ibp_build_meta_block_positions")
+           "ibp_meta_finalize", "ibp_build_meta_block_positions", "ibp_gather_dedup_scratch_bytes",
+           "ibp_decompress_gather_dedup")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -101,6 +102,9 @@ def load() -> ctypes.CDLL:
     lib.ibp_decompress_gather_positions.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp,
                                                     i64, vp, vp, vp]
     lib.ibp_meta_count.argtypes = [vp, i64, i64, i32, vp, vp]
+    lib.ibp_gather_dedup_scratch_bytes.argtypes = [i64, i64, i32, u32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.ibp_decompress_gather_dedup.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp,
+                                                ctypes.c_size_t, vp, vp]
     lib.ibp_build_meta_block_positions.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
     lib.ibp_meta_finalize.argtypes = [vp, i64, i32, dbl, u32, vp, vp]
     lib.ibp_decompress_gather_batched.argtypes = [vp, i32, i64, i32, u32, vp, vp]
@@ -258,6 +262,31 @@ def decompress_gather(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: i
                                         int(block_elems), _ptr(bitmask), _ptr(meta), _ptr(idx),
                                         idx.numel(), _ptr(out), _ptr(status), _stream(stream)),
            "ibp_decompress_gather")
+
+
+def gather_dedup_scratch_bytes(n_idx: int, row_elems: int, dtype: int, block_elems: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().ibp_gather_dedup_scratch_bytes(int(n_idx), int(row_elems), int(dtype),
+                                                 int(block_elems), ctypes.byref(out)),
+           "ibp_gather_dedup_scratch_bytes")
+    return out.value
+
+
+def decompress_gather_dedup(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
+                            block_elems: int, bitmask: torch.Tensor, meta: torch.Tensor,
+                            idx: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor,
+                            status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_decompress_gather_dedup: the result of decompress_gather, each distinct
+    row read and decoded once (``scratch``: gather_dedup_scratch_bytes bytes)."""
+    sb = slots.shape[1] * slots.element_size() if slots.dim() == 2 else slots.numel() * \
+        slots.element_size() // max(int(n_rows), 1)
+    if idx.dtype != torch.int64:
+        raise ValueError("idx must be int64")
+    _check(load().ibp_decompress_gather_dedup(
+        _ptr(slots), sb, int(n_rows), int(row_elems), int(dtype), int(block_elems), _ptr(bitmask),
+        _ptr(meta), _ptr(idx), idx.numel(), _ptr(out), _ptr(scratch),
+        scratch.numel() * scratch.element_size(), _ptr(status), _stream(stream)),
+        "ibp_decompress_gather_dedup")
 
 
 def pack_scratch_bytes(n_sel: int) -> int:

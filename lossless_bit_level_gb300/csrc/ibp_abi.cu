@@ -302,6 +302,41 @@ int ibp_decompress_gather(const void *slots, int64_t slot_bytes, int64_t n_rows,
                        reinterpret_cast<cudaStream_t>(s));
 }
 
+int ibp_gather_dedup_scratch_bytes(int64_t n_idx, int64_t row_elems, int dtype,
+                                   uint32_t block_elems, size_t *bytes) {
+  if (!bytes) return IBP_ERR_ARG;
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_idx < 0) return IBP_ERR_ARG;
+  if (n_idx > dedup_max_indices()) return IBP_ERR_UNSUPPORTED;
+  *bytes = dedup_scratch_bytes(n_idx, g);
+  return IBP_OK;
+}
+
+int ibp_decompress_gather_dedup(const void *slots, int64_t slot_bytes, int64_t n_rows,
+                                int64_t row_elems, int dtype, uint32_t block_elems,
+                                const uint32_t *d_row_bitmask, const ibp_meta *d_meta,
+                                const int64_t *d_idx, int64_t n_idx, void *out, void *d_scratch,
+                                size_t scratch_bytes, int32_t *d_status, ibp_stream_t s) {
+  RowGeom g;
+  if (int rc = make_geom(row_elems, dtype, block_elems, &g)) return rc;
+  if (n_rows < 0 || n_idx < 0 || slot_bytes < slot_bytes_of(g) || slot_bytes % 16 != 0)
+    return IBP_ERR_ARG;
+  if (n_idx > dedup_max_indices() || n_rows >= (int64_t(1) << 40)) return IBP_ERR_UNSUPPORTED;
+  if (n_idx == 0) return IBP_OK;
+  if (scratch_bytes < dedup_scratch_bytes(n_idx, g)) return IBP_ERR_ARG;
+  if (!pointer_ok(slots, Where::device_or_host, 16) ||
+      !pointer_ok(d_row_bitmask, Where::device_only, 4) ||
+      !pointer_ok(d_meta, Where::device_only, 16) || !pointer_ok(d_idx, Where::device_only, 8) ||
+      !pointer_ok(out, Where::device_only, 16) ||
+      !pointer_ok(d_scratch, Where::device_only, 16) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
+    return IBP_ERR_ARG;
+  return launch_gather_dedup(slots, slot_bytes, n_rows, g, (uint32_t)dtype, d_row_bitmask, d_meta,
+                             d_idx, n_idx, out, d_scratch, d_status, in_device_memory(slots),
+                             reinterpret_cast<cudaStream_t>(s));
+}
+
 int ibp_decompress_gather_sized(const void *slots, int64_t slot_bytes, int64_t n_rows,
                                 int64_t row_elems, int dtype, uint32_t block_elems,
                                 const uint32_t *d_row_bitmask, const uint32_t *d_row_bits,

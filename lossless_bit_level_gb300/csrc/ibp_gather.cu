@@ -70,6 +70,9 @@ struct GatherArgs {
   // 128 for host memory, where a partly read 128-byte line costs the link about as
   // much as a whole one; 16 for HBM.
   uint32_t span_align;
+  // a negative index is a unit with nothing to do, not an error (internal lists whose
+  // tail is unused, e.g. the distinct rows of a de-duplicated gather)
+  uint32_t skip_negative;
 };
 
 // The plan of one unit (identical in every lane of its team).
@@ -161,7 +164,7 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   const int nblk = min(a.seg_blocks, a.nb - b0);
   un.out_word = i * (int64_t)a.raw_words + (int64_t)b0 * a.lwb;
   if (r < 0 || r >= a.n_rows) {
-    if (leader) report(a.status, IBP_ERR_INDEX);
+    if (leader && !(a.skip_negative && r < 0)) report(a.status, IBP_ERR_INDEX);
     return un;
   }
   const bool last_seg = b0 + nblk == a.nb;  // holds the row's last block
@@ -859,7 +862,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
-                  bool slots_in_device_memory, cudaStream_t s, const uint32_t *d_row_bits) {
+                  bool slots_in_device_memory, cudaStream_t s, const uint32_t *d_row_bits,
+                  bool skip_negative) {
   if (n_idx == 0) return IBP_OK;
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
@@ -871,6 +875,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.offsets = d_offsets;
   a.row_bits = d_offsets ? nullptr : d_row_bits;
   a.span_align = slots_in_device_memory ? 16u : 128u;
+  a.skip_negative = skip_negative ? 1u : 0u;
   a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
   a.n_rows = n_rows;
   a.bitmask = d_bitmask;
@@ -920,6 +925,7 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
   GatherArgs &a = b.common;
   a = GatherArgs{};
   a.span_align = 16u;
+  a.skip_negative = 0u;
   a.status = d_status;
   a.dtype = dtype;
   a.block_elems = (uint32_t)g.B;

@@ -68,7 +68,15 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
                   bool slots_in_device_memory, cudaStream_t s,
-                  const uint32_t *d_row_bits = nullptr);
+                  const uint32_t *d_row_bits = nullptr, bool skip_negative = false);
+// De-duplicated slotted gather: every distinct row of d_idx is read and decoded
+// once (into d_scratch), then copied to each output position that asks for it.
+size_t dedup_scratch_bytes(int64_t n_idx, const RowGeom &g);
+int64_t dedup_max_indices();  // index positions share a 64-bit word with the row
+int launch_gather_dedup(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
+                        uint32_t dtype, const uint32_t *d_bitmask, const ibp_meta *d_meta,
+                        const int64_t *d_idx, int64_t n_idx, void *out, void *d_scratch,
+                        int32_t *d_status, bool slots_in_device_memory, cudaStream_t s);
 // Several slotted gathers with one row geometry in one launch per 64 jobs; in_device[j]:
 // job j's slots are in device memory.
 int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom &g,

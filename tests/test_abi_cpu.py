@@ -123,6 +123,19 @@ def test_argument_errors_before_cuda(lib):
     assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 1.2, 32, vp(16), None) == ibp.ERR_ARG
     assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 0.9, 48, vp(16), None) == \
         ibp.ERR_UNSUPPORTED
+    # de-duplicated gather: scratch size query (table, index arrays, one staged row per
+    # index), limits, and an empty list as a no-op
+    sz = ctypes.c_size_t(0)
+    assert lib.ibp_gather_dedup_scratch_bytes(100_000, 128, ibp.FP32, 32, ctypes.byref(sz)) == ibp.OK
+    assert sz.value >= 100_000 * (512 + 16) + 2 * 100_000 * 8
+    assert lib.ibp_gather_dedup_scratch_bytes(1 << 24, 128, ibp.FP32, 32, ctypes.byref(sz)) == \
+        ibp.ERR_UNSUPPORTED
+    assert lib.ibp_gather_dedup_scratch_bytes(10, 128, ibp.FP32, 32, None) == ibp.ERR_ARG
+    assert lib.ibp_decompress_gather_dedup(vp(16), 512, 10, 128, ibp.FP32, 32, vp(16), vp(16),
+                                           vp(16), 0, vp(16), vp(16), 0, None, None) == ibp.OK
+    assert lib.ibp_decompress_gather_dedup(vp(16), 512, 1 << 40, 128, ibp.FP32, 32, vp(16),
+                                           vp(16), vp(16), 5, vp(16), vp(16), 1 << 20, None,
+                                           None) == ibp.ERR_UNSUPPORTED
     # batched gathers: empty batch is a no-op; a null job array with jobs is refused
     assert lib.ibp_decompress_gather_batched(None, 0, 128, ibp.FP32, 32, None, None) == ibp.OK
     assert lib.ibp_decompress_gather_batched(None, 3, 128, ibp.FP32, 32, None, None) == ibp.ERR_ARG
