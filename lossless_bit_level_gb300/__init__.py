@@ -9,6 +9,20 @@ raises if the shared library has not been built (``build_lib.build()``).
 
 Method: "Reducing the GPU Memory Bottleneck with Lossless Compression for ML --
 Extended", technical summary, "Core algorithm" and "System integration".
+
+The path, in order:
+  build_meta (or meta_count + meta_finalize across holders; build_meta_select for
+  the saving-aware mask)       -> 16-byte metadata in device memory
+  compress                     -> fixed-size slots + bitmask (+ row sizes)
+  decompress_gather            -> the rows an index list names, rebuilt bit for bit
+Gather variants: decompress_gather_dedup (each distinct row read once),
+decompress_gather_sized (only each row's used bytes), decompress_gather_batched
+(several tables in one launch), decompress_range (rows in order). Next to them: the
+packed store (pack_offsets, pack, decompress_gather_packed) and per-position or
+block-position metadata (build_meta_positions, build_meta_block_positions,
+compress_positions, decompress_gather_positions). ``offload.py`` streams compressed
+tensors through device buffers; ``sharded.py`` builds the metadata of a table spread
+over several processes.
 """
 from __future__ import annotations
 
