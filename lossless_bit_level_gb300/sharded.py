@@ -49,8 +49,11 @@ def sharded_meta(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Ten
         meta_count(rows, counters, dtype=code, stream=stream)
     else:
         counters.zero_()
-    s = stream if stream is not None else torch.cuda.current_stream(counters.device)
-    with torch.cuda.stream(s):
+    if counters.is_cuda:  # the exchange is ordered after the count on the same stream
+        s = stream if stream is not None else torch.cuda.current_stream(counters.device)
+        with torch.cuda.stream(s):
+            total = allreduce_counts(counters, n * L, group)
+    else:
         total = allreduce_counts(counters, n * L, group)
     if total <= 0:
         raise ValueError("no rows on any rank")

@@ -100,3 +100,56 @@ def test_allreduce_counts_rejects_bad_buffer():
     from lossless_bit_level_gb300.sharded import allreduce_counts
     with pytest.raises(ValueError):
         allreduce_counts(torch.zeros(32, dtype=torch.int32), 1)
+
+
+def _sharded_worker(rank, world, port, q):
+    """sharded_meta's orchestration over gloo with the two device calls replaced by
+    host stand-ins: the local count, the exchange, the finalize with the totals."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import numpy as np
+
+    import ibp_inputs as gen
+    import lossless_bit_level_gb300.sharded as sh
+    seen = {}
+
+    def fake_count(rows, counters, dtype=None, stream=None):
+        w32 = rows.numpy().view(np.uint32).ravel()
+        counters.copy_(torch.tensor([int(((w32 >> np.uint32(j)) & np.uint32(1)).sum())
+                                     for j in range(32)], dtype=torch.int64))
+
+    def fake_finalize(counters, n_elems, dtype, T, block_elems, meta, stream=None):
+        seen.update(counters=counters.tolist(), n_elems=n_elems, T=T, B=block_elems)
+
+    sh.meta_count, sh.meta_finalize = fake_count, fake_finalize
+    words = gen.gnn_dense(600).view(np.int32)
+    bounds = [0, 600, 600]  # rank 1 holds no rows
+    mine = torch.from_numpy(np.ascontiguousarray(words[bounds[rank]:bounds[rank + 1]]))
+    counters = torch.full((32,), -1, dtype=torch.int64)
+    total = sh.sharded_meta(mine, 0.9, 32, torch.zeros(4, dtype=torch.int32), counters,
+                            dtype=0)
+    q.put((rank, total, seen))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_sharded_meta_two_ranks():
+    import numpy as np
+
+    import ibp_inputs as gen
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_sharded_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    w32 = gen.gnn_dense(600).view(np.uint32).ravel()
+    want = [int(((w32 >> np.uint32(j)) & np.uint32(1)).sum()) for j in range(32)]
+    for rank, total, seen in res:
+        assert total == w32.size == seen["n_elems"]
+        assert seen["counters"] == want
+        assert (seen["T"], seen["B"]) == (0.9, 32)
