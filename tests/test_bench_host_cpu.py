@@ -57,3 +57,15 @@ def test_workload_generators(name):
     assert idx.dtype == np.int64 and idx.size == 200
     assert idx.min() >= 0 and idx.max() < 64
     assert wl["T"] in (0.9, 0.95) and wl["B"] in (32, 64) and wl["residency"] in ("host", "device")
+
+
+def test_oracle_baselines_single_and_all_cores():
+    """The cpu_baseline legs: the oracle single-threaded and split over every core,
+    on a small prefix table and short budgets."""
+    wl = bench.workload_table("tiny")
+    one, every = bench.oracle_sample(wl, seconds_budget=0.2, sample_rows=2048,
+                                     all_cores_budget=0.2)
+    assert one["cores"] == 1 and every["cores"] == (os.cpu_count() or 1)
+    for d in (one, every):
+        assert d["kind"] == "oracle" and d["unit"] == "GB/s" and d["value"] > 0
+        assert d["batches"] >= 1
