@@ -298,6 +298,41 @@ def check_positions_meta_and_sizes(o):
         assert np.array_equal(s1, s2) and np.array_equal(b1, b2) and np.array_equal(r1, r2)
 
 
+def check_slot_bytes(o):
+    """A slot is the raw row rounded up to 16 bytes."""
+    for L, w, want in ((3, 32, 16), (4, 32, 16), (5, 32, 32), (8, 16, 16), (9, 16, 32),
+                       (24, 8, 32), (16, 8, 16), (128, 32, 512), (11008, 16, 22016)):
+        assert o.slot_bytes(L, w) == want, (L, w)
+
+
+def check_code_cut_to_width(o):
+    """The code of w-bit elements uses the low w bits of mask and bitval only: bits
+    above w change nothing."""
+    g = np.random.default_rng(31)
+    x = g.integers(0, 1 << 16, size=(20, 64), dtype=np.uint64).astype(np.uint16)
+    x[:10] = (x[:10] & np.uint16(0x00FF)) | np.uint16(0x3C00)
+    a = o.compress(x, 32, 0xFF00, 0x3C00)
+    b = o.compress(x, 32, 0xABCDFF00, 0x12343C00)
+    assert all(np.array_equal(p, q) for p, q in zip(a, b))
+    assert int(a[1][0]) != 0  # some rows compressed: the code is used
+
+
+def check_decode_rejects_uncompressible_stream(o):
+    """A slot flagged compressed whose participation bits describe a stream of at
+    least the raw row's size is corrupt (such a row is always stored raw); one word
+    less decodes. FP32, 32 elements, B = 16, mask of two bits (m = 30): header bits
+    (raw, match) give 2 + 16*32 + 16*30 = 994 bits = 32 words = the 128 raw bytes;
+    (match, match) give 2 + 2*16*30 = 962 bits = 31 words."""
+    mask, bitval = 0xC0000000, 0x40000000
+    for header, want in ((0b10, -6), (0b11, 0)):
+        slots = np.zeros((1, 128), dtype=np.uint8)
+        slots[0, 0] = header
+        bm = np.array([1], dtype=np.uint32)
+        out, rc = o.decompress_gather(slots, 1, 32, np.uint32, 16, bm, mask, bitval,
+                                      np.array([0]))
+        assert rc == want, (header, rc)
+
+
 def check_size_formula(o):
     g = np.random.default_rng(777)
     cases = [(np.uint32, 32, 32, 128), (np.uint32, 32, 64, 256), (np.uint16, 16, 64, 256),
@@ -619,4 +654,6 @@ ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_select_threshold_sweep, check_pack_hand_example, check_pack_round_trip,
               check_hand_example_u8_tail, check_tail_blocks_and_bytes,
               check_positions_hand_example, check_positions_meta_and_sizes,
-              check_block_positions_hand_example, check_block_positions_reductions]
+              check_block_positions_hand_example, check_block_positions_reductions,
+              check_slot_bytes, check_code_cut_to_width,
+              check_decode_rejects_uncompressible_stream]

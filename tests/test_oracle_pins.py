@@ -123,6 +123,19 @@ PLANTED = [
     ("block positions count a shorter last block as full",
      "    int rc = ibpo_build_meta(sample.data(), (int64_t)(sample.size() / nbytes), w_bits, T, &mask,",
      "    while ((int64_t)(sample.size() / nbytes) < n_rows * ((row_elems + block_elems - 1) / block_elems))\n      for (int k = 0; k < nbytes; ++k) sample.push_back(0);\n    int rc = ibpo_build_meta(sample.data(), (int64_t)(sample.size() / nbytes), w_bits, T, &mask,"),
+    ("decoder accepts a stream of the raw size", "if (4 * ((bits + 31) / 32) >= raw_bytes ||",
+     "if (4 * ((bits + 31) / 32) > raw_bytes ||"),
+    ("code not cut to the element width",
+     "uint32_t mk = (shared ? pmask[0] : pmask[e]) & width_mask(w_bits);",
+     "uint32_t mk = (shared ? pmask[0] : pmask[e]);"),
+    ("slot rounded to 8 bytes", "return (raw + 15) / 16 * 16;", "return (raw + 7) / 8 * 8;"),
+    ("big-endian element load", "v |= (uint32_t)base[e * nbytes + k] << (8 * k);",
+     "v |= (uint32_t)base[e * nbytes + k] << (8 * (nbytes - 1 - k));"),
+    ("fields read MSB-first", "    v |= (uint32_t)get_bit(stream, *pos) << i;",
+     "    v |= (uint32_t)get_bit(stream, *pos) << (nbits - 1 - i);"),
+    ("block match tests the block's first position only",
+     "    if ((load_elem(row, e, w_bits) & c.mask[e]) != c.bitval[e]) match = 0;",
+     "    if ((load_elem(row, e, w_bits) & c.mask[b * block_elems]) != c.bitval[b * block_elems]) match = 0;"),
     ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
      "*bitval_out = bitval0;"),
 ]
