@@ -333,6 +333,29 @@ def check_decode_rejects_uncompressible_stream(o):
         assert rc == want, (header, rc)
 
 
+def check_bad_index_semantics(o):
+    """A gather rebuilds every valid index even after a bad one; each bad index
+    (negative or past the table) leaves its output row untouched and makes the call
+    report a bad index. The same holds for the packed store's gather."""
+    rows = np.arange(8 * 32, dtype=np.uint32).reshape(8, 32) | np.uint32(0x3F000000)
+    mask, bitval = o.build_meta(rows, 0.9)
+    slots, bitmask, row_bits = o.compress(rows, 32, mask, bitval)
+    idx = np.array([3, -1, 0, 8, 7, 1 << 40, 3], dtype=np.int64)
+    good = [0, 2, 4, 6]
+    sentinel = np.full((idx.size, 32), 0xDEADBEEF, dtype=np.uint32)
+    out, rc = o.decompress_gather(slots, 8, 32, np.uint32, 32, bitmask, mask, bitval, idx,
+                                  out=sentinel.copy())
+    assert rc == -5, rc
+    assert np.array_equal(out[good], rows[idx[good]])
+    assert np.all(out[[1, 3, 5]] == 0xDEADBEEF)
+    off, packed, pbm, _ = o.pack(slots, 32, np.uint32, bitmask, row_bits)
+    out, rc = o.decompress_gather_packed(packed, off, 32, np.uint32, 32, pbm, mask, bitval, idx,
+                                         out=sentinel.copy())
+    assert rc == -5, rc
+    assert np.array_equal(out[good], rows[idx[good]])
+    assert np.all(out[[1, 3, 5]] == 0xDEADBEEF)
+
+
 def check_size_formula(o):
     g = np.random.default_rng(777)
     cases = [(np.uint32, 32, 32, 128), (np.uint32, 32, 64, 256), (np.uint16, 16, 64, 256),
@@ -656,4 +679,4 @@ ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_positions_hand_example, check_positions_meta_and_sizes,
               check_block_positions_hand_example, check_block_positions_reductions,
               check_slot_bytes, check_code_cut_to_width,
-              check_decode_rejects_uncompressible_stream]
+              check_decode_rejects_uncompressible_stream, check_bad_index_semantics]

@@ -136,6 +136,12 @@ PLANTED = [
     ("block match tests the block's first position only",
      "    if ((load_elem(row, e, w_bits) & c.mask[e]) != c.bitval[e]) match = 0;",
      "    if ((load_elem(row, e, w_bits) & c.mask[b * block_elems]) != c.bitval[b * block_elems]) match = 0;"),
+    ("gather stops at the first bad index",
+     "      if (status == IBPO_OK) status = IBPO_BAD_INDEX;\n      continue;\n    }\n    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);\n    int rc = decode_row(",
+     "      if (status == IBPO_OK) status = IBPO_BAD_INDEX;\n      break;\n    }\n    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);\n    int rc = decode_row("),
+    ("gather reports a bad index as success",
+     "    if (r < 0 || r >= n_rows) {\n      if (status == IBPO_OK) status = IBPO_BAD_INDEX;\n      continue;\n    }\n    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);\n    int rc = decode_row(",
+     "    if (r < 0 || r >= n_rows) {\n      continue;\n    }\n    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);\n    int rc = decode_row("),
     ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
      "*bitval_out = bitval0;"),
 ]
