@@ -356,6 +356,28 @@ def check_bad_index_semantics(o):
     assert np.all(out[[1, 3, 5]] == 0xDEADBEEF)
 
 
+def check_stream_padding_is_zero(o):
+    """The stored bytes of a compressed row are its stream and zero bits up to the
+    end of the last 32-bit word, whatever the slot held before: compressing into a
+    buffer full of ones gives the same used prefix as into a zeroed one."""
+    g = np.random.default_rng(12)
+    x = (g.integers(0, 1 << 20, size=(40, 96), dtype=np.uint64).astype(np.uint32)
+         | np.uint32(0x3F800000))
+    mask, bitval = o.build_meta(x, 0.9)
+    clean, bm, rb = o.compress(x, 32, mask, bitval)
+    dirty = np.full_like(clean, 0xFF)
+    bm2 = np.zeros_like(bm)
+    rb2 = np.zeros_like(rb)
+    rc = o.lib.ibpo_compress(x.ctypes.data, 40, 96, 32, 32, int(mask), int(bitval),
+                             dirty.ctypes.data, clean.shape[1], bm2.ctypes.data, rb2.ctypes.data)
+    assert rc == 0 and np.array_equal(bm, bm2) and np.array_equal(rb, rb2)
+    comp = [(bm[r // 32] >> (r % 32)) & 1 for r in range(40)]
+    assert any(comp)
+    for r in range(40):
+        used = 4 * ((int(rb[r]) + 31) // 32) if comp[r] else 96 * 4
+        assert np.array_equal(dirty[r, :used], clean[r, :used]), r
+
+
 def check_size_formula(o):
     g = np.random.default_rng(777)
     cases = [(np.uint32, 32, 32, 128), (np.uint32, 32, 64, 256), (np.uint16, 16, 64, 256),
@@ -679,4 +701,5 @@ ALL_CHECKS = [check_hand_example, check_hand_decode, check_meta_exhaustive,
               check_positions_hand_example, check_positions_meta_and_sizes,
               check_block_positions_hand_example, check_block_positions_reductions,
               check_slot_bytes, check_code_cut_to_width,
-              check_decode_rejects_uncompressible_stream, check_bad_index_semantics]
+              check_decode_rejects_uncompressible_stream, check_bad_index_semantics,
+              check_stream_padding_is_zero]

@@ -142,6 +142,9 @@ PLANTED = [
     ("gather reports a bad index as success",
      "    if (r < 0 || r >= n_rows) {\n      if (status == IBPO_OK) status = IBPO_BAD_INDEX;\n      continue;\n    }\n    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);\n    int rc = decode_row(",
      "    if (r < 0 || r >= n_rows) {\n      continue;\n    }\n    int compressed = (int)((bitmask[r / 32] >> (r % 32)) & 1u);\n    int rc = decode_row("),
+    ("compressed slot not cleared to the end of its last word",
+     "    for (int64_t k = 0; k < 4 * stored_words; ++k) slot[k] = 0;",
+     "    for (int64_t k = 0; k < 4 * stored_words - 1; ++k) slot[k] = 0;"),
     ("selection keeps the threshold bitval", "*bitval_out = bitval0 & cands[best];",
      "*bitval_out = bitval0;"),
 ]
