@@ -347,8 +347,7 @@ class Store:
                               self.meta, idx, out, status)
 
     def stats(self):
-        ibp.query(self.bitmask, self.row_bits, self.n, self.L, self.dtype, self.stats_t)
-        return ibp.read_stats(self.stats_t)
+        return ibp.query(self.bitmask, self.row_bits, self.n, self.L, self.dtype)
 
     def stored_per_row(self):
         bits = self.row_bits.cpu().numpy().view(np.uint32).astype(np.int64)

@@ -81,7 +81,11 @@ enum {
 
 /* Metadata: the fixed-size mask/bitval pair of the preprocessing stage.
  * Plain data (16 bytes); the caller may copy or serialise it. mask has a 1 at
- * every invariant bit position; bitval holds their values and is 0 elsewhere. */
+ * every invariant bit position; bitval holds their values and is 0 elsewhere.
+ * dtype == IBP_META_INVALID marks metadata that ibp_meta_finalize refused to build
+ * (every call given it reports IBP_ERR_META). */
+#define IBP_META_INVALID 0xFFFFFFFFu
+
 typedef struct {
   uint32_t mask;
   uint32_t bitval;
@@ -89,7 +93,7 @@ typedef struct {
   uint32_t block_elems; /* B */
 } ibp_meta;
 
-/* Store statistics written by ibp_query. */
+/* Store statistics written by ibp_query / ibp_query_async. */
 typedef struct {
   int64_t n_rows;
   int64_t n_compressed; /* rows whose bitmask bit is 1 */
@@ -101,10 +105,17 @@ typedef struct {
 /* Human-readable name of a return/status code (static string). */
 const char *ibp_status_string(int code);
 
-/* Bytes of one slot: row_elems * w/8 rounded up to 16. */
+/* Bytes of one slot ("System integration": every tensor gets one fixed-size buffer
+ * whose leading, compressed part is all that is read; the buffer must hold the row
+ * raw, since a row that does not shrink is stored as it is): row_elems * w/8
+ * rounded up to 16 (the kernels move 16-byte vectors). row_elems <= 0: IBP_ERR_ARG;
+ * unknown dtype: IBP_ERR_DTYPE. Pure host arithmetic, no CUDA call. */
 int ibp_slot_bytes(int64_t row_elems, int dtype, int64_t *slot_bytes);
 
-/* Bytes of device scratch ibp_build_meta needs (the per-bit-position counters). */
+/* Bytes of device scratch ibp_build_meta needs ("Core algorithm", preprocessing:
+ * the metadata follows from how often each bit position of the element word holds
+ * a 1 in the sample, so the scratch holds one 64-bit count per bit position of a
+ * 32-bit word: 256 bytes, whatever the input size). Host arithmetic only. */
 int ibp_meta_scratch_bytes(size_t *bytes);
 
 /* Preprocessing ("Core algorithm", preprocessing).
@@ -130,12 +141,18 @@ int ibp_build_meta(const void *rows, int64_t n_rows, int64_t row_elems, int dtyp
  * ibp_meta_finalize: applies the threshold rule of ibp_build_meta to the summed
  * counters, n_elems (> 0) being the total number of elements counted, and writes
  * *d_meta. T outside [0, 1] or n_elems <= 0: IBP_ERR_ARG; block_elems not 32 or 64:
- * IBP_ERR_UNSUPPORTED. With one holder the pair equals ibp_build_meta. Both calls are
- * asynchronous on s and allocate nothing. */
+ * IBP_ERR_UNSUPPORTED. A counter larger than n_elems (the counters and the element
+ * count do not describe the same rows, e.g. one holder's count passed with summed
+ * counters) is detected on the device: *d_meta is then written with mask = bitval =
+ * 0 and dtype = IBP_META_INVALID, so that every later call given it reports
+ * IBP_ERR_META, and IBP_ERR_META is recorded in *d_status (nullable, device memory,
+ * compare-and-swap from 0). With one holder the pair equals ibp_build_meta. Both
+ * calls are asynchronous on s and allocate nothing. */
 int ibp_meta_count(const void *rows, int64_t n_rows, int64_t row_elems, int dtype,
                    uint64_t *d_counters, ibp_stream_t s);
 int ibp_meta_finalize(const uint64_t *d_counters, int64_t n_elems, int dtype, double T,
-                      uint32_t block_elems, ibp_meta *d_meta, ibp_stream_t s);
+                      uint32_t block_elems, ibp_meta *d_meta, int32_t *d_status,
+                      ibp_stream_t s);
 
 /* ibp_build_meta for callers that cannot allocate device memory (the paper has no
  * counterpart; this is a library convenience). Same arguments, checks and result
@@ -148,7 +165,10 @@ int ibp_meta_finalize(const uint64_t *d_counters, int64_t n_elems, int dtype, do
  * - Allocates nothing: no cudaMalloc/cudaFree and no allocating library call.
  * - The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
- *   capture.
+ *   capture. The address is kept together with the identity of the CUDA context it
+ *   was looked up in; after a device reset (a new primary context, where the
+ *   library's device code is loaded again) the next call looks it up again, so
+ *   make that call, too, before any capture.
  * - The counters are cleared on stream s at the start of every call, so results
  *   never depend on an earlier call; but every call shares the one array, so calls
  *   whose kernels overlap on the GPU (e.g. on unordered streams) race and give
@@ -381,10 +401,28 @@ int ibp_decompress_gather_positions(const void *slots, int64_t slot_bytes, int64
                                     int64_t n_idx, void *out, int32_t *d_status,
                                     ibp_stream_t s);
 
-/* Statistics of a store: reduces the bitmask and the per-row bit counts written
- * by ibp_compress into *d_stats (device memory), asynchronously on s. */
+/* Statistics of a store ("System integration": a fixed-size buffer per tensor of
+ * which only the compressed part is used, and a GPU-resident bitmask of the
+ * compressed tensors; the statistics say how much of the buffers is used).
+ * Reduces the bitmask and the per-row bit counts written by ibp_compress
+ * (d_row_bitmask: ceil(n_rows/32) words, d_row_bits: n_rows words, device memory;
+ * both may be null when n_rows == 0) into
+ *   n_rows, n_compressed (bitmask bits set), raw_bytes (n_rows * row bytes),
+ *   stored_bytes (sum of 4*ceil(bits/32) over compressed rows plus the raw row
+ *   bytes of the others), total_bits (sum of the per-row bit counts).
+ * ibp_query writes them to *h_out (host memory of any kind) and synchronises s
+ * before it returns, so it cannot be captured in a CUDA graph. Its kernel reduces
+ * into a 40-byte array built into the library (the library allocates nothing);
+ * calls in one process take a lock around the launch and the wait, so two calls
+ * never share the array. Errors: null h_out, n_rows < 0, row_elems <= 0 or a
+ * non-device bitmask/bit-count pointer: IBP_ERR_ARG; unknown dtype: IBP_ERR_DTYPE;
+ * a failed launch, copy or synchronisation: IBP_ERR_CUDA (*h_out then unchanged).
+ * ibp_query_async: the same reduction into *d_stats (device memory, 8-byte
+ * aligned, overwritten), asynchronous on s, capturable; same argument errors. */
 int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
-              int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s);
+              int64_t row_elems, int dtype, ibp_stats *h_out, ibp_stream_t s);
+int ibp_query_async(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                    int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s);
 
 /* Measurement helper, not part of the codec: streams `bytes` (a multiple of 16)
  * from src (device or registered host memory) with 16-byte loads across the whole

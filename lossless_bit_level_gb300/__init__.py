@@ -76,7 +76,7 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_compress_positions", "ibp_decompress_gather_positions",
            "ibp_decompress_gather_sized", "ibp_decompress_gather_batched", "ibp_meta_count",
            "ibp_meta_finalize", "ibp_build_meta_block_positions", "ibp_gather_dedup_scratch_bytes",
-           "ibp_decompress_gather_dedup")
+           "ibp_decompress_gather_dedup", "ibp_query_async")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -105,6 +105,7 @@ def load() -> ctypes.CDLL:
     lib.ibp_compress.argtypes = [vp, i64, i64, i32, u32, vp, vp, i64, vp, vp, vp, vp]
     lib.ibp_decompress_gather.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp, vp]
     lib.ibp_query.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.ibp_query_async.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.ibp_probe_read.argtypes = [vp, i64, vp, vp]
     lib.ibp_build_meta_noalloc.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp]
     lib.ibp_meta_select_scratch_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
@@ -120,7 +121,7 @@ def load() -> ctypes.CDLL:
     lib.ibp_decompress_gather_dedup.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, i64, vp, vp,
                                                 ctypes.c_size_t, vp, vp]
     lib.ibp_build_meta_block_positions.argtypes = [vp, i64, i64, i32, dbl, u32, vp, vp, vp, vp]
-    lib.ibp_meta_finalize.argtypes = [vp, i64, i32, dbl, u32, vp, vp]
+    lib.ibp_meta_finalize.argtypes = [vp, i64, i32, dbl, u32, vp, vp, vp]
     lib.ibp_decompress_gather_batched.argtypes = [vp, i32, i64, i32, u32, vp, vp]
     lib.ibp_decompress_gather_sized.argtypes = [vp, i64, i64, i64, i32, u32, vp, vp, vp, vp, i64,
                                                 vp, vp, vp]
@@ -203,10 +204,12 @@ def meta_count(rows: torch.Tensor, counters: torch.Tensor, dtype: int | None = N
 
 
 def meta_finalize(counters: torch.Tensor, n_elems: int, dtype: int, T: float, block_elems: int,
-                  meta: torch.Tensor, stream=None) -> None:
-    """ibp_meta_finalize: the threshold rule applied to (summed) ``counters``."""
+                  meta: torch.Tensor, status: torch.Tensor | None = None, stream=None) -> None:
+    """ibp_meta_finalize: the threshold rule applied to (summed) ``counters``; counters
+    larger than ``n_elems`` give invalid metadata and ERR_META in ``status``."""
     _check(load().ibp_meta_finalize(_ptr(counters), int(n_elems), int(dtype), float(T),
-                                    int(block_elems), _ptr(meta), _stream(stream)),
+                                    int(block_elems), _ptr(meta), _ptr(status),
+                                    _stream(stream)),
            "ibp_meta_finalize")
 
 
@@ -459,10 +462,20 @@ def decompress_range(slots: torch.Tensor, n_rows: int, row_elems: int, dtype: in
 
 
 def query(bitmask: torch.Tensor, row_bits: torch.Tensor, n_rows: int, row_elems: int, dtype: int,
-          stats: torch.Tensor, stream=None) -> None:
-    """ibp_query: store statistics into ``stats`` (40 device bytes, see Stats)."""
+          stream=None) -> Stats:
+    """ibp_query: store statistics, returned in host memory (synchronises the stream)."""
+    out = Stats()
     _check(load().ibp_query(_ptr(bitmask), _ptr(row_bits), int(n_rows), int(row_elems),
-                            int(dtype), _ptr(stats), _stream(stream)), "ibp_query")
+                            int(dtype), ctypes.byref(out), _stream(stream)), "ibp_query")
+    return out
+
+
+def query_async(bitmask: torch.Tensor, row_bits: torch.Tensor, n_rows: int, row_elems: int,
+                dtype: int, stats: torch.Tensor, stream=None) -> None:
+    """ibp_query_async: store statistics into ``stats`` (40 device bytes, see Stats),
+    asynchronously."""
+    _check(load().ibp_query_async(_ptr(bitmask), _ptr(row_bits), int(n_rows), int(row_elems),
+                                  int(dtype), _ptr(stats), _stream(stream)), "ibp_query_async")
 
 
 def read_stats(stats: torch.Tensor) -> Stats:

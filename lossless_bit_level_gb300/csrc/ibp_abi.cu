@@ -159,6 +159,35 @@ int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t 
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
+// ibp_query's result lives in this array (one per device that loads the library):
+// the synchronous form takes no caller device memory and the library allocates
+// none. A process-wide lock is held from the clear to the end of the wait, so two
+// calls never use the array at the same time. Its address is looked up on every
+// call (a table lookup in the runtime), which stays right across device resets.
+static __device__ __align__(16) ibp_stats g_query_result;
+static std::mutex g_query_mutex;
+
+int launch_query_sync(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                      int64_t raw_bytes, ibp_stats *h_out, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_query_mutex);
+  void *d = nullptr;
+  if (cudaGetSymbolAddress(&d, g_query_result) != cudaSuccess || !d) {
+    cudaGetLastError();
+    return IBP_ERR_CUDA;
+  }
+  ibp_stats *d_stats = static_cast<ibp_stats *>(d);
+  if (int rc = launch_query(d_bitmask, d_row_bits, n_rows, raw_bytes, d_stats, s)) return rc;
+  ibp_stats host;
+  if (cudaMemcpyAsync(&host, d_stats, sizeof(ibp_stats), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return IBP_ERR_CUDA;
+  }
+  *h_out = host;
+  return IBP_OK;
+}
+
 int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s) {
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
@@ -233,14 +262,18 @@ int ibp_meta_count(const void *rows, int64_t n_rows, int64_t row_elems, int dtyp
 }
 
 int ibp_meta_finalize(const uint64_t *d_counters, int64_t n_elems, int dtype, double T,
-                      uint32_t block_elems, ibp_meta *d_meta, ibp_stream_t s) {
+                      uint32_t block_elems, ibp_meta *d_meta, int32_t *d_status,
+                      ibp_stream_t s) {
   if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
   if (n_elems <= 0 || !(T >= 0.0 && T <= 1.0)) return IBP_ERR_ARG;
   if (block_elems != 32 && block_elems != 64) return IBP_ERR_UNSUPPORTED;
-  if (!pointer_ok(d_counters, Where::device_only, 8) || !pointer_ok(d_meta, Where::device_only, 16))
+  if (!pointer_ok(d_counters, Where::device_only, 8) ||
+      !pointer_ok(d_meta, Where::device_only, 16) ||
+      (d_status && !pointer_ok(d_status, Where::device_only, 4)))
     return IBP_ERR_ARG;
   return launch_meta_finalize(reinterpret_cast<const unsigned long long *>(d_counters), n_elems,
-                              dtype, T, block_elems, d_meta, reinterpret_cast<cudaStream_t>(s));
+                              dtype, T, block_elems, d_meta, d_status,
+                              reinterpret_cast<cudaStream_t>(s));
 }
 
 int ibp_meta_select_scratch_bytes(size_t *bytes) {
@@ -571,16 +604,30 @@ int ibp_decompress_gather_positions(const void *slots, int64_t slot_bytes, int64
                                  d_idx, n_idx, out, d_status, reinterpret_cast<cudaStream_t>(s));
 }
 
-int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
-              int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s) {
+static int query_args_ok(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits,
+                         int64_t n_rows, int64_t row_elems, int dtype) {
   if (!dtype_ok(dtype)) return IBP_ERR_DTYPE;
   if (n_rows < 0 || row_elems <= 0) return IBP_ERR_ARG;
-  if (!pointer_ok(d_stats, Where::device_only, 8)) return IBP_ERR_ARG;
   if (n_rows > 0 && (!pointer_ok(d_row_bitmask, Where::device_only, 4) ||
                      !pointer_ok(d_row_bits, Where::device_only, 4)))
     return IBP_ERR_ARG;
+  return IBP_OK;
+}
+
+int ibp_query_async(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                    int64_t row_elems, int dtype, ibp_stats *d_stats, ibp_stream_t s) {
+  if (int rc = query_args_ok(d_row_bitmask, d_row_bits, n_rows, row_elems, dtype)) return rc;
+  if (!pointer_ok(d_stats, Where::device_only, 8)) return IBP_ERR_ARG;
   return launch_query(d_row_bitmask, d_row_bits, n_rows, row_elems * width_of(dtype) / 8, d_stats,
                       reinterpret_cast<cudaStream_t>(s));
+}
+
+int ibp_query(const uint32_t *d_row_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+              int64_t row_elems, int dtype, ibp_stats *h_out, ibp_stream_t s) {
+  if (!h_out) return IBP_ERR_ARG;
+  if (int rc = query_args_ok(d_row_bitmask, d_row_bits, n_rows, row_elems, dtype)) return rc;
+  return launch_query_sync(d_row_bitmask, d_row_bits, n_rows, row_elems * width_of(dtype) / 8,
+                           h_out, reinterpret_cast<cudaStream_t>(s));
 }
 
 int ibp_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, ibp_stream_t s) {

@@ -41,7 +41,8 @@ int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, ui
 int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *counters,
                       cudaStream_t s);
 int launch_meta_finalize(const unsigned long long *counters, int64_t n_elems, int dtype, double T,
-                         uint32_t block_elems, ibp_meta *d_meta, cudaStream_t s);
+                         uint32_t block_elems, ibp_meta *d_meta, int32_t *d_status,
+                         cudaStream_t s);
 int launch_build_meta_select(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                              double T, ibp_meta *d_meta, ibp_mask_candidate *d_candidates,
                              void *d_scratch, cudaStream_t s);
@@ -107,6 +108,10 @@ int launch_pack(const void *slots, int64_t slot_bytes, int64_t n_rows, int64_t r
                 cudaStream_t s);
 int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
                  int64_t raw_bytes, ibp_stats *d_stats, cudaStream_t s);
+// The same reduction into a result array built into the library, copied to *h_out;
+// synchronises s.
+int launch_query_sync(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
+                      int64_t raw_bytes, ibp_stats *h_out, cudaStream_t s);
 int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s);
 
 }  // namespace ibp

@@ -86,14 +86,20 @@ __global__ void __launch_bounds__(META_THREADS)
   if (mine) atomicAdd(&counters[lane], mine);
 }
 
+// Counters that exceed the element count cannot come from n_elems elements (e.g. one
+// holder's element count passed with counters summed over several holders): the
+// metadata is then written with no invariant position and an invalid dtype, so that
+// compression and gathers with it report IBP_ERR_META instead of silently storing
+// every row raw, and IBP_ERR_META is recorded in *status.
 __global__ void meta_finalize_kernel(const unsigned long long *counters, int64_t n_elems, int w,
                                      double T, uint32_t dtype, uint32_t block_elems,
-                                     ibp_meta *meta) {
+                                     ibp_meta *meta, int32_t *status) {
   const int j = threadIdx.x;  // one warp
   unsigned long long c1 = 0;  // element bit j: bits j, j + w, ... of the 32-bit words
   if (j < w)
     for (int q = j; q < 32; q += w) c1 += counters[q];
   const unsigned long long N = (unsigned long long)n_elems;
+  const bool bad = __any_sync(FULL, c1 > N);
   const unsigned long long c0 = N - c1;
   const bool v = c1 > c0;  // a tie keeps 0
   const unsigned long long cv = v ? c1 : c0;
@@ -102,11 +108,12 @@ __global__ void meta_finalize_kernel(const unsigned long long *counters, int64_t
   const uint32_t bitval = __ballot_sync(FULL, inv && v);
   if (j == 0) {
     ibp_meta m;
-    m.mask = mask;
-    m.bitval = bitval;
-    m.dtype = dtype;
+    m.mask = bad ? 0u : mask;
+    m.bitval = bad ? 0u : bitval;
+    m.dtype = bad ? IBP_META_INVALID : dtype;
     m.block_elems = block_elems;
     *meta = m;
+    if (bad) report(status, IBP_ERR_META);
   }
 }
 
@@ -125,8 +132,8 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
   const int64_t want = std::max<int64_t>(1, (npairs + META_THREADS - 1) / META_THREADS);
   // one wave of resident CTAs (the loop is grid-strided; a partial second wave
   // would run at a fraction of the occupancy)
-  static std::atomic<int> occupancy{0};  // resident CTAs per SM, looked up once
-  int per_sm = occupancy.load(std::memory_order_relaxed);
+  static std::atomic<int> occupancy[64];  // resident CTAs per SM, looked up once per device
+  int per_sm = dev.device < 64 ? occupancy[dev.device].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, meta_count_kernel, META_THREADS, 0) !=
@@ -134,7 +141,7 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
         n < 1)
       n = 1;
     per_sm = n;
-    occupancy.store(n, std::memory_order_relaxed);
+    if (dev.device < 64) occupancy[dev.device].store(n, std::memory_order_relaxed);
   }
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
   meta_count_kernel<<<grid, META_THREADS, 0, s>>>(static_cast<const uint4 *>(rows), nvec, tail,
@@ -143,9 +150,10 @@ int launch_meta_count(const void *rows, int64_t n_words, unsigned long long *cou
 }
 
 int launch_meta_finalize(const unsigned long long *counters, int64_t n_elems, int dtype, double T,
-                         uint32_t block_elems, ibp_meta *d_meta, cudaStream_t s) {
+                         uint32_t block_elems, ibp_meta *d_meta, int32_t *d_status,
+                         cudaStream_t s) {
   meta_finalize_kernel<<<1, 32, 0, s>>>(counters, n_elems, width_of(dtype), T, (uint32_t)dtype,
-                                        block_elems, d_meta);
+                                        block_elems, d_meta, d_status);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 
@@ -153,7 +161,7 @@ int launch_build_meta(const void *rows, int64_t n_words, int dtype, double T, ui
                       int64_t n_elems, ibp_meta *d_meta, void *d_scratch, cudaStream_t s) {
   unsigned long long *counters = static_cast<unsigned long long *>(d_scratch);
   if (int rc = launch_meta_count(rows, n_words, counters, s)) return rc;
-  return launch_meta_finalize(counters, n_elems, dtype, T, block_elems, d_meta, s);
+  return launch_meta_finalize(counters, n_elems, dtype, T, block_elems, d_meta, nullptr, s);
 }
 
 }  // namespace ibp
@@ -182,26 +190,72 @@ constexpr int NOALLOC_COUNTER_WORDS = 32;  // one 64-bit counter per bit positio
 static __device__ __align__(256) unsigned long long g_noalloc_meta_counters[NOALLOC_COUNTER_WORDS];
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
+
+// The looked-up address of the array on one device, and the CUDA context it
+// belongs to. A device reset destroys the primary context; the next one loads the
+// library's device code again, possibly at another address, so an address is
+// reused only while the current context is the one it was found in.
+struct NoallocEntry {
+  void *ptr;
+  unsigned long long ctx_id;
+};
 std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {nullptr};
+NoallocEntry g_noalloc[NOALLOC_MAX_DEVICES] = {};
+
+// Unique id of the calling thread's current CUDA context (driver entry points
+// reached through the runtime, so the library needs no link-time driver
+// dependency). False when there is no current context or the driver lacks the call.
+bool current_context_id(unsigned long long *id) {
+  typedef int (*GetCurrentFn)(void **);
+  typedef int (*GetIdFn)(void *, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+    cudaGetLastError();
+  });
+  if (!get_current || !get_id) return false;
+  void *ctx = nullptr;
+  if (get_current(&ctx) != 0 || !ctx) return false;
+  return get_id(ctx, id) == 0;
+}
 
 // Device address of the counter array on the current device. The array's name is
-// only a host-side stand-in in host code, so the address is looked up once per
-// device (with that device current) and reused.
+// only a host-side stand-in in host code, so the address is looked up with the
+// device current, once per device and context, and reused.
 int noalloc_counters(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return IBP_ERR_CUDA;
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (dev >= 0 && dev < NOALLOC_MAX_DEVICES && g_noalloc_ptr[dev]) {
-    *out = g_noalloc_ptr[dev];
+  const bool cacheable = dev >= 0 && dev < NOALLOC_MAX_DEVICES;
+  if (cacheable && have_id && g_noalloc[dev].ptr && g_noalloc[dev].ctx_id == id) {
+    *out = g_noalloc[dev].ptr;
     return IBP_OK;
   }
-  void *ptr = nullptr;
+  void *ptr = nullptr;  // (this also makes the device's primary context current)
   if (cudaGetSymbolAddress(&ptr, g_noalloc_meta_counters) != cudaSuccess || !ptr) {
     cudaGetLastError();
     return IBP_ERR_CUDA;
   }
-  if (dev >= 0 && dev < NOALLOC_MAX_DEVICES) g_noalloc_ptr[dev] = ptr;
+  unsigned long long id_now = 0;
+  if (cacheable) {
+    // without a context id the address is not kept: every call looks it up again
+    g_noalloc[dev].ptr = current_context_id(&id_now) ? ptr : nullptr;
+    g_noalloc[dev].ctx_id = id_now;
+  }
   *out = ptr;
   return IBP_OK;
 }

@@ -45,10 +45,9 @@ def sharded_meta(rows: torch.Tensor, T: float, block_elems: int, meta: torch.Ten
     total number of elements. A rank with no rows passes an empty [0, L] tensor."""
     code = dtype_code(rows, dtype)
     n, L = rows.shape[0], rows.shape[1]
-    if n > 0:
-        meta_count(rows, counters, dtype=code, stream=stream)
-    else:
-        counters.zero_()
+    # with no rows the call only clears the counters, on the same stream as the
+    # exchange and the finalize below (so nothing reads them before the clear)
+    meta_count(rows, counters, dtype=code, stream=stream)
     if counters.is_cuda:  # the exchange is ordered after the count on the same stream
         s = stream if stream is not None else torch.cuda.current_stream(counters.device)
         with torch.cuda.stream(s):

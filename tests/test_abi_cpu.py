@@ -120,9 +120,22 @@ def test_argument_errors_before_cuda(lib):
                                         None) == ibp.ERR_ARG
     # split preprocessing: counts of rows not whole 32-bit words, bad T, bad block
     assert lib.ibp_meta_count(vp(16), 3, 3, ibp.W8, vp(16), None) == ibp.ERR_ARG
-    assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 1.2, 32, vp(16), None) == ibp.ERR_ARG
-    assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 0.9, 48, vp(16), None) == \
+    assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 1.2, 32, vp(16), None, None) == \
+        ibp.ERR_ARG
+    assert lib.ibp_meta_finalize(vp(16), 100, ibp.FP32, 0.9, 48, vp(16), None, None) == \
         ibp.ERR_UNSUPPORTED
+    assert lib.ibp_meta_finalize(vp(16), 0, ibp.FP32, 0.9, 32, vp(16), None, None) == ibp.ERR_ARG
+    assert lib.ibp_meta_finalize(vp(16), 100, 6, 0.9, 32, vp(16), None, None) == ibp.ERR_DTYPE
+    # store statistics: host output needs a destination; sizes, dtype, null arrays
+    st = ibp.Stats()
+    assert lib.ibp_query(None, None, 0, 128, ibp.FP32, None, None) == ibp.ERR_ARG
+    assert lib.ibp_query(None, None, -1, 128, ibp.FP32, ctypes.byref(st), None) == ibp.ERR_ARG
+    assert lib.ibp_query(None, None, 0, 0, ibp.FP32, ctypes.byref(st), None) == ibp.ERR_ARG
+    assert lib.ibp_query(None, None, 5, 128, ibp.FP32, ctypes.byref(st), None) == ibp.ERR_ARG
+    assert lib.ibp_query(None, None, 5, 128, 8, ctypes.byref(st), None) == ibp.ERR_DTYPE
+    assert lib.ibp_query_async(None, None, 0, 128, ibp.FP32, None, None) == ibp.ERR_ARG
+    assert lib.ibp_query_async(None, None, 5, 128, 8, vp(16), None) == ibp.ERR_DTYPE
+    assert ctypes.sizeof(ibp.Stats) == 40
     # de-duplicated gather: scratch size query (table, index arrays, one staged row per
     # index), limits, and an empty list as a no-op
     sz = ctypes.c_size_t(0)

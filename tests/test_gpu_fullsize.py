@@ -168,12 +168,11 @@ def test_gnn_dense_variants_full():
     m0 = sum(1 << j for j in range(32) if float(held[j]) >= T * float(N))
     assert cands[0][0] == m0
     store = GpuStore(n, L, ibp.FP32, B, "host")
-    stats_t = torch.zeros(10, dtype=torch.int32, device=dev)
     for mk, bv, score in cands:
         m = meta_tensor(mk, bv, ibp.FP32, B)
         gpu_compress(rows, m, store)
-        ibp.query(store.bitmask, store.row_bits, n, L, ibp.FP32, stats_t)
-        assert ibp.read_stats(stats_t).stored_bytes == score, hex(mk)
+        assert ibp.query(store.bitmask, store.row_bits, n, L, ibp.FP32).stored_bytes == score, \
+            hex(mk)
     chosen = meta.cpu().numpy().view(np.uint32)
     assert int(chosen[0]) == min(cands, key=lambda c: (c[2], -bin(c[0]).count("1")))[0]
     # sized and packed gathers of the chosen store

@@ -238,6 +238,8 @@ def test_error_status_and_edge_cases():
 
 
 def test_query_stats():
+    """ibp_query (host output, synchronising) and ibp_query_async (device output)
+    against the oracle's totals, on the current stream and on a side stream."""
     words = words_of(gen.gnn_dense(5000))
     n, L = words.shape
     mask, bitval, o_slots, o_bitmask, o_row_bits = oracle_store(words, 0.9, 32)
@@ -245,16 +247,32 @@ def test_query_stats():
     meta = gpu_meta(rows_t, FP32, 0.9, 32)
     store = GpuStore(n, L, FP32, 32, "device")
     gpu_compress(rows_t, meta, store)
-    stats_t = torch.zeros((10,), dtype=torch.int32, device="cuda")
-    ibp.query(store.bitmask, store.row_bits, n, L, FP32, stats_t)
-    st = ibp.read_stats(stats_t)
     stored = oracle.stored_bytes(o_row_bits, o_bitmask, L * 4)
     flags = (o_bitmask[np.arange(n) // 32] >> (np.arange(n) % 32).astype(np.uint32)) & 1
-    assert st.n_rows == n
-    assert st.n_compressed == int(flags.sum())
-    assert st.raw_bytes == n * L * 4
-    assert st.stored_bytes == int(stored.sum())
-    assert st.total_bits == int(o_row_bits.astype(np.int64).sum())
+    expect = (n, int(flags.sum()), n * L * 4, int(stored.sum()),
+              int(o_row_bits.astype(np.int64).sum()))
+
+    def fields(st):
+        return (st.n_rows, st.n_compressed, st.raw_bytes, st.stored_bytes, st.total_bits)
+
+    torch.cuda.synchronize()
+    assert fields(ibp.query(store.bitmask, store.row_bits, n, L, FP32)) == expect
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    assert fields(ibp.query(store.bitmask, store.row_bits, n, L, FP32, stream=side)) == expect
+    stats_t = torch.full((10,), -1, dtype=torch.int32, device="cuda")
+    ibp.query_async(store.bitmask, store.row_bits, n, L, FP32, stats_t)
+    assert fields(ibp.read_stats(stats_t)) == expect
+    # a prefix of the store, and an empty one (null arrays allowed)
+    k = 1234
+    o_k = oracle.stored_bytes(o_row_bits[:k], o_bitmask, L * 4)
+    st = ibp.query(store.bitmask, store.row_bits, k, L, FP32)
+    assert (st.n_rows, st.n_compressed, st.stored_bytes) == (k, int(flags[:k].sum()),
+                                                              int(o_k.sum()))
+    assert fields(ibp.query(None, None, 0, L, FP32)) == (0, 0, 0, 0, 0)
+    with pytest.raises(ibp.IBPError) as e:
+        ibp.query(store.bitmask, store.row_bits, n, L, 7)
+    assert e.value.code == ibp.ERR_DTYPE
 
 
 def test_meta_from_host_rows_matches():

@@ -42,9 +42,7 @@ def select_check(words: np.ndarray, dtype_code: int, T: float, B: int, where: st
     # the chosen metadata stores exactly its score and round-trips
     store = GpuStore(n, L, dtype_code, B, "device")
     gpu_compress(rows_t, meta, store)
-    stats_t = torch.zeros(10, dtype=torch.int32, device="cuda")
-    ibp.query(store.bitmask, store.row_bits, n, L, dtype_code, stats_t)
-    st = ibp.read_stats(stats_t)
+    st = ibp.query(store.bitmask, store.row_bits, n, L, dtype_code)
     assert st.stored_bytes == dict(o_cands)[o_mask]
     idx = np.random.default_rng(n).integers(0, n, size=min(2000, 4 * n)).astype(np.int64)
     out, rc = gpu_gather(store, meta, idx)

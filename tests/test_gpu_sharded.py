@@ -18,7 +18,7 @@ import torch
 import ibp_inputs as gen
 import lossless_bit_level_gb300 as ibp
 import oracle
-from codec_harness import gpu_meta, meta_values, to_torch
+from codec_harness import GpuStore, gpu_meta, meta_values, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +91,41 @@ def test_empty_shard_and_tie():
         assert bool(mask >> 5 & 1) == (T <= 0.5) and not (bitval >> 5 & 1)
 
 
+def test_finalize_rejects_counts_above_element_count():
+    """Counters summed over two holders finalized with one holder's element count:
+    no such set of elements exists, so the metadata comes back invalid (no invariant
+    position, dtype IBP_META_INVALID), ERR_META is recorded, and compression given
+    that metadata reports ERR_META instead of storing every row raw."""
+    words = gen.gnn_dense(4000).view(np.uint32)
+    (_, _, _, _), total = split_meta(words, [2000], FP32, 0.9, 32)
+    counters = torch.from_numpy(total.astype(np.int64)).cuda()
+    meta = torch.zeros(4, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # the first holder's element count with the summed counters: some position has
+    # more ones than elements
+    n_one = 2000 * words.shape[1]
+    assert int(total.max()) > n_one
+    ibp.meta_finalize(counters, n_one, FP32, 0.9, 32, meta, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == ibp.ERR_META
+    m = meta.cpu().numpy().view(np.uint32)
+    assert (int(m[0]), int(m[1]), int(m[2]), int(m[3])) == (0, 0, 0xFFFFFFFF, 32)
+    # the right count on the same counters gives the oracle's metadata, status untouched
+    status.zero_()
+    ibp.meta_finalize(counters, words.size, FP32, 0.9, 32, meta, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert meta_values(meta) == (*oracle.build_meta(words, 0.9), FP32, 32)
+    # a compression given the refused metadata reports it
+    bad = torch.tensor([0, 0, -1, 32], dtype=torch.int32, device="cuda")
+    n, L = words.shape
+    store = GpuStore(n, L, FP32, 32, "device")
+    ibp.compress(to_torch(words, "device"), 32, bad, store.slots, store.bitmask, store.row_bits,
+                 store.status, dtype=FP32)
+    torch.cuda.synchronize()
+    assert int(store.status.item()) == ibp.ERR_META
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
@@ -112,5 +147,15 @@ def test_sharded_meta_through_nccl():
         assert total == words.size
         assert np.array_equal(counters.cpu().numpy(), bit_counts(words))
         assert meta_values(meta) == (*oracle.build_meta(words, 0.9), FP32, 64)
+        # a holder with no rows, called on a stream that is not the current one: the
+        # counters are cleared on that stream, before the exchange reads them
+        counters.fill_(-7)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        empty = torch.empty((0, words.shape[1]), dtype=torch.int32, device="cuda")
+        with pytest.raises(ValueError):
+            sharded_meta(empty, 0.9, 64, meta, counters, dtype=FP32, stream=side)
+        torch.cuda.synchronize()
+        assert np.array_equal(counters.cpu().numpy(), np.zeros(32, dtype=np.int64))
     finally:
         dist.destroy_process_group()
