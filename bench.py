@@ -248,6 +248,41 @@ def measure_link(dev, nbytes=1 << 30, reps=10):
             "zero_copy_read_gbs": best_probe, "bytes": nbytes, "reps": reps}
 
 
+def host_placement(dev):
+    """Where the page-locked buffers can live relative to the GPU, read from sysfs and
+    the process status (read-only): the GPU's NUMA node, the nodes online, and the
+    CPUs and memory nodes this process may use. With a single node every pinned
+    buffer is local to the GPU."""
+    out = {}
+    bus = None
+    try:
+        q = subprocess.run(["nvidia-smi", f"--id={dev.index or 0}", "--query-gpu=pci.bus_id",
+                            "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+        bus = q.stdout.strip() or bus
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if bus:
+        dom, rest = bus.split(":", 1)
+        sysfs = f"/sys/bus/pci/devices/{dom[-4:].lower()}:{rest.lower()}/numa_node"
+        try:
+            out["gpu_numa_node"] = int(open(sysfs).read().strip())
+        except (OSError, ValueError):
+            out["gpu_numa_node"] = None
+        out["gpu_pci"] = bus
+    try:
+        out["nodes_online"] = open("/sys/devices/system/node/online").read().strip()
+    except OSError:
+        out["nodes_online"] = None
+    try:
+        for line in open("/proc/self/status"):
+            if line.startswith(("Cpus_allowed_list", "Mems_allowed_list")):
+                k, v = line.split(":", 1)
+                out[k.strip().lower()] = v.strip()
+    except OSError:
+        pass
+    return out
+
+
 def measure_hbm_copy(dev, nbytes=1 << 30, reps=10):
     a_t = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).fill_(1)
     b_t = torch.empty_like(a_t)
@@ -813,6 +848,272 @@ def run_e2e(store, host_batches, steps, warmup, dev):
             "ms_per_step": t * 1e3, "streams": ns}
 
 
+# ----------------------------------------------------------------------------- five configs
+
+def _sig(x, nd=3):
+    """x rounded to nd significant digits (the per-config summary is kept short)."""
+    if x is None or x == 0 or not np.isfinite(x):
+        return x
+    return float(f"{x:.{nd}g}")
+
+
+def time_steps(fn, steps, warmup, flush):
+    """warmup untimed calls, then steps calls, each after an L2 flush and timed with
+    CUDA events on the launch stream; mean seconds per call. fn(k) runs step k."""
+    s = torch.cuda.current_stream()
+    for k in range(warmup):
+        flush()
+        fn(k)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for k in range(steps):
+        flush()
+        starts[k].record(s)
+        fn(k)
+        ends[k].record(s)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)])) * 1e-3
+
+
+class TableBench:
+    """One table of a workload, measured the way every config is: rows and slots in
+    HBM, metadata and compression timed (raw input per second; compression's roofline
+    counts the rows read, the stored bytes and the bitmask/row-size words written),
+    then gathers of index batches (or in-order streams of whole tables, idx None)
+    from the slots in HBM and from a copy of them in page-locked host memory."""
+
+    def __init__(self, words, dtype, T, B, dev, flush, hbm_peak):
+        self.st = Store(words, dtype, T, B, "device", dev)
+        self.dev, self.flush, self.hbm_peak = dev, flush, hbm_peak
+        st = self.st
+        self.t_meta, _ = time_stage(st.build_meta, 3, flush)
+        self.t_comp, _ = time_stage(st.compress, 3, flush)
+        torch.cuda.synchronize()
+        assert int(st.status.item()) == 0
+        self.stats = st.stats()
+        self.stored = st.stored_per_row()
+        self.raw = st.n * st.raw_bytes
+        self.comp_alg = self.raw + float(self.stored.sum()) + 4 * ((st.n + 31) // 32) + 4 * st.n
+        self.host_slots = None
+
+    def slots(self, where):
+        if where == "device":
+            return self.st.slots
+        if self.host_slots is None:
+            self.host_slots = torch.empty(self.st.slots.shape, dtype=torch.uint8, pin_memory=True)
+            self.host_slots.copy_(self.st.slots)
+        return self.host_slots
+
+    def gather(self, where, batches_np, steps=10, warmup=3):
+        """Mean seconds per gather of batches_np[k % len] (None: every row in order
+        through ibp_decompress_range), and the output checked on the device against
+        the rows of the last batch."""
+        st = self.st
+        slots = self.slots(where)
+        if batches_np is None:
+            out = torch.empty_like(st.rows)
+
+            def fn(k):
+                ibp.decompress_range(slots, st.n, st.L, st.dtype, st.B, st.bitmask, st.meta, 0,
+                                     st.n, out, st.status)
+        else:
+            batches = [torch.from_numpy(b).to(self.dev) for b in batches_np]
+            out = torch.empty((batches_np[0].size, st.L), dtype=st.word_dtype, device=self.dev)
+
+            def fn(k):
+                ibp.decompress_gather(slots, st.n, st.L, st.dtype, st.B, st.bitmask, st.meta,
+                                      batches[k % len(batches)], out, st.status)
+        t = time_steps(fn, steps, warmup, self.flush)
+        torch.cuda.synchronize()
+        assert int(st.status.item()) == 0
+        want = st.rows if batches_np is None else st.rows[batches[(steps - 1) % len(batches)]]
+        assert torch.equal(out, want), "gathered rows differ from the originals"
+        del out
+        return t
+
+    def summary(self):
+        st = self.st
+        return {"rows": st.n, "save_pct": _sig(100.0 * (1.0 - self.stats.stored_bytes / self.raw)),
+                "meta_GBs": _sig(self.raw / self.t_meta / 1e9),
+                "comp_GBs": _sig(self.raw / self.t_comp / 1e9),
+                "comp_frac": _sig(self.comp_alg / self.t_comp / 1e9 / self.hbm_peak)}
+
+
+def gather_entry(t, n_idx, row_bytes, stored_gathered, distinct_stored, where, h2d, hbm_peak,
+                 index_bytes=8):
+    """One gather result: GB/s of output rows and the roofline fraction. HBM: (index +
+    stored + output bytes) / t over the device copy. Host slots: stored bytes of the
+    gathered rows (duplicates counted) / t over the pinned H2D copy, and the same for
+    the distinct rows only (each distinct row crosses the link at least once, so the
+    true link fraction lies at or above it)."""
+    out_bytes = n_idx * row_bytes
+    e = {"ms": _sig(t * 1e3), "GBs": _sig(out_bytes / t / 1e9)}
+    if where == "device":
+        alg = n_idx * index_bytes + stored_gathered + out_bytes
+        e["frac"] = _sig(alg / t / 1e9 / hbm_peak)
+        e["alg_MB"] = _sig(alg / 1e6)
+    else:
+        e["link_frac"] = _sig(stored_gathered / t / 1e9 / h2d)
+        e["link_frac_distinct"] = _sig(distinct_stored / t / 1e9 / h2d)
+        e["link_MB"] = _sig(stored_gathered / 1e6)
+    return e
+
+
+def configs_leg(dev, flush, hbm_peak, link, main):
+    """Every configuration of the workload set, measured in one pass (inputs generated
+    from the seeded recipe, the big ones in parallel host threads):
+      tiny FP32 4096 x 128, 1024 uniform indices, HBM;
+      dense GNN 2,000,000 x 128 (the headline store, from the main measurement) plus a
+        1,000,000-index Zipf(1.0) gather from HBM whose output (512 MB) exceeds L2;
+      sparse GNN 500,000 x 512, 100,000 uniform indices, host and HBM;
+      DLRM: table 0 (65,536 Zipf(1.05) lookups, host and HBM) and all 26 tables in
+        HBM, one lookup batch per table per step, 26 separate calls vs one batched call;
+      LLM BF16: layer 0's seven weights and its K and V caches (8 x 4096 tokens), each
+        tensor streamed in order through ibp_decompress_range from host and from HBM;
+        summed over the layer (the other 31 layers have the same shapes and
+        distributions, so a layer's time scales by 32 for the model).
+    Every gather's output is checked against the original rows on the device."""
+    import concurrent.futures as cf
+
+    h2d = link["h2d_memcpy_gbs"]
+    res = {}
+    pool = cf.ThreadPoolExecutor(max_workers=max(2, min(16, os.cpu_count() or 2)))
+    # the big inputs are generated in the background while the small configs run
+    dlrm_f = [pool.submit(gen.dlrm_table, t) for t in range(26)]
+    llm_f = {name: pool.submit(gen.llm_weight, 0, name) for name in gen.LLM_MATRICES}
+    llm_f["K"] = pool.submit(gen.llm_kv, 0, 0)
+    llm_f["V"] = pool.submit(gen.llm_kv, 0, 1)
+    sparse_f = pool.submit(gen.gnn_sparse)
+
+    def table_config(words, dtype, T, B, batches_np, wheres, steps=10):
+        tb = TableBench(words, dtype, T, B, dev, flush, hbm_peak)
+        r = tb.summary()
+        for where in wheres:
+            t = tb.gather(where, batches_np, steps=steps)
+            if batches_np is None:
+                n_idx, g_st, d_st, ib = tb.st.n, float(tb.stored.sum()), float(tb.stored.sum()), 0
+            else:
+                n_idx = batches_np[0].size
+                g_st = float(np.mean([tb.stored[b].sum() for b in batches_np]))
+                d_st = float(np.mean([tb.stored[np.unique(b)].sum() for b in batches_np]))
+                ib = 8
+            r["hbm" if where == "device" else "host"] = gather_entry(
+                t, n_idx, tb.st.raw_bytes, g_st, d_st, where, h2d, hbm_peak, ib)
+        return tb, r
+
+    # tiny: a correctness config (0.5 MB of output per launch is launch-bound)
+    words = gen.tiny_fp32().view(np.uint32)
+    b = [gen.uniform_indices(words.shape[0], 1024, part=k, workload=gen.TINY) for k in range(4)]
+    tb, res["tiny"] = table_config(words, ibp.FP32, 0.9, 32, b, ("device",), steps=20)
+    del tb
+
+    # dense GNN: the headline store's figures, and a large HBM batch
+    res["gnn_dense"] = main
+    words = gen.gnn_dense().view(np.uint32)
+    big = [gen.zipf_indices(words.shape[0], 1_000_000, 1.0, part=100 + k,
+                            workload=gen.GNN_DENSE) for k in range(2)]
+    tb = TableBench(words, ibp.FP32, 0.9, 32, dev, flush, hbm_peak)
+    t = tb.gather("device", big, steps=6)
+    g_st = float(np.mean([tb.stored[x].sum() for x in big]))
+    res["gnn_dense"]["hbm_1M_idx"] = gather_entry(t, big[0].size, tb.st.raw_bytes, g_st, g_st,
+                                                  "device", h2d, hbm_peak)
+    del tb, words, big
+    torch.cuda.empty_cache()
+
+    # sparse GNN
+    words = sparse_f.result().view(np.uint32)
+    b = [gen.uniform_indices(words.shape[0], 100_000, part=k, workload=gen.GNN_SPARSE)
+         for k in range(4)]
+    tb, res["gnn_sparse"] = table_config(words, ibp.FP32, 0.9, 32, b, ("host", "device"))
+    del tb, words
+    torch.cuda.empty_cache()
+
+    # DLRM: table 0 alone, then the 26 tables in HBM
+    L, T, B, lookups = 128, 0.95, 32, 65_536
+    tables, jobs, stored_g = [], [], 0
+    for t_id in range(26):
+        words = dlrm_f[t_id].result().view(np.uint32)
+        dlrm_f[t_id] = None
+        ix = gen.zipf_indices(words.shape[0], lookups, 1.05, part=t_id, workload=gen.DLRM)
+        if t_id == 0:
+            tb, r = table_config(words, ibp.FP32, T, B, [ix], ("host", "device"))
+            res["dlrm"] = {"table0": r}
+            tb.host_slots = None
+        else:
+            tb = TableBench(words, ibp.FP32, T, B, dev, flush, hbm_peak)
+        st = tb.st
+        stored_g += int(tb.stored[ix].sum())
+        out = torch.empty((lookups, L), dtype=torch.int32, device=dev)
+        jobs.append((st.slots, st.n, st.bitmask, st.meta, torch.from_numpy(ix).to(dev), out))
+        st.rows = None  # rows are not needed past compression; keep HBM use down
+        tables.append(tb)
+        del words
+    out_bytes = 26 * lookups * 4 * L
+    alg = 26 * lookups * 8 + stored_g + out_bytes
+
+    def separate(k):
+        for slots, n, bm, meta, ix, out in jobs:
+            ibp.decompress_gather(slots, n, L, ibp.FP32, B, bm, meta, ix, out)
+
+    def batched(k):
+        ibp.decompress_gather_batched(jobs, L, ibp.FP32, B)
+
+    d = {"save_pct": _sig(100.0 * (1.0 - sum(x.stats.stored_bytes for x in tables) /
+                                   sum(x.raw for x in tables))),
+         "comp_GBs": _sig(sum(x.raw for x in tables) / sum(x.t_comp for x in tables) / 1e9),
+         "comp_frac": _sig(sum(x.comp_alg for x in tables) / sum(x.t_comp for x in tables) /
+                           1e9 / hbm_peak)}
+    for name, fn in (("separate_hbm", separate), ("batched_hbm", batched)):
+        t = time_steps(fn, 8, 3, flush)
+        d[name] = {"ms": _sig(t * 1e3), "GBs": _sig(out_bytes / t / 1e9),
+                   "frac": _sig(alg / t / 1e9 / hbm_peak)}
+    torch.cuda.synchronize()
+    for j in (0, 13, 25):  # rows back exactly (the tables' rows are regenerated)
+        ref = torch.from_numpy(gen.dlrm_table(j).view(np.int32)).to(dev)
+        assert torch.equal(jobs[j][5], ref[jobs[j][4]])
+        del ref
+    res["dlrm"]["tables26"] = d
+    del tables, jobs
+    torch.cuda.empty_cache()
+
+    # LLM: one decoder layer, every row of each tensor streamed in order
+    parts = {"weights": [*gen.LLM_MATRICES], "kv": ["K", "V"]}
+    acc = {}
+    for part, names in parts.items():
+        a = dict(raw=0, stored=0, t_comp=0.0, comp_alg=0.0, host=0.0, device=0.0)
+        for name in names:
+            words = llm_f[name].result()
+            llm_f[name] = None
+            tb = TableBench(words, ibp.BF16, 0.9, 64, dev, flush, hbm_peak)
+            a["raw"] += tb.raw
+            a["stored"] += int(tb.stats.stored_bytes)
+            a["t_comp"] += tb.t_comp
+            a["comp_alg"] += tb.comp_alg
+            for where in ("host", "device"):
+                a[where] += tb.gather(where, None, steps=6)
+            del tb, words
+            torch.cuda.empty_cache()
+        acc[part] = a
+    pool.shutdown()
+
+    def llm_entry(a):
+        e = {"save_pct": _sig(100.0 * (1.0 - a["stored"] / a["raw"])),
+             "comp_GBs": _sig(a["raw"] / a["t_comp"] / 1e9),
+             "comp_frac": _sig(a["comp_alg"] / a["t_comp"] / 1e9 / hbm_peak)}
+        e["host"] = gather_entry(a["host"], 1, a["raw"], a["stored"], a["stored"], "host", h2d,
+                                 hbm_peak)
+        e["hbm"] = gather_entry(a["device"], 1, a["raw"], a["stored"], a["stored"], "device",
+                                h2d, hbm_peak, index_bytes=0)
+        return e
+
+    layer = {k: acc["weights"][k] + acc["kv"][k] for k in acc["weights"]}
+    res["llm_layer0"] = {"all": llm_entry(layer), "weights": llm_entry(acc["weights"]),
+                         "kv": llm_entry(acc["kv"]),
+                         "note": "ms per layer; 32 layers of the same shapes: x32"}
+    return res
+
+
 # ----------------------------------------------------------------------------- oracle arm
 
 def oracle_sample(wl, seconds_budget=10.0, sample_rows=200_000, all_cores_budget=4.0):
@@ -960,6 +1261,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gnn_dense")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the HBM-resident and e2e legs")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the pass over every configuration (default workload only)")
     ap.add_argument("--residency", choices=["host", "device"], default=None,
                     help="override where slots and rows live (default: the workload's)")
     ap.add_argument("--indices", choices=["zipf", "uniform"], default=None,
@@ -1188,7 +1491,8 @@ def main():
             "compress": {"gbs_raw_in": table_raw / comp_t / 1e9, "ms": comp_t * 1e3,
                          "residency": residency},
         },
-        "link": link, "hbm_copy_gbs_this_run": hbm_copy_now,
+        "link": link, "host_placement": host_placement(dev),
+        "hbm_copy_gbs_this_run": hbm_copy_now,
         "launch_floor_us": {"value": launch_floor * 1e6,
                             "what": "CUDA-event time of a one-element kernel after the L2 "
                                     "flush, timed like a gather step"},
@@ -1206,6 +1510,33 @@ def main():
             comp_t / 1e9 / hbm_peak
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"], line["cpu_baseline_all_cores"] = oracle_sample(wl)
+    if (args.workload == "gnn_dense" and not args.quick and not args.no_configs and
+            not args.rows and residency == "host"):
+        # every configuration, summarised in one short object at the end of the line
+        distinct = float(np.mean([stored[np.unique(hb.numpy())].sum()
+                                  for hb in host_batches]))
+        main_cfg = {
+            "rows": n, "save_pct": _sig(line["space_saving_pct"]),
+            "meta_GBs": _sig(table_raw / meta_t / 1e9),
+            "comp_host_GBs": _sig(table_raw / comp_t / 1e9),
+            "host": gather_entry(t_step, wl["batch"], store.raw_bytes, stored_per_step, distinct,
+                                 "host", link["h2d_memcpy_gbs"], hbm_peak)}
+        if roofline.get("traffic_frac"):
+            main_cfg["host"]["link_frac_ncu"] = _sig(roofline["traffic_frac"])
+        if "stages_hbm" in line:
+            main_cfg["comp_GBs"] = _sig(line["stages_hbm"]["compress"]["gbs_raw_in"])
+            main_cfg["comp_frac"] = _sig(line["stages_hbm"]["compress"]["frac_of_hbm"])
+        if "hbm_resident" in line:
+            h = line["hbm_resident"]
+            main_cfg["hbm"] = {"ms": _sig(h["ms_per_step"]), "GBs": _sig(h["value"]),
+                               "frac": _sig(h["roofline"]["frac"]),
+                               "alg_MB": _sig(h["roofline"]["algorithmic_bytes_per_launch"] / 1e6)}
+        del store
+        torch.cuda.empty_cache()
+        with ClockSampler(torch.cuda.current_device()) as clk_c:
+            cfgs = configs_leg(dev, flush, hbm_peak, link, main_cfg)
+        cfgs["clocks"] = clk_c.summary()
+        line["configs"] = cfgs
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:

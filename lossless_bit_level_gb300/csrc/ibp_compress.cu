@@ -544,10 +544,10 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
       default: return launch_groups_lwb<64>(a, dev, ns, s);
     }
   }
-  if (g.raw_bytes <= compress_rows_max_bytes()) {  // long rows: one CTA per row
-    const int rc = launch_compress_rows(rows, n_rows, g, dtype, d_meta, slots, slot_bytes,
-                                        d_bitmask, d_row_bits, d_status, dev, s);
-    if (rc != IBP_ERR_UNSUPPORTED) return rc;  // else (shared memory too small): a warp per row
+  if (g.raw_bytes <= compress_stream_max_bytes()) {  // long rows: one warp per row, one pass
+    const int rc = launch_compress_stream(rows, n_rows, g, dtype, d_meta, slots, slot_bytes,
+                                          d_bitmask, d_row_bits, d_status, dev, s);
+    if (rc != IBP_ERR_UNSUPPORTED) return rc;
   }
   const size_t smem = (size_t)a.warps * a.warp_bytes;
   switch (g.lwb) {

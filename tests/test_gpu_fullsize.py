@@ -11,6 +11,9 @@ Tables are generated, checked and freed one at a time.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -25,14 +28,19 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
 def check_table(words: np.ndarray, dtype: int, T: float, B: int, batches, residencies,
-                sample_rows: int = 4096, oracle_meta: bool = True, seed: int = 0):
+                sample_rows: int = 4096, oracle_meta: bool = True, seed: int = 0,
+                oracle_meta_future=None):
+    """oracle_meta_future: the oracle's (mask, bitval) of ``words`` being computed in
+    another thread (a concurrent.futures.Future), used instead of computing it here."""
     n, L = words.shape
     raw = L * words.dtype.itemsize
     rows_host = to_torch(words, "host")
     meta = gpu_meta(rows_host, dtype, T, B)
     mask, bitval, mdt, mb = meta_values(meta)
     assert (mdt, mb) == (dtype, B)
-    if oracle_meta:
+    if oracle_meta_future is not None:
+        assert (mask, bitval) == oracle_meta_future.result()
+    elif oracle_meta:
         assert (mask, bitval) == oracle.build_meta(words, T)
     # compress zero-copy from host rows into host slots (the bench's configuration)
     store = GpuStore(n, L, dtype, B, "host")
@@ -113,22 +121,54 @@ def test_dlrm_all_tables_full():
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("layer", [0, 31])
+_LLM_TENSORS = [*gen.LLM_MATRICES, "K", "V"]
+_pool = None
+_pending = {}  # layer -> {tensor name: Future of its words}
+
+
+def _llm_pool() -> cf.ThreadPoolExecutor:
+    global _pool
+    if _pool is None:  # numpy's generators and the oracle's C calls release the GIL
+        _pool = cf.ThreadPoolExecutor(max_workers=max(2, min(12, os.cpu_count() or 2)))
+    return _pool
+
+
+def _llm_layer_futures(layer: int) -> dict:
+    if layer not in _pending:
+        pool = _llm_pool()
+        futs = {name: pool.submit(gen.llm_weight, layer, name) for name in gen.LLM_MATRICES}
+        futs["K"] = pool.submit(gen.llm_kv, layer, 0)
+        futs["V"] = pool.submit(gen.llm_kv, layer, 1)
+        _pending[layer] = futs
+    return _pending[layer]
+
+
+@pytest.mark.parametrize("layer", range(gen.LLM_LAYERS))
 def test_llm_layer_full(layer):
-    """One decoder layer at full size: the seven weight matrices and K, V caches
-    (8 x 4096 tokens x 4096 channels), per tensor T = 0.9, B = 64; every row streamed
-    in order from host slots."""
-    for name in gen.LLM_MATRICES:
-        words = gen.llm_weight(layer, name)
-        idx = np.arange(words.shape[0], dtype=np.int64)
-        check_table(words, ibp.BF16, 0.9, 64, [idx], ("host",), sample_rows=512, seed=layer)
-    for kv in (0, 1):
-        words = gen.llm_kv(layer, kv)
-        idx = np.arange(words.shape[0], dtype=np.int64)
-        check_table(words, ibp.BF16, 0.9, 64, [idx], ("host", "device"), sample_rows=1024,
-                    seed=layer + kv)
-        del words
-        torch.cuda.empty_cache()
+    """Every decoder layer at full size: the seven weight matrices and the K, V caches
+    (8 x 4096 tokens x 4096 channels), per tensor T = 0.9, B = 64; the metadata of
+    every tensor against the oracle's over the whole tensor, sampled slots against
+    the oracle's, every row streamed in order from host slots (the K and V caches
+    also from HBM) against the original. The next layer is generated in background
+    threads while this one is checked."""
+    futs = _llm_layer_futures(layer)
+    if layer + 1 < gen.LLM_LAYERS:
+        _llm_layer_futures(layer + 1)
+    pool = _llm_pool()
+    try:
+        for name in _LLM_TENSORS:
+            words = futs[name].result()
+            o_meta = pool.submit(oracle.build_meta, words, 0.9)
+            idx = np.arange(words.shape[0], dtype=np.int64)
+            kv = name in ("K", "V")
+            check_table(words, ibp.BF16, 0.9, 64, [idx], ("host", "device") if kv else ("host",),
+                        sample_rows=1024 if kv else 512, seed=layer + (name == "V"),
+                        oracle_meta_future=o_meta)
+            del words
+            futs[name] = None
+            torch.cuda.empty_cache()
+    finally:
+        _pending.pop(layer, None)
 
 
 def test_gnn_dense_variants_full():
