@@ -964,8 +964,9 @@ def configs_leg(dev, flush, hbm_peak, link, main):
     """Every configuration of the workload set, measured in one pass (inputs generated
     from the seeded recipe, the big ones in parallel host threads):
       tiny FP32 4096 x 128, 1024 uniform indices, HBM;
-      dense GNN 2,000,000 x 128 (the headline store, from the main measurement) plus a
-        1,000,000-index Zipf(1.0) gather from HBM whose output (512 MB) exceeds L2;
+      dense GNN 2,000,000 x 128 (the headline store, from the main measurement) plus
+        1,000,000-index gathers from HBM whose output (512 MB) exceeds L2, Zipf(1.0)
+        and uniform;
       sparse GNN 500,000 x 512, 100,000 uniform indices, host and HBM;
       DLRM: table 0 (65,536 Zipf(1.05) lookups, host and HBM) and all 26 tables in
         HBM, one lookup batch per table per step, 26 separate calls vs one batched call;
@@ -1018,7 +1019,15 @@ def configs_leg(dev, flush, hbm_peak, link, main):
     g_st = float(np.mean([tb.stored[x].sum() for x in big]))
     res["gnn_dense"]["hbm_1M_idx"] = gather_entry(t, big[0].size, tb.st.raw_bytes, g_st, g_st,
                                                   "device", h2d, hbm_peak)
-    del tb, words, big
+    # the same size with uniform indices: few duplicates, so nearly every byte counted
+    # is a DRAM byte (Zipf's hot rows are served from L2)
+    uni = [gen.uniform_indices(words.shape[0], 1_000_000, part=200 + k, workload=gen.GNN_DENSE)
+           for k in range(2)]
+    t = tb.gather("device", uni, steps=6)
+    g_st = float(np.mean([tb.stored[x].sum() for x in uni]))
+    res["gnn_dense"]["hbm_1M_uniform"] = gather_entry(t, uni[0].size, tb.st.raw_bytes, g_st,
+                                                      g_st, "device", h2d, hbm_peak)
+    del tb, words, big, uni
     torch.cuda.empty_cache()
 
     # sparse GNN
