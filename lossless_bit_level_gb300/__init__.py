@@ -78,6 +78,9 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_meta_finalize", "ibp_build_meta_block_positions", "ibp_gather_dedup_scratch_bytes",
            "ibp_decompress_gather_dedup", "ibp_query_async")
 
+# declared in include/ibp_testing.h (a testing hook, not part of the codec)
+TESTING_SYMBOLS = ("ibp_testing_set_wait_limit_ns",)
+
 MAX_MASK_CANDIDATES = 33
 
 
@@ -133,6 +136,8 @@ def load() -> ctypes.CDLL:
                                                  vp, vp, vp]
     for name in SYMBOLS[1:]:
         getattr(lib, name).restype = i32
+    lib.ibp_testing_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.ibp_testing_set_wait_limit_ns.restype = ctypes.c_uint64
     _lib = lib
     return lib
 
@@ -488,3 +493,9 @@ def probe_read(src: torch.Tensor, sink: torch.Tensor, nbytes: int | None = None,
     """ibp_probe_read: stream ``nbytes`` of ``src`` through the GPU (bandwidth probe)."""
     n = src.numel() * src.element_size() if nbytes is None else int(nbytes)
     _check(load().ibp_probe_read(_ptr(src), n, _ptr(sink), _stream(stream)), "ibp_probe_read")
+
+
+def testing_set_wait_limit_ns(ns: int) -> int:
+    """ibp_testing_set_wait_limit_ns (include/ibp_testing.h): the limit of the gather
+    kernels' bounded waits, in ns (0: the default 2 s); returns the previous one."""
+    return int(load().ibp_testing_set_wait_limit_ns(int(ns)))

@@ -166,8 +166,9 @@ __device__ __forceinline__ void cp_async_wait() {
 // ---- mbarrier helpers ------------------------------------------------------------
 // Waits are bounded: each poll asks the hardware to suspend the warp for up to
 // WAIT_SUSPEND_NS (it wakes as soon as the phase completes, so a waiting warp takes
-// no issue slots); a wait gives up after WAIT_TIMEOUT_NS of global time or
-// WAIT_POLLS polls, whichever comes first, and the caller then records
+// no issue slots); a wait gives up after timeout_ns of global time (WAIT_TIMEOUT_NS
+// unless a launcher passes another limit) or WAIT_POLLS polls, whichever comes
+// first, and the caller then records
 // IBP_ERR_TIMEOUT instead of waiting forever.
 constexpr uint32_t WAIT_SUSPEND_NS = 1u << 16;
 constexpr uint64_t WAIT_TIMEOUT_NS = 2000000000ull;
@@ -219,12 +220,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait for the phase of `bar` with the given parity to complete; gives up when the
 // time or poll bound runs out, or as soon as *abort (nullable) is set. Returns true
 // when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                          uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < WAIT_POLLS; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((abort && *abort) || global_ns() - t0 > WAIT_TIMEOUT_NS) return false;
+    if ((abort && *abort) || global_ns() - t0 > timeout_ns) return false;
   }
   return false;
 }

@@ -73,6 +73,8 @@ struct GatherArgs {
   // a negative index is a unit with nothing to do, not an error (internal lists whose
   // tail is unused, e.g. the distinct rows of a de-duplicated gather)
   uint32_t skip_negative;
+  // limit of each bounded wait of the warp-specialised kernel, in ns of global time
+  uint64_t wait_ns;
 };
 
 // The plan of one unit (identical in every lane of its team).
@@ -610,7 +612,7 @@ __device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64
                           ? plan_unit<true>(a, shrink, u0 + k, r, true, load_span(a, r))
                           : plan_unit<false>(a, shrink, u0 + k, r, true, EntrySpan{0, 0});
       const int slot = (int)(k % PLAN_SLOTS);
-      ok = mbar_wait(&freed[slot], (uint32_t)((k / PLAN_SLOTS) & 1) ^ 1u, abort);
+      ok = mbar_wait(&freed[slot], (uint32_t)((k / PLAN_SLOTS) & 1) ^ 1u, abort, a.wait_ns);
       if (ok) {
         PlanSlot p;
         p.src = un.src;
@@ -645,7 +647,7 @@ __device__ __forceinline__ Unit ws_take(const GatherArgs &a, int64_t k, int64_t 
   *ok = true;
   if (k >= count) return un;
   const int slot = (int)(k % PLAN_SLOTS);
-  *ok = mbar_wait(&planned[slot], (uint32_t)((k / PLAN_SLOTS) & 1), abort);
+  *ok = mbar_wait(&planned[slot], (uint32_t)((k / PLAN_SLOTS) & 1), abort, a.wait_ns);
   if (*ok) {
     const PlanSlot p = plans[slot];
     un.src = p.src;
@@ -858,6 +860,15 @@ int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const 
 
 }  // namespace
 
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{0};  // 0: WAIT_TIMEOUT_NS
+}  // namespace
+
+uint64_t gather_wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v ? v : WAIT_TIMEOUT_NS;
+}
+
 int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
                   uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
@@ -876,6 +887,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.row_bits = d_offsets ? nullptr : d_row_bits;
   a.span_align = slots_in_device_memory ? 16u : 128u;
   a.skip_negative = skip_negative ? 1u : 0u;
+  a.wait_ns = gather_wait_limit_ns();
   a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
   a.n_rows = n_rows;
   a.bitmask = d_bitmask;
@@ -926,6 +938,7 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
   a = GatherArgs{};
   a.span_align = 16u;
   a.skip_negative = 0u;
+  a.wait_ns = gather_wait_limit_ns();
   a.status = d_status;
   a.dtype = dtype;
   a.block_elems = (uint32_t)g.B;
@@ -1025,3 +1038,7 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
 }
 
 }  // namespace ibp
+
+extern "C" uint64_t ibp_testing_set_wait_limit_ns(uint64_t ns) {
+  return ibp::g_wait_limit_ns.exchange(ns, std::memory_order_relaxed);
+}

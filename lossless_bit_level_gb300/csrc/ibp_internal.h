@@ -113,5 +113,8 @@ int launch_query(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t 
 int launch_query_sync(const uint32_t *d_bitmask, const uint32_t *d_row_bits, int64_t n_rows,
                       int64_t raw_bytes, ibp_stats *h_out, cudaStream_t s);
 int launch_probe_read(const void *src, int64_t bytes, uint64_t *d_sink, cudaStream_t s);
+// Limit of each bounded wait inside the gather kernels launched from now on (ns of
+// global time): WAIT_TIMEOUT_NS unless ibp_testing_set_wait_limit_ns set another.
+uint64_t gather_wait_limit_ns();
 
 }  // namespace ibp

@@ -9,8 +9,8 @@ import pytest
 import lossless_bit_level_gb300 as ibp
 from lossless_bit_level_gb300 import build_lib
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
-                      "ibp.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "ibp.h")
 
 
 @pytest.fixture(scope="module")
@@ -19,8 +19,8 @@ def lib():
     return ibp.load()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(ibp_[a-z_]+)\s*\(", text)))
 
@@ -31,6 +31,20 @@ def test_every_declared_symbol_is_exported(lib):
     for name in names:
         assert hasattr(lib, name), name
     assert set(names) == set(ibp.SYMBOLS)
+    # every header of include/ is covered: the codec's and the testing hook's
+    headers = sorted(f for f in os.listdir(INCLUDE) if f.endswith(".h"))
+    assert headers == ["ibp.h", "ibp_testing.h"]
+    testing = declared_functions(os.path.join(INCLUDE, "ibp_testing.h"))
+    assert set(testing) == set(ibp.TESTING_SYMBOLS)
+    for name in testing:
+        assert hasattr(lib, name), name
+
+
+def test_testing_wait_limit_hook(lib):
+    """Host-side only: returns the previous setting, 0 meaning the default."""
+    assert ibp.testing_set_wait_limit_ns(5) == 0
+    assert ibp.testing_set_wait_limit_ns(0) == 5
+    assert ibp.testing_set_wait_limit_ns(0) == 0
 
 
 def test_size_queries(lib):
