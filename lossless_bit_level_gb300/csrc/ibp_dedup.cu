@@ -8,14 +8,18 @@
 // (Zipf-distributed lookups) name the same hot rows many times, and requests for a
 // row that is already in flight miss in L2 and cross again. Here every distinct row
 // is read and decoded once:
-//   1. dedup_insert_kernel: an open-addressing hash table in device memory maps each
+//   1. dedup_init_kernel clears the hash table and the counter and fills the compact
+//      row list with -1 (one launch);
+//   2. dedup_insert_kernel: an open-addressing hash table in device memory maps each
 //      row to the first position that inserts it (one 64-bit compare-and-swap holds
 //      row and position together, so the owner is fixed by a single atomic); the
-//      owners take consecutive slots of a compact row list (one atomic per warp);
-//   2. the slotted gather kernel decodes the compact list into a staging buffer (the
-//      list's unused tail is -1: units with nothing to do);
-//   3. dedup_scatter_kernel copies each staged row to every position that asked for
-//      it (a warp per output row, 16-byte vectors).
+//      owners take consecutive entries of the compact row list (one atomic per warp),
+//      each entry holding the row and its owner's output position;
+//   3. the slotted gather kernel decodes the compact list straight into the owners'
+//      output rows; it reads the list's length from device memory when it starts and
+//      stops there (the unused tail is -1 as well);
+//   4. dedup_scatter_kernel copies each owner's output row to every other position
+//      that asked for the same row (a warp per output row, 16-byte vectors).
 // An index outside [0, n_rows) records IBP_ERR_INDEX and leaves its output row
 // untouched, as in the plain gather.
 #include <algorithm>
@@ -34,9 +38,21 @@ __device__ __forceinline__ uint32_t table_slot(unsigned long long key, uint32_t 
 }
 
 __global__ void __launch_bounds__(DEDUP_THREADS)
+    dedup_init_kernel(unsigned long long *table, uint32_t cap, unsigned long long *count,
+                      int64_t *uidx, int64_t n_idx) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < (int64_t)cap || k < n_idx;
+       k += stride) {
+    if (k < (int64_t)cap) table[k] = 0ull;
+    if (k < n_idx) uidx[k] = -1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *count = 0ull;
+}
+
+__global__ void __launch_bounds__(DEDUP_THREADS)
     dedup_insert_kernel(const int64_t *__restrict__ idx, int64_t n_idx, int64_t n_rows,
                         unsigned long long *table, uint32_t mask, unsigned long long *count,
-                        int32_t *owner, int32_t *kslot, int64_t *uidx, int32_t *status) {
+                        int32_t *owner, int64_t *uidx, int32_t *status) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   bool inserted = false;
   int64_t r = -1;
@@ -68,7 +84,8 @@ __global__ void __launch_bounds__(DEDUP_THREADS)
       owner[i] = own;
     }
   }
-  // the rows first seen in this warp take consecutive slots of the compact list
+  // the rows first seen in this warp take consecutive entries of the compact list:
+  // the row in bits 0..39, the owner's output position in bits 40..63
   const uint32_t lanes = __ballot_sync(FULL, inserted);
   if (lanes) {
     const int lane = threadIdx.x & 31;
@@ -78,24 +95,23 @@ __global__ void __launch_bounds__(DEDUP_THREADS)
     base = __shfl_sync(FULL, base, leader);
     if (inserted) {
       const unsigned long long k = base + (unsigned long long)__popc(lanes & low_mask(lane));
-      uidx[k] = r;
-      kslot[i] = (int32_t)k;
+      uidx[k] = (i << 40) | r;
     }
   }
 }
 
+// Every position whose row another position owns gets a copy of the owner's output row
+// (which the gather wrote); owners and bad indices are left as they are.
 __global__ void __launch_bounds__(DEDUP_THREADS)
-    dedup_scatter_kernel(const uint4 *__restrict__ staged, const int32_t *__restrict__ owner,
-                         const int32_t *__restrict__ kslot, int64_t n_idx, int nvec_row,
+    dedup_scatter_kernel(const int32_t *__restrict__ owner, int64_t n_idx, int nvec_row,
                          uint4 *out) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (DEDUP_THREADS / 32);
   for (int64_t i = (int64_t)blockIdx.x * (DEDUP_THREADS / 32) + (threadIdx.x >> 5); i < n_idx;
        i += warps) {
     const int32_t o = __ldg(owner + i);
-    if (o < 0) continue;  // bad index: row untouched
-    const int64_t k = __ldg(kslot + o);
-    const uint4 *src = staged + k * nvec_row;
+    if (o < 0 || o == i) continue;  // bad index, or the row's owner (written by the gather)
+    const uint4 *src = out + (int64_t)o * nvec_row;
     uint4 *dst = out + i * nvec_row;
     for (int v = lane; v < nvec_row; v += 32) dst[v] = src[v];
   }
@@ -103,12 +119,12 @@ __global__ void __launch_bounds__(DEDUP_THREADS)
 
 struct DedupLayout {
   uint32_t cap;  // hash table slots (a power of two, at least 2 * n_idx)
-  size_t table, count, owner, kslot, uidx, staged, total;  // byte offsets
+  size_t table, count, owner, uidx, total;  // byte offsets
 };
 
 size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
-DedupLayout dedup_layout(int64_t n_idx, const RowGeom &g) {
+DedupLayout dedup_layout(int64_t n_idx, const RowGeom &) {
   DedupLayout L;
   uint32_t cap = 256;
   while ((int64_t)cap < 2 * n_idx) cap <<= 1;
@@ -116,10 +132,8 @@ DedupLayout dedup_layout(int64_t n_idx, const RowGeom &g) {
   L.table = 0;
   L.count = L.table + align16((size_t)cap * 8);
   L.owner = L.count + 16;
-  L.kslot = L.owner + align16((size_t)n_idx * 4);
-  L.uidx = L.kslot + align16((size_t)n_idx * 4);
-  L.staged = L.uidx + align16((size_t)n_idx * 8);
-  L.total = L.staged + (size_t)n_idx * (size_t)g.raw_bytes;
+  L.uidx = L.owner + align16((size_t)n_idx * 4);
+  L.total = L.uidx + align16((size_t)n_idx * 8);
   return L;
 }
 
@@ -141,27 +155,25 @@ int launch_gather_dedup(const void *slots, int64_t slot_bytes, int64_t n_rows, c
   auto *table = reinterpret_cast<unsigned long long *>(base + L.table);
   auto *count = reinterpret_cast<unsigned long long *>(base + L.count);
   auto *owner = reinterpret_cast<int32_t *>(base + L.owner);
-  auto *kslot = reinterpret_cast<int32_t *>(base + L.kslot);
   auto *uidx = reinterpret_cast<int64_t *>(base + L.uidx);
-  void *staged = base + L.staged;
-  // empty table and counter; the compact list's unused tail reads as -1
-  if (cudaMemsetAsync(table, 0, L.owner - L.table, s) != cudaSuccess ||
-      cudaMemsetAsync(uidx, 0xFF, (size_t)n_idx * 8, s) != cudaSuccess)
-    return IBP_ERR_CUDA;
+  const int init_grid = (int)std::min<int64_t>(
+      (std::max<int64_t>(L.cap, n_idx) + DEDUP_THREADS - 1) / DEDUP_THREADS,
+      (int64_t)dev.sm_count * 8);
+  dedup_init_kernel<<<init_grid, DEDUP_THREADS, 0, s>>>(table, L.cap, count, uidx, n_idx);
+  if (cudaGetLastError() != cudaSuccess) return IBP_ERR_CUDA;
   const int64_t blocks = (n_idx + DEDUP_THREADS - 1) / DEDUP_THREADS;
   dedup_insert_kernel<<<(unsigned)blocks, DEDUP_THREADS, 0, s>>>(
-      d_idx, n_idx, n_rows, table, L.cap - 1, count, owner, kslot, uidx, d_status);
+      d_idx, n_idx, n_rows, table, L.cap - 1, count, owner, uidx, d_status);
   if (cudaGetLastError() != cudaSuccess) return IBP_ERR_CUDA;
   if (int rc = launch_gather(slots, slot_bytes, nullptr, 0, n_rows, g, dtype, d_bitmask, d_meta,
-                             uidx, 0, n_idx, staged, d_status, slots_in_device_memory, s,
-                             nullptr, true))
+                             uidx, 0, n_idx, out, d_status, slots_in_device_memory, s, nullptr,
+                             true, true, count))
     return rc;
   const int64_t rows_per_cta = DEDUP_THREADS / 32;
   const int grid = (int)std::min<int64_t>((n_idx + rows_per_cta - 1) / rows_per_cta,
                                           (int64_t)dev.sm_count * 8);
-  dedup_scatter_kernel<<<grid, DEDUP_THREADS, 0, s>>>(
-      static_cast<const uint4 *>(staged), owner, kslot, n_idx, (int)(g.raw_bytes / 16),
-      static_cast<uint4 *>(out));
+  dedup_scatter_kernel<<<grid, DEDUP_THREADS, 0, s>>>(owner, n_idx, (int)(g.raw_bytes / 16),
+                                                      static_cast<uint4 *>(out));
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
 

@@ -73,6 +73,13 @@ struct GatherArgs {
   // a negative index is a unit with nothing to do, not an error (internal lists whose
   // tail is unused, e.g. the distinct rows of a de-duplicated gather)
   uint32_t skip_negative;
+  // index entries carry the output row of their unit in bits 40..63 and the row in
+  // bits 0..39 (the compact list of a de-duplicated gather: each distinct row is
+  // decoded straight into the first output row that asks for it)
+  uint32_t pos_in_index;
+  // number of index entries to gather, read on the device when the kernel starts
+  // (null: all n_idx); entries past it are not even looked at
+  const unsigned long long *idx_count;
   // limit of each bounded wait of the warp-specialised kernel, in ns of global time
   uint64_t wait_ns;
 };
@@ -105,8 +112,15 @@ __device__ __forceinline__ bool whole_slot(const GatherArgs &a, uint32_t shrink)
   return (int64_t)((min_bits + 31) >> 5) * 4 * 5 >= a.raw_bytes * 4;
 }
 
-__device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u) {
-  if (u >= a.n_units) return -1;
+// Units to gather: all of them, or those of the first *idx_count index entries.
+__device__ __forceinline__ int64_t units_of(const GatherArgs &a) {
+  if (!a.idx_count) return a.n_units;
+  const int64_t c = (int64_t)*a.idx_count * a.nseg;
+  return c < a.n_units ? c : a.n_units;
+}
+
+__device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u, int64_t n_units) {
+  if (u >= n_units) return -1;
   const int64_t i = a.nseg == 1 ? u : u / a.nseg;
   return a.idx ? __ldg(a.idx + i) : a.row0 + i;
 }
@@ -144,7 +158,8 @@ __device__ __forceinline__ EntrySpan load_span(const GatherArgs &a, int64_t r) {
 // plain slotted instantiation carries none of it.
 template <bool PACKED>
 __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, int64_t u,
-                                          int64_t r, bool leader, EntrySpan span) {
+                                          int64_t n_units, int64_t r, bool leader,
+                                          EntrySpan span) {
   Unit un;
   un.src = a.slots;
   un.out_word = 0;
@@ -155,7 +170,7 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   un.bmw = 0;
   un.echunk = 0;
   un.lead = 0;
-  if (u >= a.n_units) return un;
+  if (u >= n_units) return un;
   int64_t i = u;
   int s = 0;
   if (a.nseg != 1) {
@@ -164,6 +179,10 @@ __device__ __forceinline__ Unit plan_unit(const GatherArgs &a, uint32_t shrink, 
   }
   const int b0 = s * a.seg_blocks;
   const int nblk = min(a.seg_blocks, a.nb - b0);
+  if (a.pos_in_index && r >= 0) {
+    i = r >> 40;
+    r &= (int64_t(1) << 40) - 1;
+  }
   un.out_word = i * (int64_t)a.raw_words + (int64_t)b0 * a.lwb;
   if (r < 0 || r >= a.n_rows) {
     if (leader && !(a.skip_negative && r < 0)) report(a.status, IBP_ERR_INDEX);
@@ -396,13 +415,14 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
   const int buf_step = TPW * a.unit_bytes;
   StagedMeta *const metas = warp_meta + team;  // meta k at metas[k * TPW]
 
+  const int64_t n_units = units_of(a);
   int64_t base = warp_gid * TPW;  // first unit of this warp in the current iteration
-  if (base >= a.n_units) return;
+  if (base >= n_units) return;
   int64_t u_plan = base + team;  // next unit this team plans
-  int64_t r_plan = load_index(a, u_plan);
+  int64_t r_plan = load_index(a, u_plan, n_units);
   // packed stores: the unit after next's index and the next unit's entry span are
   // loaded one step ahead, so neither dependent load waits in front of staging
-  int64_t r_next = PACKED ? load_index(a, u_plan + stride) : -1;
+  int64_t r_next = PACKED ? load_index(a, u_plan + stride, n_units) : -1;
   EntrySpan span_plan = PACKED ? load_span(a, r_plan) : EntrySpan{0, 0};
   int k_plan = 0;                // buffer it goes to
   uint32_t pend_bmw = 0;         // bitmask word loaded for the last planned unit,
@@ -413,12 +433,12 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     int64_t r_after;
     EntrySpan span_after{0, 0};
     if (PACKED) {
-      r_after = load_index(a, u_plan + 2 * stride);  // prefetch, two units ahead
+      r_after = load_index(a, u_plan + 2 * stride, n_units);  // prefetch, two units ahead
       span_after = load_span(a, r_next);            // the next unit's entry
     } else {
-      r_after = load_index(a, u_plan + stride);  // prefetch
+      r_after = load_index(a, u_plan + stride, n_units);  // prefetch
     }
-    const Unit un = plan_unit<PACKED>(a, shrink, u_plan, r_plan, leader, span_plan);
+    const Unit un = plan_unit<PACKED>(a, shrink, u_plan, n_units, r_plan, leader, span_plan);
     if (leader && pend_k >= 0) metas[pend_k * TPW].bmw = pend_bmw;
     pend_bmw = un.lsb == PARSE_HEADER ? __ldg(a.bitmask + (un.segp >> 5)) : 0u;
     pend_k = k_plan;
@@ -467,7 +487,7 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     decode_dispatch<TL, PACKED>(a, code, sruns, nr, un, bufs + k_dec * buf_step, tl);
     __syncwarp();
     base += stride;
-    if (base >= a.n_units) break;
+    if (base >= n_units) break;
     k_dec = k_dec + 1 == GATHER_NBUF ? 0 : k_dec + 1;
   }
   cp_async_wait<0>();
@@ -605,12 +625,13 @@ __device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64
   for (; k - lane < count; k += step) {
     const bool have = k < count;
     const int64_t r = r_next;
-    r_next = k + step < count ? load_index(a, u0 + k + step) : -1;  // prefetch
+    r_next = k + step < count ? load_index(a, u0 + k + step, a.n_units) : -1;  // prefetch
     bool ok = true;
     if (have) {
       const Unit un = (a.offsets || a.row_bits)
-                          ? plan_unit<true>(a, shrink, u0 + k, r, true, load_span(a, r))
-                          : plan_unit<false>(a, shrink, u0 + k, r, true, EntrySpan{0, 0});
+                          ? plan_unit<true>(a, shrink, u0 + k, a.n_units, r, true, load_span(a, r))
+                          : plan_unit<false>(a, shrink, u0 + k, a.n_units, r, true,
+                                             EntrySpan{0, 0});
       const int slot = (int)(k % PLAN_SLOTS);
       ok = mbar_wait(&freed[slot], (uint32_t)((k / PLAN_SLOTS) & 1) ^ 1u, abort, a.wait_ns);
       if (ok) {
@@ -723,12 +744,15 @@ __global__ void __launch_bounds__(WS_THREADS, 2) gather_ws_kernel(GatherArgs a) 
   __shared__ int abort_flag;
   __shared__ PlanSlot plans[PLAN_SLOTS];
   __shared__ uint64_t planned[PLAN_SLOTS], freed[PLAN_SLOTS];
-  const int64_t u0 = a.n_units * blockIdx.x / gridDim.x;
-  const int64_t count = a.n_units * (blockIdx.x + 1) / gridDim.x - u0;
+  // the CTAs split the units to gather evenly (with a device-side count, only those)
+  const int64_t n_units = units_of(a);
+  const int64_t u0 = n_units * blockIdx.x / gridDim.x;
+  const int64_t count = n_units * (blockIdx.x + 1) / gridDim.x - u0;
   const int warp = threadIdx.x >> 5;
   // planners fetch their first indices while the metadata load is in flight
   const int64_t k_first = 32 * (int64_t)warp + (threadIdx.x & 31);
-  const int64_t r_first = warp < WS_PLANNERS && k_first < count ? load_index(a, u0 + k_first) : -1;
+  const int64_t r_first =
+      warp < WS_PLANNERS && k_first < count ? load_index(a, u0 + k_first, a.n_units) : -1;
   const ibp_meta m = load_meta(a.meta);
   if (m.dtype != a.dtype || m.block_elems != a.block_elems) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, IBP_ERR_META);
@@ -874,7 +898,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
                   bool slots_in_device_memory, cudaStream_t s, const uint32_t *d_row_bits,
-                  bool skip_negative) {
+                  bool skip_negative, bool pos_in_index,
+                  const unsigned long long *d_idx_count) {
   if (n_idx == 0) return IBP_OK;
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
@@ -887,6 +912,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.row_bits = d_offsets ? nullptr : d_row_bits;
   a.span_align = slots_in_device_memory ? 16u : 128u;
   a.skip_negative = skip_negative ? 1u : 0u;
+  a.pos_in_index = pos_in_index ? 1u : 0u;
+  a.idx_count = d_idx_count;
   a.wait_ns = gather_wait_limit_ns();
   a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
   a.n_rows = n_rows;
@@ -938,6 +965,8 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
   a = GatherArgs{};
   a.span_align = 16u;
   a.skip_negative = 0u;
+  a.pos_in_index = 0u;
+  a.idx_count = nullptr;
   a.wait_ns = gather_wait_limit_ns();
   a.status = d_status;
   a.dtype = dtype;

@@ -64,12 +64,18 @@ int launch_compress_stream(const void *rows, int64_t n_rows, const RowGeom &g, u
 // device memory before the slot is read, and only that prefix is staged.
 // d_offsets non-null: a packed store (entry r at slots + d_offsets[r], packed_bytes
 // long in all); otherwise slot r at slots + r * slot_bytes.
+// skip_negative: a negative index is a unit with nothing to do, not an error.
+// pos_in_index (slotted stores only): index entries hold (output row << 40) | row.
+// d_idx_count (device memory, nullable): only the first *d_idx_count index entries
+// are gathered (read when the kernel starts).
 int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
                   uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
                   bool slots_in_device_memory, cudaStream_t s,
-                  const uint32_t *d_row_bits = nullptr, bool skip_negative = false);
+                  const uint32_t *d_row_bits = nullptr, bool skip_negative = false,
+                  bool pos_in_index = false,
+                  const unsigned long long *d_idx_count = nullptr);
 // De-duplicated slotted gather: every distinct row of d_idx is read and decoded
 // once (into d_scratch), then copied to each output position that asks for it.
 size_t dedup_scratch_bytes(int64_t n_idx, const RowGeom &g);

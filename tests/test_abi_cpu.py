@@ -150,11 +150,11 @@ def test_argument_errors_before_cuda(lib):
     assert lib.ibp_query_async(None, None, 0, 128, ibp.FP32, None, None) == ibp.ERR_ARG
     assert lib.ibp_query_async(None, None, 5, 128, 8, vp(16), None) == ibp.ERR_DTYPE
     assert ctypes.sizeof(ibp.Stats) == 40
-    # de-duplicated gather: scratch size query (table, index arrays, one staged row per
-    # index), limits, and an empty list as a no-op
+    # de-duplicated gather: scratch size query (a hash table of at least 16 bytes per
+    # index, then 4 + 8 bytes per index), limits, and an empty list as a no-op
     sz = ctypes.c_size_t(0)
     assert lib.ibp_gather_dedup_scratch_bytes(100_000, 128, ibp.FP32, 32, ctypes.byref(sz)) == ibp.OK
-    assert sz.value >= 100_000 * (512 + 16) + 2 * 100_000 * 8
+    assert sz.value == 262_144 * 8 + 16 + 100_000 * 4 + 100_000 * 8
     assert lib.ibp_gather_dedup_scratch_bytes(1 << 24, 128, ibp.FP32, 32, ctypes.byref(sz)) == \
         ibp.ERR_UNSUPPORTED
     assert lib.ibp_gather_dedup_scratch_bytes(10, 128, ibp.FP32, 32, None) == ibp.ERR_ARG
