@@ -6,20 +6,9 @@
 // per block, run on the GPU over zero-copy memory) and "System integration"
 // (fixed-size buffer per row, GPU bitmask of compressed rows).
 //
-// One warp encodes one row at a time; warps take rows grid-strided and stage the
-// next row with cp.async while encoding the current one. Per row:
-//   a. (staged) the raw row in shared memory, read once, also from host memory;
-//   b. match pass: each lane tests four consecutive lane words (one 16-byte shared
-//      load); a block's participation bit is the AND of its lanes' ballot bits;
-//      the compressed-block count gives the row's exact size and the
-//      raw-or-compressed decision;
-//   c. pack pass (compressed rows only): each lane extracts its four fields,
-//      concatenates them into one chunk, finds the chunk's stream position with a
-//      warp scan of chunk sizes and ORs its words into a shared-memory copy of the
-//      stream (only a chunk's first and last words can be shared with a
-//      neighbour, and OR makes the order irrelevant);
-//   d. the stream (or the raw row) is written to the slot with 128-bit stores, and
-//      the row's bitmask bit is set or cleared with one atomic (one writer per bit).
+// Rows of at most 2 KiB (four 512-byte steps): compress_groups_kernel below, a warp
+// per group of 32 consecutive rows held in registers. Longer rows:
+// compress_stream_kernel (ibp_compress_stream.cu), a warp per row in one pass.
 #include <algorithm>
 #include <atomic>
 
@@ -30,7 +19,6 @@ namespace ibp {
 namespace {
 
 constexpr int COMPRESS_MAX_WARPS = 8;
-constexpr int COMPRESS_SMEM_BUDGET = 200 * 1024;
 
 struct CompressArgs {
   const uint8_t *rows;
@@ -42,217 +30,11 @@ struct CompressArgs {
   int32_t *status;
   const ibp_meta *meta;
   uint32_t dtype, block_elems;
-  int lwb, lwb_shift, nb, raw_words;
-  int lwt;         // lane words of the last block (lwb, or fewer for a shorter tail)
-  int warps;
-  int warp_bytes;  // shared bytes per warp
-  int hdr_words;   // header words reserved per warp (multiple of 4)
+  int lwb, nb, raw_words;
+  int lwt;    // lane words of the last block (lwb, or fewer for a shorter tail)
+  int warps;  // warps per CTA
   int64_t raw_bytes;
 };
-
-// Encode one staged row. LWB = lane words per block (8, 16, 32 or 64). Lane l works
-// on lane words [128 i + 4 l, 128 i + 4 l + 4) of each 128-word span i; a block is
-// then a group of LWB/4 consecutive lanes of a span. A shorter last block covers
-// fewer lanes of its group; the lanes past the row's end vote "match" and so
-// leave the AND to the block's own lanes.
-template <int NR, int LWB>
-__device__ bool compress_row(const CompressArgs &a, const Code &code, const RegRuns<NR> &runs,
-                             const SharedRuns &sruns, int64_t r, const uint32_t *RAW,
-                             uint32_t *OUT, uint32_t *HDR) {
-  constexpr int GS = LWB / 4;  // lanes per block
-  constexpr int BPS = 32 / GS;  // blocks per span
-  const int lane = threadIdx.x & 31;
-  const int nvec = a.raw_words / 4;
-  const int nspan = (a.raw_words + 127) >> 7;
-  const uint4 *RAW4 = reinterpret_cast<const uint4 *>(RAW);
-
-  // b. participation bits: a block's bit is the AND of its lanes' ballot bits,
-  // folded with shifts; a span's BPS bits never straddle a header word.
-  uint32_t hacc = 0, cnt_all = 0, last_frag = 0;
-  int last_b0 = 0;
-  for (int i = 0; i < nspan; ++i) {
-    const int v = 32 * i + lane;
-    bool ok = true;
-    if (v < nvec) {
-      const uint4 x = RAW4[v];
-      ok = ((x.x & code.mask32) == code.bitval32) & ((x.y & code.mask32) == code.bitval32) &
-           ((x.z & code.mask32) == code.bitval32) & ((x.w & code.mask32) == code.bitval32);
-    }
-    uint32_t A = __ballot_sync(FULL, ok);
-#pragma unroll
-    for (int sft = 1; sft < GS; sft <<= 1) A &= A >> sft;  // bit GS*j: AND of group j
-    uint32_t frag = 0;
-#pragma unroll
-    for (int j = 0; j < BPS; ++j) frag |= ((A >> (GS * j)) & 1u) << j;
-    const int b0 = i * BPS;
-    if (b0 + BPS > a.nb) frag &= low_mask((uint32_t)(a.nb - b0));
-    hacc |= frag << (b0 & 31);
-    cnt_all += __popc(frag);
-    last_frag = frag;
-    last_b0 = b0;
-    if (((b0 + BPS) & 31) == 0 || b0 + BPS >= a.nb) {
-      if (lane == 0) HDR[b0 >> 5] = hacc;
-      hacc = 0;
-    }
-  }
-  const uint32_t fc = (uint32_t)code.fc;
-  const uint32_t shrink = 32u - fc;
-  // bits = nb + sum over blocks of lane words * (p ? fc : 32); every block has LWB
-  // lane words but the last, which has lwt
-  const uint32_t p_last = (last_frag >> (a.nb - 1 - last_b0)) & 1u;
-  const uint32_t total = (uint32_t)a.nb + 32u * (uint32_t)a.raw_words -
-                         shrink * ((uint32_t)LWB * cnt_all - (uint32_t)(LWB - a.lwt) * p_last);
-  const uint32_t sw = (total + 31) >> 5;
-  const bool comp = (int64_t)sw * 4 < a.raw_bytes;
-  if (a.row_bits && lane == 0) a.row_bits[r] = total;
-  __syncwarp();
-
-  uint4 *dst = reinterpret_cast<uint4 *>(a.slots + r * a.slot_bytes);
-  if (!comp) {
-    for (int v = lane; v < nvec; v += 32) dst[v] = RAW4[v];
-    return false;
-  }
-
-  // c. pack. The stream is assembled in OUT: zero it, put the header bits in, then
-  // every lane ORs its bits in (only a chunk's first and last words can be shared
-  // with a neighbour, and OR makes the order irrelevant).
-  const uint32_t nout = (sw + 3) & ~3u;
-  for (uint32_t v = lane; v < nout / 4; v += 32)
-    reinterpret_cast<uint4 *>(OUT)[v] = make_uint4(0u, 0u, 0u, 0u);
-  __syncwarp();
-  const uint32_t nhw = ((uint32_t)a.nb + 31) >> 5;
-  for (uint32_t q = lane; q < nhw; q += 32) OUT[q] = HDR[q];
-  __syncwarp();
-  uint32_t base = (uint32_t)a.nb;  // stream position of the current span
-  for (int i = 0; i < nspan; ++i) {
-    const int v = 32 * i + lane;
-    const bool in = v < nvec;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (in) x = RAW4[v];
-    const uint32_t blk = (uint32_t)(4 * v) / LWB;
-    const bool p = in && ((HDR[blk >> 5] >> (blk & 31)) & 1u);
-    const uint32_t F = in ? (p ? fc : 32u) : 0u;  // bits per lane word
-    // the lane's chunk: its four fields, lowest word first, as c0..c3 (4F <= 128 bits)
-    uint32_t c0, c1, c2, c3;
-    if (!p) {
-      c0 = x.x;
-      c1 = x.y;
-      c2 = x.z;
-      c3 = x.w;
-    } else if (F == 0) {
-      c0 = c1 = c2 = c3 = 0u;
-    } else {
-      const uint64_t f0 = extract<NR>(x.x, runs, sruns), f1 = extract<NR>(x.y, runs, sruns);
-      const uint64_t f2 = extract<NR>(x.z, runs, sruns), f3 = extract<NR>(x.w, runs, sruns);
-      const uint64_t lo = f0 | (f1 << F), hi = f2 | (f3 << F);  // 2F < 64 bits each
-      const uint64_t w01 = lo | (hi << (2 * F));
-      const uint64_t w23 = hi >> (64 - 2 * F);
-      c0 = (uint32_t)w01;
-      c1 = (uint32_t)(w01 >> 32);
-      c2 = (uint32_t)w23;
-      c3 = (uint32_t)(w23 >> 32);
-    }
-    const uint32_t T = 4 * F;  // chunk bits
-    // exclusive prefix of chunk sizes over the span's lanes
-    uint32_t incl = T;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const uint32_t pos = base + incl - T;
-    base += __shfl_sync(FULL, incl, 31);
-    if (T) {
-      const uint32_t sh = pos & 31u, q = pos >> 5;
-      const uint32_t nw = (sh + T + 31) >> 5;  // words touched (1..5)
-      const uint32_t W0 = c0 << sh;
-      const uint32_t W1 = __funnelshift_l(c0, c1, sh);
-      const uint32_t W2 = __funnelshift_l(c1, c2, sh);
-      const uint32_t W3 = __funnelshift_l(c2, c3, sh);
-      const uint32_t W4 = __funnelshift_l(c3, 0u, sh);
-      atomicOr(&OUT[q], W0);
-      if (nw > 1) atomicOr(&OUT[q + 1], W1);
-      if (nw > 2) atomicOr(&OUT[q + 2], W2);
-      if (nw > 3) atomicOr(&OUT[q + 3], W3);
-      if (nw > 4) atomicOr(&OUT[q + 4], W4);
-    }
-  }
-  __syncwarp();
-  // d. store the stream (tail of the last 16-byte vector is zero)
-  for (uint32_t v = lane; v < nout / 4; v += 32) dst[v] = reinterpret_cast<const uint4 *>(OUT)[v];
-  return true;
-}
-
-// Stage row r into RAW with 16-byte cp.async copies (one commit group).
-__device__ __forceinline__ void prefetch_row(const CompressArgs &a, int64_t r, uint32_t *RAW) {
-  if (r < a.n_rows) {
-    const uint8_t *src = a.rows + r * a.raw_bytes;
-    const int nvec = a.raw_words / 4;
-    for (int v = threadIdx.x & 31; v < nvec; v += 32)
-      cp_async16(reinterpret_cast<uint8_t *>(RAW) + 16 * v, src + 16 * v);
-  }
-  cp_async_commit();
-}
-
-// Warps take rows grid-strided (row warp_gid, then + total warps, ...) and stage each
-// one's next row while encoding the current. Every row sets or clears its own bit of
-// the bitmask with one atomic (each bit has exactly one writer, so the final words
-// do not depend on the order); warp 0 of CTA 0 clears the bits past n_rows.
-template <int NR, int LWB>
-__device__ void compress_body(const CompressArgs &a, const Code &code, const SharedRuns &sruns,
-                              uint8_t *smem) {
-  const RegRuns<NR> runs = load_runs<NR>(sruns);
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  uint8_t *mine = smem + (size_t)warp * a.warp_bytes;
-  uint32_t *HDR = reinterpret_cast<uint32_t *>(mine);
-  uint32_t *RAW0 = HDR + a.hdr_words;
-  uint32_t *OUT = RAW0 + 2 * a.raw_words;
-  const int64_t first = (int64_t)blockIdx.x * a.warps + warp;
-  const int64_t step = (int64_t)gridDim.x * a.warps;
-  if (first == 0 && lane == 0 && (a.n_rows & 31))
-    atomicAnd(&a.bitmask[a.n_rows >> 5], low_mask((uint32_t)(a.n_rows & 31)));
-  if (first >= a.n_rows) return;
-  prefetch_row(a, first, RAW0);
-  int b = 0;
-  for (int64_t r = first; r < a.n_rows; r += step) {
-    prefetch_row(a, r + step, RAW0 + (b ^ 1) * a.raw_words);  // no-op past the end
-    cp_async_wait<1>();
-    __syncwarp();
-    const bool comp =
-        compress_row<NR, LWB>(a, code, runs, sruns, r, RAW0 + b * a.raw_words, OUT, HDR);
-    if (lane == 0) {
-      const uint32_t bit = 1u << (r & 31);
-      if (comp) atomicOr(&a.bitmask[r >> 5], bit);
-      else atomicAnd(&a.bitmask[r >> 5], ~bit);
-    }
-    __syncwarp();
-    b ^= 1;
-  }
-  cp_async_wait<0>();
-}
-
-template <int LWB>
-__global__ void __launch_bounds__(COMPRESS_MAX_WARPS * 32) compress_kernel(CompressArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ SharedRuns sruns;
-  const ibp_meta m = load_meta(a.meta);
-  if (m.dtype != a.dtype || m.block_elems != a.block_elems) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, IBP_ERR_META);
-    return;
-  }
-  const Code code = make_code(m);
-  if (threadIdx.x == 0) make_runs(~code.mask32, sruns);
-  __syncthreads();
-  switch (sruns.n) {
-    case 0: compress_body<0, LWB>(a, code, sruns, smem); break;
-    case 1: compress_body<1, LWB>(a, code, sruns, smem); break;
-    case 2: compress_body<2, LWB>(a, code, sruns, smem); break;
-    case 3: compress_body<3, LWB>(a, code, sruns, smem); break;
-    case 4: compress_body<4, LWB>(a, code, sruns, smem); break;
-    default: compress_body<-1, LWB>(a, code, sruns, smem); break;
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Rows of at most 4 x 128 lane words (2 KiB): a warp owns groups of 32 consecutive
@@ -475,33 +257,6 @@ int launch_groups_lwb(const CompressArgs &a, const DeviceInfo &dev, int nspan, c
   return launch_groups<LWB, 4>(a, dev, s);
 }
 
-int ilog2(int x) {
-  int s = 0;
-  while ((1 << s) < x) ++s;
-  return s;
-}
-
-template <int LWB>
-int launch_lwb(const CompressArgs &a, const DeviceInfo &dev, int limit, size_t smem,
-               cudaStream_t s) {
-  static std::atomic<int> configured[64];  // the attribute is set once per device
-  if (dev.device >= 64 || !configured[dev.device].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(compress_kernel<LWB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             limit) != cudaSuccess)
-      return IBP_ERR_CUDA;
-    if (dev.device < 64) configured[dev.device].store(1, std::memory_order_release);
-  }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_kernel<LWB>, a.warps * 32,
-                                                    smem) != cudaSuccess ||
-      per_sm < 1)
-    return IBP_ERR_CUDA;
-  const int64_t want = (a.n_rows + a.warps - 1) / a.warps;
-  const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
-  compress_kernel<LWB><<<grid, a.warps * 32, smem, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
-}
-
 }  // namespace
 
 int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
@@ -522,20 +277,13 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
   a.dtype = dtype;
   a.block_elems = (uint32_t)g.B;
   a.lwb = g.lwb;
-  a.lwb_shift = ilog2(g.lwb);
   a.nb = g.nb;
   a.raw_words = g.raw_words;
   a.lwt = g.lwt;
   a.raw_bytes = g.raw_bytes;
-  a.hdr_words = (((g.nb + 31) / 32) + 3) & ~3;
-  // header + two staged raw rows + stream (never longer than the raw row when kept)
-  a.warp_bytes = 4 * (a.hdr_words + 3 * g.raw_words);
-  const int limit = std::min(COMPRESS_SMEM_BUDGET, dev.max_smem_optin - 2048);
-  a.warps = std::min(COMPRESS_MAX_WARPS, limit / a.warp_bytes);
-  if (a.warps < 1) return IBP_ERR_UNSUPPORTED;
+  a.warps = COMPRESS_MAX_WARPS;
   const int nspan = (g.raw_words + 127) / 128;
   if (nspan <= 4) {  // short rows: the register path
-    a.warps = COMPRESS_MAX_WARPS;
     const int ns = nspan <= 1 ? 1 : (nspan <= 2 ? 2 : 4);
     switch (g.lwb) {
       case 8: return launch_groups_lwb<8>(a, dev, ns, s);
@@ -544,18 +292,9 @@ int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t
       default: return launch_groups_lwb<64>(a, dev, ns, s);
     }
   }
-  if (g.raw_bytes <= compress_stream_max_bytes()) {  // long rows: one warp per row, one pass
-    const int rc = launch_compress_stream(rows, n_rows, g, dtype, d_meta, slots, slot_bytes,
-                                          d_bitmask, d_row_bits, d_status, dev, s);
-    if (rc != IBP_ERR_UNSUPPORTED) return rc;
-  }
-  const size_t smem = (size_t)a.warps * a.warp_bytes;
-  switch (g.lwb) {
-    case 8: return launch_lwb<8>(a, dev, limit, smem, s);
-    case 16: return launch_lwb<16>(a, dev, limit, smem, s);
-    case 32: return launch_lwb<32>(a, dev, limit, smem, s);
-    default: return launch_lwb<64>(a, dev, limit, smem, s);
-  }
+  // long rows: one warp per row, one pass
+  return launch_compress_stream(rows, n_rows, g, dtype, d_meta, slots, slot_bytes, d_bitmask,
+                                d_row_bits, d_status, dev, s);
 }
 
 }  // namespace ibp

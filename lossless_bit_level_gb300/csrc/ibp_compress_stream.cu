@@ -1,5 +1,5 @@
-// Compression of long rows (over 2 KiB, up to 64 KiB) for sm_103a: one warp per row,
-// one pass over the row, no CTA barriers.
+// Compression of long rows (over 2 KiB, up to the longest row the library accepts)
+// for sm_103a: one warp per row, one pass over the row, no CTA barriers.
 //
 // "Reducing the GPU Memory Bottleneck with Lossless Compression for ML --
 // Extended", technical summary, "Core algorithm" (compression: per-block match
@@ -31,7 +31,9 @@
 //     index of the stream word they start;
 //   * the complete 16-byte stream vectors go out to the slot, each lane's words
 //     funnel-shifted from two payload words. The vectors that hold participation
-//     bits are kept back and written last, with the bits ORed in.
+//     bits are written last: those below the first payload word from the warp's copy
+//     of the bits, the one shared with the payload (at most one) kept back from the
+//     flush and written with the bits ORed in.
 // The row's size is nb plus the payload bits; a row whose stream would not be
 // shorter than the raw row is rewritten raw from the source (only rows that matched
 // somewhere and still save nothing).
@@ -48,10 +50,7 @@ constexpr int SW_THREADS = 256;
 constexpr int SW_WARPS = SW_THREADS / 32;
 constexpr int RING_WORDS = 256;   // payload words per warp; a step adds at most 128
 constexpr int RING_VECS = RING_WORDS / 4;
-constexpr int HEAD_VECS = 16;     // vectors holding participation bits: nb <= 2048
-constexpr int HDR_WORDS = 64;     // participation-bit words: nb <= 2048
 constexpr int PF = 8;             // staging slots per warp: PF - 1 steps in flight
-constexpr int64_t STREAM_MAX_BYTES = 64 * 1024;
 
 struct StreamArgs {
   const uint8_t *rows;
@@ -64,16 +63,37 @@ struct StreamArgs {
   const ibp_meta *meta;
   uint32_t dtype, block_elems;
   int nb, raw_words;
+  int hdr_words;  // participation-bit words per warp: ceil(nb / 32) rounded up to 4
   int64_t raw_bytes;
 };
 
-// Per-warp shared memory (dynamic; every part 16-byte aligned).
-struct __align__(16) WarpRing {
+// Per-warp shared memory (dynamic; every part 16-byte aligned): the staging slots, the
+// payload ring, the one vector shared by participation bits and payload, then the
+// row's participation bits (hdr_words words, a multiple of 4).
+struct __align__(16) WarpFixed {
   uint4 stage[PF][32];  // the row's next steps, one 16-byte vector per lane (cp.async)
   uint32_t ring[RING_WORDS];
-  uint4 head[HEAD_VECS];
-  uint32_t hdr[HDR_WORDS];
+  uint4 head;
 };
+
+// The warp's part of shared memory: one base address, the parts at constant offsets.
+struct WarpRing {
+  uint8_t *base;
+  __device__ __forceinline__ uint4 (*stage() const)[32] {
+    return reinterpret_cast<WarpFixed *>(base)->stage;
+  }
+  __device__ __forceinline__ uint32_t *ring() const {
+    return reinterpret_cast<WarpFixed *>(base)->ring;
+  }
+  __device__ __forceinline__ uint4 *head() const { return &reinterpret_cast<WarpFixed *>(base)->head; }
+  __device__ __forceinline__ uint32_t *hdr() const {
+    return reinterpret_cast<uint32_t *>(base + sizeof(WarpFixed));
+  }
+};
+
+__host__ __device__ inline size_t warp_ring_bytes(int hdr_words) {
+  return sizeof(WarpFixed) + 4 * (size_t)hdr_words;
+}
 
 __device__ __forceinline__ uint4 load_vec(const uint4 *p) {
   uint4 v;
@@ -203,13 +223,13 @@ __device__ __forceinline__ void pack_full(const Code &code, const Runs4 &runs,
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const uint32_t c = pack3(extract4_mul(xg[g], runs), pl);
-      if ((uint32_t)lane < fc) w.ring[wq & (RING_WORDS - 1)] = c;
+      if ((uint32_t)lane < fc) w.ring()[wq & (RING_WORDS - 1)] = c;
       wq += fc;
     }
   } else if (frag == 0u) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      w.ring[wq & (RING_WORDS - 1)] = xg[g];
+      w.ring()[wq & (RING_WORDS - 1)] = xg[g];
       wq += 32u;
     }
   } else {
@@ -220,7 +240,7 @@ __device__ __forceinline__ void pack_full(const Code &code, const Runs4 &runs,
       if (FAST) c = pack3(extract4_mul(xg[g], runs), pl);
       else if (fc != 0u) c = pack_word<32>(extract4(xg[g], runs, sruns), fc, pl);
       const uint32_t n = p ? fc : 32u;
-      if ((uint32_t)lane < n) w.ring[wq & (RING_WORDS - 1)] = p ? c : xg[g];
+      if ((uint32_t)lane < n) w.ring()[wq & (RING_WORDS - 1)] = p ? c : xg[g];
       wq += n;
     }
   }
@@ -262,7 +282,7 @@ __device__ __forceinline__ void pack_step(const Code &code, const Runs4 &runs,
     const uint32_t mb = __popc(segp & low_mask((uint32_t)seg));
     const uint32_t before = (mb * (uint32_t)SEG * fc + ((uint32_t)seg - mb) * 32u * SEG) >> 5;
     if ((uint32_t)kk < words)
-      w.ring[(wq0 + (bits >> 5) + before + (uint32_t)kk) & (RING_WORDS - 1)] = out;
+      w.ring()[(wq0 + (bits >> 5) + before + (uint32_t)kk) & (RING_WORDS - 1)] = out;
     for (int s2 = 0; s2 * SEG < nvg; ++s2) {
       const uint32_t n2 = (uint32_t)min(SEG, nvg - s2 * SEG);
       bits += ((segp >> s2) & 1u) ? n2 * fc : 32u * n2;
@@ -271,41 +291,44 @@ __device__ __forceinline__ void pack_step(const Code &code, const Runs4 &runs,
   sp.pb += bits;
 }
 
-// The complete stream vectors [sp.fv, fe) to the slot: stream word q is payload word
-// q - qh (ring index q) moved up by s0 bits over the top of the word before it (ring
-// words below qh are zero: those bits are participation bits, ORed in at the end).
-// Vectors holding participation bits go to the warp's head buffer; only vectors
-// below nvec are written (a stream that reaches further belongs to a row stored raw).
+// The complete stream vectors [sp.fv, fe) to the slot (sp.fv starts at the vector of
+// stream word qh, the first with payload bits; the ones before hold participation
+// bits only and are written at the row's end): stream word q is payload word q - qh
+// (ring index q) moved up by s0 bits over the top of the word before it (ring words
+// below qh read as zero: those bits are participation bits, ORed in at the end). The
+// vector below hv that also holds participation bits goes to the warp's head buffer;
+// only vectors below nvec are written (a stream that reaches further belongs to a row
+// stored raw).
 __device__ __forceinline__ void flush(WarpRing &w, uint4 *dst, StreamPos &sp, int fe,
                                       uint32_t s0, int hv, int nvec, int lane) {
-  const uint4 *ring4 = reinterpret_cast<const uint4 *>(w.ring);
+  const uint4 *ring4 = reinterpret_cast<const uint4 *>(w.ring());
   for (int v = sp.fv + lane; v < fe; v += 32) {
     const uint4 cur = ring4[v & (RING_VECS - 1)];
-    const uint32_t prev = w.ring[(4 * v - 1) & (RING_WORDS - 1)];
+    const uint32_t prev = w.ring()[(4 * v - 1) & (RING_WORDS - 1)];
     const uint4 val = make_uint4(__funnelshift_l(prev, cur.x, s0), __funnelshift_l(cur.x, cur.y, s0),
                                  __funnelshift_l(cur.y, cur.z, s0), __funnelshift_l(cur.z, cur.w, s0));
-    if (v < hv) w.head[v] = val;
+    if (v < hv) *w.head() = val;
     else if (v < nvec) dst[v] = val;
   }
   if (fe > sp.fv) sp.fv = fe;
 }
 
-// flush for the vectors a step completes: at most 48 (a step adds at most 128
-// payload words; the first one also completes the up to 64 words of participation
-// bits before them), so at most two per lane.
+// flush for the vectors a step completes: at most 33 (a step adds at most 128
+// payload words, and up to three words before them were complete already), so at
+// most two per lane.
 __device__ __forceinline__ void flush_step(WarpRing &w, uint4 *dst, StreamPos &sp, int fe,
                                            uint32_t s0, int hv, int nvec, int lane) {
-  const uint4 *ring4 = reinterpret_cast<const uint4 *>(w.ring);
+  const uint4 *ring4 = reinterpret_cast<const uint4 *>(w.ring());
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int v = sp.fv + lane + 32 * i;
     if (v < fe) {
       const uint4 cur = ring4[v & (RING_VECS - 1)];
-      const uint32_t prev = w.ring[(4 * v - 1) & (RING_WORDS - 1)];
+      const uint32_t prev = w.ring()[(4 * v - 1) & (RING_WORDS - 1)];
       const uint4 val =
           make_uint4(__funnelshift_l(prev, cur.x, s0), __funnelshift_l(cur.x, cur.y, s0),
                      __funnelshift_l(cur.y, cur.z, s0), __funnelshift_l(cur.z, cur.w, s0));
-      if (v < hv) w.head[v] = val;
+      if (v < hv) *w.head() = val;
       else if (v < nvec) dst[v] = val;
     }
   }
@@ -340,17 +363,21 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
   const int64_t nwarps = (int64_t)gridDim.x * SW_WARPS;
   if (blockIdx.x == 0 && threadIdx.x == 0 && (a.n_rows & 31))
     atomicAnd(&a.bitmask[a.n_rows >> 5], low_mask((uint32_t)(a.n_rows & 31)));
+  // every row rewrites each participation-bit word below ceil(nb / 32); the words
+  // past it up to the vector boundary are read at the row's end and stay zero
+  for (int q = lane; q < a.hdr_words; q += 32) w.hdr()[q] = 0u;
   for (int64_t r = gw; r < a.n_rows; r += nwarps) {
     const uint4 *src = reinterpret_cast<const uint4 *>(a.rows + r * a.raw_bytes);
     uint4 *dst = reinterpret_cast<uint4 *>(a.slots + r * a.slot_bytes);
-    // ring words below the first payload word stand for participation bits, and the
-    // flush of vector 0 reads the ring's last word as the word before it: zero all
-    reinterpret_cast<uint4 *>(w.ring)[lane] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4 *>(w.ring)[lane + 32] = make_uint4(0u, 0u, 0u, 0u);
-    w.hdr[lane] = 0u;
-    w.hdr[lane + 32] = 0u;
+    // the first flushed vector (that of stream word qh) reads the ring words from the
+    // one before it up to qh - 1: they stand for participation bits and read as zero;
+    // every later word the flush reads is written by this row first
+    if (lane < 4) {
+      const int q = 4 * (qh >> 2) - 1 + lane;
+      if (q < qh) w.ring()[q & (RING_WORDS - 1)] = 0u;
+    }
     __syncwarp();
-    StreamPos sp{0u, 0};
+    StreamPos sp{0u, qh >> 2};
     bool streaming = false;  // false: no block has matched yet, vectors copied raw
     int k_seen = 0;          // steps whose match bits are in the header
     uint32_t hcur = 0;       // participation-bit word being filled
@@ -358,7 +385,7 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
     for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
       for (int i = 0; i < PF - 1; ++i) {
-        if (32 * i + lane < nvec) cp_async16(&w.stage[i][lane], src + 32 * i + lane);
+        if (32 * i + lane < nvec) cp_async16(&w.stage()[i][lane], src + 32 * i + lane);
         cp_async_commit();
       }
       bool restart = false;
@@ -366,13 +393,13 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
       for (int k = 0; k < nsteps; ++k) {
         {
           const int kn = k + PF - 1, vn = 32 * kn + lane;  // into the slot step k - 1 used
-          if (vn < nvec) cp_async16(&w.stage[kn % PF][lane], src + vn);
+          if (vn < nvec) cp_async16(&w.stage()[kn % PF][lane], src + vn);
           cp_async_commit();
         }
         cp_async_wait<PF - 1>();  // this lane's copy of step k has landed
         __syncwarp();             // ... and every other lane's
         const int nw_step = min(128, a.raw_words - 128 * k);
-        uint32_t *S = reinterpret_cast<uint32_t *>(&w.stage[k % PF][0]);
+        uint32_t *S = reinterpret_cast<uint32_t *>(&w.stage()[k % PF][0]);
         uint32_t xg[4];
         if (nw_step == 128) {
 #pragma unroll
@@ -386,7 +413,7 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
         if (k >= k_seen) {
           hcur |= frag << (b0 & 31);
           if (((b0 + BPS) & 31) == 0 || k == nsteps - 1) {
-            if (lane == 0) w.hdr[b0 >> 5] = hcur;
+            if (lane == 0) w.hdr()[b0 >> 5] = hcur;
             hcur = 0;
           }
           k_seen = k + 1;
@@ -394,7 +421,7 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
         if (!streaming) {
           if (frag == 0) {  // still no match in the row: copy the vector raw
             const int v = 32 * k + lane;
-            if (v < nvec) dst[v] = w.stage[k % PF][lane];
+            if (v < nvec) dst[v] = w.stage()[k % PF][lane];
             __syncwarp();  // the others read this slot; the next step's copies reuse it
             continue;
           }
@@ -423,15 +450,20 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
     if (comp) {
       // payload words past the last one read as zeros, then the rest of the stream
       if (lane < 8)
-        w.ring[((uint32_t)qh + ((sp.pb + 31) >> 5) + (uint32_t)lane) & (RING_WORDS - 1)] = 0u;
+        w.ring()[((uint32_t)qh + ((sp.pb + 31) >> 5) + (uint32_t)lane) & (RING_WORDS - 1)] = 0u;
       __syncwarp();
       flush(w, dst, sp, (int)((sw + 3) >> 2), s0, hv, nvec, lane);
       __syncwarp();
-      // the vectors holding participation bits, with the bits ORed in
-      if (lane < hv) {
-        const uint4 h = w.head[lane];
-        dst[lane] = make_uint4(h.x | w.hdr[4 * lane], h.y | w.hdr[4 * lane + 1],
-                               h.z | w.hdr[4 * lane + 2], h.w | w.hdr[4 * lane + 3]);
+      // the vectors holding participation bits: those before the first payload word
+      // are the bits alone, the one shared with the payload gets them ORed in
+      const uint4 *hdr4 = reinterpret_cast<const uint4 *>(w.hdr());
+      for (int v = lane; v < hv; v += 32) {
+        uint4 h = hdr4[v];
+        if (v >= (qh >> 2)) {
+          const uint4 p = *w.head();
+          h = make_uint4(h.x | p.x, h.y | p.y, h.z | p.z, h.w | p.w);
+        }
+        dst[v] = h;
       }
     } else if (streaming) {  // matched somewhere but saves nothing: store the row raw
       for (int v = lane; v < nvec; v += 32) dst[v] = load_vec(src + v);
@@ -447,7 +479,7 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
 }
 
 template <int LWB>
-__global__ void __launch_bounds__(SW_THREADS, 4) compress_stream_kernel(StreamArgs a) {
+__global__ void __launch_bounds__(SW_THREADS, 3) compress_stream_kernel(StreamArgs a) {
   extern __shared__ __align__(16) uint8_t smem_stream[];
   __shared__ SharedRuns sruns;
   const ibp_meta m = load_meta(a.meta);
@@ -458,7 +490,8 @@ __global__ void __launch_bounds__(SW_THREADS, 4) compress_stream_kernel(StreamAr
   const Code code = make_code(m);
   if (threadIdx.x == 0) make_runs(~code.mask32, sruns);
   __syncthreads();
-  WarpRing &w = reinterpret_cast<WarpRing *>(smem_stream)[threadIdx.x >> 5];
+  WarpRing w;
+  w.base = smem_stream + (threadIdx.x >> 5) * warp_ring_bytes(a.hdr_words);
   // the common masks (fields of at least 16 bits, at most four runs of kept bits, bit
   // 0 kept) get their own copy of the row loop; only one copy runs in a launch
   if (code.fc >= 16 && sruns.n <= 4 && sruns.n > 0 && sruns.sh[0] == 0u)
@@ -469,19 +502,22 @@ __global__ void __launch_bounds__(SW_THREADS, 4) compress_stream_kernel(StreamAr
 
 template <int LWB>
 int launch_stream(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t s) {
-  const size_t smem = sizeof(WarpRing) * SW_WARPS;
-  static std::atomic<int> occupancy[64];  // resident CTAs per SM, looked up once per device
-  int per_sm = dev.device < 64 ? occupancy[dev.device].load(std::memory_order_acquire) : 0;
-  if (per_sm == 0) {
+  // the largest dynamic size, leaving room for the kernel's static shared memory
+  const int dyn_max = dev.max_smem_optin - (int)sizeof(SharedRuns) - 1024;
+  const size_t smem = warp_ring_bytes(a.hdr_words) * SW_WARPS;
+  if (smem > (size_t)dyn_max) return IBP_ERR_UNSUPPORTED;
+  static std::atomic<int> configured[64];  // the attribute is set once per device
+  if (dev.device >= 64 || !configured[dev.device].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(compress_stream_kernel<LWB>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) != cudaSuccess)
       return IBP_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_stream_kernel<LWB>,
-                                                      SW_THREADS, smem) != cudaSuccess ||
-        per_sm < 1)
-      return IBP_ERR_CUDA;
-    if (dev.device < 64) occupancy[dev.device].store(per_sm, std::memory_order_release);
+    if (dev.device < 64) configured[dev.device].store(1, std::memory_order_release);
   }
+  int per_sm = 0;  // 80 registers a thread: three CTAs per SM
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compress_stream_kernel<LWB>,
+                                                    SW_THREADS, smem) != cudaSuccess ||
+      per_sm < 1)
+    return IBP_ERR_CUDA;
   const int64_t want = (a.n_rows + SW_WARPS - 1) / SW_WARPS;
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
   compress_stream_kernel<LWB><<<grid, SW_THREADS, smem, s>>>(a);
@@ -490,14 +526,11 @@ int launch_stream(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t s) {
 
 }  // namespace
 
-int64_t compress_stream_max_bytes() { return STREAM_MAX_BYTES; }
-
 int launch_compress_stream(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                            const ibp_meta *d_meta, void *slots, int64_t slot_bytes,
                            uint32_t *d_bitmask, uint32_t *d_row_bits, int32_t *d_status,
                            const DeviceInfo &dev, cudaStream_t s) {
-  if (g.raw_words % 4 != 0 || g.raw_bytes > STREAM_MAX_BYTES || g.nb > 32 * HDR_WORDS)
-    return IBP_ERR_UNSUPPORTED;
+  if (g.raw_words % 4 != 0) return IBP_ERR_UNSUPPORTED;
   StreamArgs a;
   a.rows = static_cast<const uint8_t *>(rows);
   a.n_rows = n_rows;
@@ -512,6 +545,7 @@ int launch_compress_stream(const void *rows, int64_t n_rows, const RowGeom &g, u
   a.nb = g.nb;
   a.raw_words = g.raw_words;
   a.raw_bytes = g.raw_bytes;
+  a.hdr_words = ((g.nb + 31) / 32 + 3) & ~3;
   switch (g.lwb) {
     case 8: return launch_stream<8>(a, dev, s);
     case 16: return launch_stream<16>(a, dev, s);

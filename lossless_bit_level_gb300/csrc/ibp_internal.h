@@ -50,9 +50,8 @@ size_t select_scratch_bytes();
 int launch_compress(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                     const ibp_meta *d_meta, void *slots, int64_t slot_bytes, uint32_t *d_bitmask,
                     uint32_t *d_row_bits, int32_t *d_status, cudaStream_t s);
-// Rows of 2 KiB to compress_stream_max_bytes(): one warp per row in one pass (the
-// caller has checked the arguments and looked up the device).
-int64_t compress_stream_max_bytes();
+// Rows over 2 KiB: one warp per row in one pass (the caller has checked the arguments
+// and looked up the device).
 int launch_compress_stream(const void *rows, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                            const ibp_meta *d_meta, void *slots, int64_t slot_bytes,
                            uint32_t *d_bitmask, uint32_t *d_row_bits, int32_t *d_status,

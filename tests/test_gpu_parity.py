@@ -111,6 +111,27 @@ def test_shapes_and_ragged_tails(dtype_code, np_dt, B, L):
     full_check(words, dtype_code, 0.9, B, idx)
 
 
+@pytest.mark.parametrize("dtype_code,np_dt,B,L,n", [
+    (FP32, np.uint32, 32, 20480, 40),       # 80 KiB rows
+    (BF16, np.uint16, 64, 65544, 12),       # 128 KiB rows, an 8-element last block
+    (W8, np.uint8, 32, 1 << 20, 3),         # 1 MiB rows of 8-bit words
+    (FP32, np.uint32, 64, 1 << 20, 2)])     # 4 MiB rows: the longest row accepted
+def test_very_long_rows(dtype_code, np_dt, B, L, n):
+    """Rows far past 64 KiB (participation bits of up to 32,768 blocks, most of them in
+    vectors before the first payload word), host and HBM slots, compressed rows and
+    raw ones (some rows are made incompressible), gathers of every row and repeats."""
+    g = np.random.default_rng(L + B)
+    w = 8 * np.dtype(np_dt).itemsize
+    base = g.integers(0, 1 << w, size=(n, L), dtype=np.uint64)
+    hi = np.uint64(((1 << w) - 1) ^ ((1 << (w // 2 + 1)) - 1))
+    flip = g.random(size=(n, L)) < 0.0005
+    words = np.where(flip, base, (base & ~hi) | (np.uint64(0x3F1E3F1E) & hi)).astype(np_dt)
+    words[-1] = base[-1].astype(np_dt)  # one row of random words: stored raw
+    idx = np.concatenate([np.arange(n), np.arange(n)[::-1], [0]]).astype(np.int64)
+    for where in ("device", "host"):
+        full_check(words, dtype_code, 0.9, B, idx, where=where)
+
+
 @pytest.mark.parametrize("mask,bitval", [
     (0x00000000, 0x00000000),          # empty mask: every row raw
     (0xFFFFFFFF, 0x00000000),          # full mask: matching blocks are 0 bits
