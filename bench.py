@@ -86,6 +86,11 @@ WORKLOADS = {
 }
 
 
+# the legs that follow the timed gather, in the order they run
+LEGS = ("hbm", "e2e", "stages", "dedup", "select", "packed", "positions", "offload", "dlrm26",
+        "configs")
+
+
 # ----------------------------------------------------------------------------- utilities
 
 def env_rank():
@@ -1270,6 +1275,9 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gnn_dense")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the HBM-resident and e2e legs")
+    ap.add_argument("--legs", default=None,
+                    help="run only these of the legs after the timed gather (comma-separated: "
+                         f"{','.join(LEGS)}); default: all of them unless --quick")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the pass over every configuration (default workload only)")
     ap.add_argument("--residency", choices=["host", "device"], default=None,
@@ -1391,88 +1399,101 @@ def main():
                     "peak_source": f"{hbm_peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg}
 
+    legs = None if args.legs is None else set(args.legs.split(","))
+    if legs is not None and not legs <= set(LEGS):
+        raise SystemExit(f"unknown legs: {sorted(legs - set(LEGS))}")
+
+    def want(leg):
+        return (not args.quick) if legs is None else leg in legs
+
     extra = {}
-    if not args.quick:
-        # HBM-resident gather of the same store
-        if residency == "host":
-            dstore = Store.__new__(Store)
-            dstore.__dict__.update(store.__dict__)
-            dstore.slots = store.slots.to(dev)
-            dstore.residency = "device"
-            per_step_h, clk_h = timed_gather(dstore, batches, out, max(50, steps // 4), warmup,
-                                             flush, barrier)
-            th = float(np.mean(per_step_h))
-            alg = wl["batch"] * 8 + stored_per_step + out_bytes
-            rec_d = recorded_traffic(f"{args.workload}/device{idx_key}") if not args.rows else None
-            extra["hbm_resident"] = {
-                "value": out_bytes / th / 1e9, "unit": "GB/s", "ms_per_step": th * 1e3,
-                "roofline": {"bound": "hbm", "achieved": alg / th / 1e9, "peak": hbm_peak,
-                             "unit": "GB/s", "frac": alg / th / 1e9 / hbm_peak,
-                             "traffic": (rec_d["dram_read_bytes"] + rec_d["dram_write_bytes"])
-                             if rec_d else None,
-                             "peak_source": f"{hbm_peak_src} hbm_gbs",
-                             "algorithmic_bytes_per_launch": alg},
-                "clocks": clk_h}
-            del dstore
+    # HBM-resident gather of the same store
+    if residency == "host" and want("hbm"):
+        dstore = Store.__new__(Store)
+        dstore.__dict__.update(store.__dict__)
+        dstore.slots = store.slots.to(dev)
+        dstore.residency = "device"
+        per_step_h, clk_h = timed_gather(dstore, batches, out, max(50, steps // 4), warmup,
+                                         flush, barrier)
+        th = float(np.mean(per_step_h))
+        alg = wl["batch"] * 8 + stored_per_step + out_bytes
+        rec_d = recorded_traffic(f"{args.workload}/device{idx_key}") if not args.rows else None
+        extra["hbm_resident"] = {
+            "value": out_bytes / th / 1e9, "unit": "GB/s", "ms_per_step": th * 1e3,
+            "roofline": {"bound": "hbm", "achieved": alg / th / 1e9, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": alg / th / 1e9 / hbm_peak,
+                         "traffic": (rec_d["dram_read_bytes"] + rec_d["dram_write_bytes"])
+                         if rec_d else None,
+                         "peak_source": f"{hbm_peak_src} hbm_gbs",
+                         "algorithmic_bytes_per_launch": alg},
+            "clocks": clk_h}
+        del dstore
+    if want("e2e"):
         extra["e2e"] = run_e2e(store, host_batches, max(20, steps // 10), warmup, dev)
-        if residency == "host":
-            # bytes over the link per step: the rows the gather reads (the ncu-measured
-            # link bytes when recorded, else the stored bytes), the index batch up,
-            # the rows back down
-            up = (rec["sysmem_read_bytes"] if rec else stored_per_step) + wl["batch"] * 8
-            both = up + out_bytes
-            t_e = extra["e2e"]["ms_per_step"] * 1e-3
-            extra["e2e"]["roofline"] = {
-                "bound": "host_link_both_directions", "achieved": both / t_e / 1e9,
-                "peak": link["bidirectional_memcpy_gbs"], "unit": "GB/s",
-                "frac": both / t_e / 1e9 / link["bidirectional_memcpy_gbs"],
-                "link_bytes_per_step": both}
-        # preprocessing stages with rows and slots in HBM
-        if residency == "host":
-            dstore = Store.__new__(Store)
-            dstore.__dict__.update(store.__dict__)
-            dstore.rows = store.rows.to(dev)
-            dstore.slots = torch.empty((n, store.slot_bytes), dtype=torch.uint8, device=dev)
-            dstore.bitmask = torch.zeros_like(store.bitmask)
-            dstore.row_bits = torch.zeros_like(store.row_bits)
-            dstore.status = torch.zeros_like(store.status)
-            mt, _ = time_stage(dstore.build_meta, reps, flush)
-            ct, _ = time_stage(dstore.compress, reps, flush)
-            sel_d = MaskSelect(dstore)
-            sdt, _ = time_stage(sel_d.run, reps, flush)
-            torch.cuda.synchronize()
-            same = bool(torch.equal(dstore.bitmask, store.bitmask))
-            comp_bytes = table_raw + float(stored.sum())
-            extra["stages_hbm"] = {
-                "build_meta": {"gbs_raw_in": table_raw / mt / 1e9, "ms": mt * 1e3,
-                               "frac_of_hbm": table_raw / mt / 1e9 / hbm_peak},
-                "compress": {"gbs_raw_in": table_raw / ct / 1e9, "ms": ct * 1e3,
-                             "frac_of_hbm": comp_bytes / ct / 1e9 / hbm_peak,
-                             "same_bitmask_as_host_run": same},
-                "build_meta_select": {"gbs_raw_in": table_raw / sdt / 1e9, "ms": sdt * 1e3,
-                                      "frac_of_hbm": 2 * table_raw / sdt / 1e9 / hbm_peak,
-                                      "reads_rows": 2}}
-            del dstore, sel_d
-            torch.cuda.empty_cache()
-        # before the mask-selection leg, which recompresses into the store's slots
+    if residency == "host" and want("e2e"):
+        # bytes over the link per step: the rows the gather reads (the ncu-measured
+        # link bytes when recorded, else the stored bytes), the index batch up,
+        # the rows back down
+        up = (rec["sysmem_read_bytes"] if rec else stored_per_step) + wl["batch"] * 8
+        both = up + out_bytes
+        t_e = extra["e2e"]["ms_per_step"] * 1e-3
+        extra["e2e"]["roofline"] = {
+            "bound": "host_link_both_directions", "achieved": both / t_e / 1e9,
+            "peak": link["bidirectional_memcpy_gbs"], "unit": "GB/s",
+            "frac": both / t_e / 1e9 / link["bidirectional_memcpy_gbs"],
+            "link_bytes_per_step": both}
+    # preprocessing stages with rows and slots in HBM
+    if residency == "host" and want("stages"):
+        dstore = Store.__new__(Store)
+        dstore.__dict__.update(store.__dict__)
+        dstore.rows = store.rows.to(dev)
+        dstore.slots = torch.empty((n, store.slot_bytes), dtype=torch.uint8, device=dev)
+        dstore.bitmask = torch.zeros_like(store.bitmask)
+        dstore.row_bits = torch.zeros_like(store.row_bits)
+        dstore.status = torch.zeros_like(store.status)
+        mt, _ = time_stage(dstore.build_meta, reps, flush)
+        ct, _ = time_stage(dstore.compress, reps, flush)
+        sel_d = MaskSelect(dstore)
+        sdt, _ = time_stage(sel_d.run, reps, flush)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(dstore.bitmask, store.bitmask))
+        comp_bytes = table_raw + float(stored.sum())
+        extra["stages_hbm"] = {
+            "build_meta": {"gbs_raw_in": table_raw / mt / 1e9, "ms": mt * 1e3,
+                           "frac_of_hbm": table_raw / mt / 1e9 / hbm_peak},
+            "compress": {"gbs_raw_in": table_raw / ct / 1e9, "ms": ct * 1e3,
+                         "frac_of_hbm": comp_bytes / ct / 1e9 / hbm_peak,
+                         "same_bitmask_as_host_run": same},
+            "build_meta_select": {"gbs_raw_in": table_raw / sdt / 1e9, "ms": sdt * 1e3,
+                                  "frac_of_hbm": 2 * table_raw / sdt / 1e9 / hbm_peak,
+                                  "reads_rows": 2}}
+        del dstore, sel_d
+        torch.cuda.empty_cache()
+    # before the mask-selection leg, which recompresses into the store's slots
+    if want("dedup"):
         extra["dedup"] = dedup_leg(store, wl, batches, out, steps, warmup, flush, barrier,
                                    out_bytes, link, hbm_peak, dev)
-        sstore, extra["mask_select"] = mask_select_leg(store, wl, batches, out, steps, warmup,
-                                                       flush, barrier, reps, table_raw,
-                                                       out_bytes, residency, link, hbm_peak)
-        extra["packed"] = packed_leg(sstore, wl, batches, out, steps, warmup, flush, barrier,
-                                     table_raw, out_bytes, link, hbm_peak, dev)
+    if want("select") or want("packed"):  # the packed store is made of the selected mask
+        sstore, mask_select = mask_select_leg(store, wl, batches, out, steps, warmup, flush,
+                                              barrier, reps, table_raw, out_bytes, residency,
+                                              link, hbm_peak)
+        if want("select"):
+            extra["mask_select"] = mask_select
+        if want("packed"):
+            extra["packed"] = packed_leg(sstore, wl, batches, out, steps, warmup, flush,
+                                         barrier, table_raw, out_bytes, link, hbm_peak, dev)
         del sstore
-        if store.raw_bytes <= 16384:  # per-position tables are built for rows up to 16 KiB
-            extra["positions"] = positions_leg(store, wl, batches, out, steps, warmup, flush,
-                                               barrier, reps, table_raw, out_bytes, link,
-                                               hbm_peak, dev)
-        if args.workload == "gnn_dense":
-            extra["offload"] = offload_leg(dev)
-        if args.workload == "dlrm_table":
-            extra["dlrm_26_tables"] = dlrm_batched_leg(dev, flush, barrier, steps, warmup,
-                                                       hbm_peak, n_tables=args.tables,
-                                                       n_rows=args.rows or 1_000_000)
+    # per-position tables are built for rows up to 16 KiB
+    if store.raw_bytes <= 16384 and want("positions"):
+        extra["positions"] = positions_leg(store, wl, batches, out, steps, warmup, flush,
+                                           barrier, reps, table_raw, out_bytes, link,
+                                           hbm_peak, dev)
+    if args.workload == "gnn_dense" and want("offload"):
+        extra["offload"] = offload_leg(dev)
+    if args.workload == "dlrm_table" and want("dlrm26"):
+        extra["dlrm_26_tables"] = dlrm_batched_leg(dev, flush, barrier, steps, warmup,
+                                                   hbm_peak, n_tables=args.tables,
+                                                   n_rows=args.rows or 1_000_000)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
@@ -1519,7 +1540,7 @@ def main():
             comp_t / 1e9 / hbm_peak
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"], line["cpu_baseline_all_cores"] = oracle_sample(wl)
-    if (args.workload == "gnn_dense" and not args.quick and not args.no_configs and
+    if (args.workload == "gnn_dense" and want("configs") and not args.no_configs and
             not args.rows and residency == "host"):
         # every configuration, summarised in one short object at the end of the line
         distinct = float(np.mean([stored[np.unique(hb.numpy())].sum()
