@@ -590,6 +590,16 @@ def positions_leg(store, wl, batches, out, steps, warmup, flush, barrier, reps, 
     return res
 
 
+def dedup_launches(store):
+    """Kernel launches of one de-duplicated gather: clear, claiming gather and copy for
+    rows of at most 32 blocks and 4 KiB (one gather unit each); a separate hash pass
+    before the gather for longer rows."""
+    block_bytes = store.B * ibp.WIDTH[store.dtype] // 8
+    nb = -(-store.L // store.B)
+    seg_blocks = max(1, min(nb, 32, 4096 // block_bytes))
+    return 3 if nb <= seg_blocks else 4
+
+
 def dedup_leg(store, wl, batches, out, steps, warmup, flush, barrier, out_bytes, link, hbm_peak,
               dev):
     """The same gathers through ibp_decompress_gather_dedup: each distinct row of a batch
@@ -621,7 +631,7 @@ def dedup_leg(store, wl, batches, out, steps, warmup, flush, barrier, out_bytes,
     torch.cuda.empty_cache()
     r = {"value": out_bytes / ts / 1e9, "unit": "GB/s", "ms_per_step": ts * 1e3, "clocks": clk,
          "distinct_fraction": distinct, "distinct_stored_bytes_per_launch": distinct_bytes,
-         "launches_per_call": 4}
+         "launches_per_call": dedup_launches(store)}
     if store.residency == "host":
         r["link_frac_distinct_bytes"] = distinct_bytes / ts / 1e9 / link["h2d_memcpy_gbs"]
     else:

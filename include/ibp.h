@@ -292,14 +292,16 @@ int ibp_decompress_gather_packed(const void *packed, uint64_t packed_bytes,
  * result as ibp_decompress_gather: out[i] (n_idx x row_elems words, device memory)
  * is row d_idx[i]; an index outside [0, n_rows) records IBP_ERR_INDEX in *d_status
  * and leaves its output row untouched. Each distinct row of d_idx is read from its
- * slot and decoded once, straight into the first output row that names it, then
- * copied from there to every other position that names it: for skewed index lists a
- * row crosses the host link once instead of once per request. d_scratch: device
- * memory of scratch_bytes >= the size ibp_gather_dedup_scratch_bytes reports (12
- * bytes per index plus a hash table of at least 16 bytes per index, all rounded up),
- * 16-byte aligned, overwritten; scratch_bytes too small: IBP_ERR_ARG. n_idx up to
- * 2^24 - 1 and n_rows below 2^40, else IBP_ERR_UNSUPPORTED. Asynchronous on s (four
- * launches: clear, hash, gather, copy); allocates nothing. */
+ * slot and decoded once, straight into the output row of one position that names it
+ * (the first to claim it), then copied from there to every other position that names
+ * it: for skewed index lists a row crosses the host link once instead of once per
+ * request. d_scratch: device memory of scratch_bytes >= the size
+ * ibp_gather_dedup_scratch_bytes reports (12 bytes per index plus a hash table of at
+ * least 16 bytes per index, all rounded up), 16-byte aligned, overwritten;
+ * scratch_bytes too small: IBP_ERR_ARG. n_idx up to 2^24 - 1 and n_rows below 2^40,
+ * else IBP_ERR_UNSUPPORTED. Asynchronous on s: three launches (clear, a gather that
+ * claims each row as it goes, copy) for rows of at most 32 blocks and 4 KiB, four (a
+ * hash pass before the gather) for longer rows; allocates nothing. */
 int ibp_gather_dedup_scratch_bytes(int64_t n_idx, int64_t row_elems, int dtype,
                                    uint32_t block_elems, size_t *bytes);
 int ibp_decompress_gather_dedup(const void *slots, int64_t slot_bytes, int64_t n_rows,

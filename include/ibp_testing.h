@@ -1,7 +1,7 @@
 /*
- * ibp_testing.h -- a testing hook of the GB300 IBP codec library (libibp_gb300.so).
+ * ibp_testing.h -- testing hooks of the GB300 IBP codec library (libibp_gb300.so).
  *
- * Not part of the codec: the paper has no counterpart. It exists so that the
+ * Not part of the codec: the paper has no counterpart. They exist so that the
  * failure path of the gather's bounded waits can be exercised on a GPU without
  * faulting, trapping or hanging it.
  *
@@ -27,6 +27,16 @@ extern "C" {
  * *d_status reads IBP_ERR_TIMEOUT. Host-side only: no CUDA call, never fails. Not
  * meant for normal use; a test that lowers the limit restores it. */
 uint64_t ibp_testing_set_wait_limit_ns(uint64_t ns);
+
+/* on != 0: the planner warps of warp-specialised gathers launched from now on (in
+ * this process, on every device) plan their units but never hand them to the
+ * decoders, so the decoders' first wait cannot complete and runs out after the wait
+ * limit: the call then records IBP_ERR_TIMEOUT in *d_status and its output is
+ * incomplete; every warp still ends within the limit. on = 0 restores normal
+ * operation. Returns the previous setting. Host-side only: no CUDA call, never fails.
+ * Gathers served by the other kernels are unaffected. Not meant for normal use; a
+ * test that sets it clears it. */
+int ibp_testing_withhold_plans(int on);
 
 #ifdef __cplusplus
 }

@@ -79,7 +79,7 @@ SYMBOLS = ("ibp_status_string", "ibp_slot_bytes", "ibp_meta_scratch_bytes", "ibp
            "ibp_decompress_gather_dedup", "ibp_query_async")
 
 # declared in include/ibp_testing.h (a testing hook, not part of the codec)
-TESTING_SYMBOLS = ("ibp_testing_set_wait_limit_ns",)
+TESTING_SYMBOLS = ("ibp_testing_set_wait_limit_ns", "ibp_testing_withhold_plans")
 
 MAX_MASK_CANDIDATES = 33
 
@@ -138,6 +138,8 @@ def load() -> ctypes.CDLL:
         getattr(lib, name).restype = i32
     lib.ibp_testing_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.ibp_testing_set_wait_limit_ns.restype = ctypes.c_uint64
+    lib.ibp_testing_withhold_plans.argtypes = [ctypes.c_int]
+    lib.ibp_testing_withhold_plans.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -499,3 +501,9 @@ def testing_set_wait_limit_ns(ns: int) -> int:
     """ibp_testing_set_wait_limit_ns (include/ibp_testing.h): the limit of the gather
     kernels' bounded waits, in ns (0: the default 2 s); returns the previous one."""
     return int(load().ibp_testing_set_wait_limit_ns(int(ns)))
+
+
+def testing_withhold_plans(on: bool) -> bool:
+    """ibp_testing_withhold_plans (include/ibp_testing.h): the warp-specialised
+    gather's planners keep their plans from the decoders; returns the previous setting."""
+    return bool(load().ibp_testing_withhold_plans(1 if on else 0))

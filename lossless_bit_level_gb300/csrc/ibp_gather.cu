@@ -82,6 +82,14 @@ struct GatherArgs {
   const unsigned long long *idx_count;
   // limit of each bounded wait of the warp-specialised kernel, in ns of global time
   uint64_t wait_ns;
+  // de-duplicated gather of rows that are one unit each (null table: off): before a
+  // unit is planned its position claims the row in this hash table; only the first
+  // claimant decodes it, claim_owner[position] receives the claimant
+  unsigned long long *claim_table;
+  uint32_t claim_mask;
+  int32_t *claim_owner;
+  // testing hook: the warp-specialised kernel's planners never hand a plan over
+  uint32_t withhold_plans;
 };
 
 // The plan of one unit (identical in every lane of its team).
@@ -123,6 +131,45 @@ __device__ __forceinline__ int64_t load_index(const GatherArgs &a, int64_t u, in
   if (u >= n_units) return -1;
   const int64_t i = a.nseg == 1 ? u : u / a.nseg;
   return a.idx ? __ldg(a.idx + i) : a.row0 + i;
+}
+
+// The claim of unit u's row (a row of one unit, so u is the output position) for a
+// de-duplicated gather, by one lane per unit. The table maps row + 1 to the first
+// position that claimed it, both in one 64-bit word (row in the top 40 bits), set by
+// one compare-and-swap; a row claimed earlier is usually seen by a plain L2 load,
+// without an atomic. Returns r for the claimant (it decodes the row) and -1 for every
+// other position (nothing to stage; the copy comes later) and for a bad index
+// (reported here). claim_owner[u] receives the claimant, or -1 for a bad index.
+constexpr int CLAIM_POS_BITS = 24;
+
+__device__ int64_t claim_row(const GatherArgs &a, int64_t u, int64_t n_units, int64_t r) {
+  if (u >= n_units) return r;
+  if (r < 0 || r >= a.n_rows) {
+    a.claim_owner[u] = -1;
+    report(a.status, IBP_ERR_INDEX);
+    return -1;
+  }
+  const unsigned long long key = (unsigned long long)r + 1ull;
+  const unsigned long long mine = (key << CLAIM_POS_BITS) | (unsigned long long)u;
+  uint32_t h = (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> 32) & a.claim_mask;  // Fibonacci
+  int32_t own = -1;
+  // at least two slots per position: a free slot or the row's entry is found within
+  // mask + 1 probes
+  for (uint32_t probe = 0; probe <= a.claim_mask; ++probe) {
+    unsigned long long old = __ldcg(a.claim_table + h);
+    if (old == 0ull) old = atomicCAS(a.claim_table + h, 0ull, mine);
+    if (old == 0ull) {
+      own = (int32_t)u;
+      break;
+    }
+    if ((old >> CLAIM_POS_BITS) == key) {
+      own = (int32_t)(old & ((1ull << CLAIM_POS_BITS) - 1));
+      break;
+    }
+    h = (h + 1) & a.claim_mask;
+  }
+  a.claim_owner[u] = own;
+  return own == (int32_t)u ? r : -1;
 }
 
 // The bytes of row r to stage, [o0, o1) of the buffer at slots: a packed store's
@@ -438,6 +485,10 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     } else {
       r_after = load_index(a, u_plan + stride, n_units);  // prefetch
     }
+    if (!PACKED && a.claim_table) {  // the team's leader claims, the team follows
+      const int64_t rc = leader ? claim_row(a, u_plan, n_units, r_plan) : 0;
+      r_plan = __shfl_sync(FULL, rc, lane & ~(TL - 1));
+    }
     const Unit un = plan_unit<PACKED>(a, shrink, u_plan, n_units, r_plan, leader, span_plan);
     if (leader && pend_k >= 0) metas[pend_k * TPW].bmw = pend_bmw;
     pend_bmw = un.lsb == PARSE_HEADER ? __ldg(a.bitmask + (un.segp >> 5)) : 0u;
@@ -522,6 +573,8 @@ template <int TL, int MINB, bool PACKED>
 __global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
+  // a de-duplicated gather is launched as a dependent of the kernel clearing its table
+  if (a.claim_table) grid_dependency_wait();
   team_gather<TL, PACKED>(a, smem, sruns);
 }
 
@@ -624,8 +677,9 @@ __device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64
   int64_t r_next = r_first;
   for (; k - lane < count; k += step) {
     const bool have = k < count;
-    const int64_t r = r_next;
+    int64_t r = r_next;
     r_next = k + step < count ? load_index(a, u0 + k + step, a.n_units) : -1;  // prefetch
+    if (have && a.claim_table) r = claim_row(a, u0 + k, a.n_units, r);
     bool ok = true;
     if (have) {
       const Unit un = (a.offsets || a.row_bits)
@@ -643,7 +697,7 @@ __device__ void ws_plan(const GatherArgs &a, const Code &code, int64_t u0, int64
         p.segp = un.segp;
         p.nvec = un.nvec;
         plans[slot] = p;
-        mbar_arrive(&planned[slot]);
+        if (!a.withhold_plans) mbar_arrive(&planned[slot]);
       }
     }
     if (!ok) ws_abort(a, abort);
@@ -744,6 +798,8 @@ __global__ void __launch_bounds__(WS_THREADS, 2) gather_ws_kernel(GatherArgs a) 
   __shared__ int abort_flag;
   __shared__ PlanSlot plans[PLAN_SLOTS];
   __shared__ uint64_t planned[PLAN_SLOTS], freed[PLAN_SLOTS];
+  // a de-duplicated gather is launched as a dependent of the kernel clearing its table
+  if (a.claim_table) grid_dependency_wait();
   // the CTAs split the units to gather evenly (with a device-side count, only those)
   const int64_t n_units = units_of(a);
   const int64_t u0 = n_units * blockIdx.x / gridDim.x;
@@ -818,6 +874,12 @@ int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   GatherArgs g = a;
   g.cta0 = 0;
   g.ncta = grid;
+  if (g.claim_table) {
+    if (launch_dependent(gather_kernel<TL, MINB, PACKED>, dim3(grid), dim3(GATHER_WARPS * 32),
+                         smem, s, g) != cudaSuccess)
+      return IBP_ERR_CUDA;
+    return IBP_OK;
+  }
   gather_kernel<TL, MINB, PACKED><<<grid, GATHER_WARPS * 32, smem, s>>>(g);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
@@ -839,6 +901,12 @@ int launch_ws_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
     return IBP_ERR_CUDA;
   const int64_t want = std::max<int64_t>(1, (a.n_units + 63) / 64);
   const int grid = (int)std::min<int64_t>(want, (int64_t)dev.sm_count * per_sm);
+  if (a.claim_table) {
+    if (launch_dependent(gather_ws_kernel<TL>, dim3(grid), dim3(WS_THREADS), smem, s, a) !=
+        cudaSuccess)
+      return IBP_ERR_CUDA;
+    return IBP_OK;
+  }
   gather_ws_kernel<TL><<<grid, WS_THREADS, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? IBP_OK : IBP_ERR_CUDA;
 }
@@ -886,11 +954,18 @@ int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const 
 
 namespace {
 std::atomic<uint64_t> g_wait_limit_ns{0};  // 0: WAIT_TIMEOUT_NS
+std::atomic<int> g_withhold_plans{0};
 }  // namespace
 
 uint64_t gather_wait_limit_ns() {
   const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
   return v ? v : WAIT_TIMEOUT_NS;
+}
+
+int gather_units_per_row(const RowGeom &g) {
+  const int block_bytes = g.lwb * 4;
+  const int seg_blocks = std::max(1, std::min({g.nb, 32, SEG_TARGET_BYTES / block_bytes}));
+  return (g.nb + seg_blocks - 1) / seg_blocks;
 }
 
 int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
@@ -899,7 +974,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   int64_t row0, int64_t n_idx, void *out, int32_t *d_status,
                   bool slots_in_device_memory, cudaStream_t s, const uint32_t *d_row_bits,
                   bool skip_negative, bool pos_in_index,
-                  const unsigned long long *d_idx_count) {
+                  const unsigned long long *d_idx_count, const ClaimTable *claim) {
   if (n_idx == 0) return IBP_OK;
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
@@ -915,6 +990,11 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   a.pos_in_index = pos_in_index ? 1u : 0u;
   a.idx_count = d_idx_count;
   a.wait_ns = gather_wait_limit_ns();
+  a.withhold_plans = g_withhold_plans.load(std::memory_order_relaxed) ? 1u : 0u;
+  a.claim_table = claim ? claim->table : nullptr;
+  a.claim_mask = claim ? claim->mask : 0u;
+  a.claim_owner = claim ? claim->owner : nullptr;
+  if (claim && (d_offsets || d_row_bits || gather_units_per_row(g) != 1)) return IBP_ERR_ARG;
   a.packed_bytes = d_offsets ? packed_bytes : (uint64_t)n_rows * (uint64_t)slot_bytes;
   a.n_rows = n_rows;
   a.bitmask = d_bitmask;
@@ -1070,4 +1150,8 @@ int launch_gather_batched(const ibp_gather_job *jobs, int n_jobs, const RowGeom 
 
 extern "C" uint64_t ibp_testing_set_wait_limit_ns(uint64_t ns) {
   return ibp::g_wait_limit_ns.exchange(ns, std::memory_order_relaxed);
+}
+
+extern "C" int ibp_testing_withhold_plans(int on) {
+  return ibp::g_withhold_plans.exchange(on ? 1 : 0, std::memory_order_relaxed);
 }

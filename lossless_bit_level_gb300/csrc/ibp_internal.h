@@ -67,6 +67,37 @@ int launch_compress_stream(const void *rows, int64_t n_rows, const RowGeom &g, u
 // pos_in_index (slotted stores only): index entries hold (output row << 40) | row.
 // d_idx_count (device memory, nullable): only the first *d_idx_count index entries
 // are gathered (read when the kernel starts).
+// claim (nullable; slotted stores whose rows are one gather unit each): each index
+// position first claims its row in claim->table (an open-addressing hash table of
+// mask + 1 zeroed 64-bit slots, at least two per position): only the first position
+// to claim a row decodes it, and claim->owner[i] receives the position that claimed
+// row d_idx[i] (i itself for that one, -1 for a bad index).
+// The gather is then launched as a programmatic dependent of the kernel before it on
+// the stream (which clears the table), so that its launch overlaps that kernel.
+struct ClaimTable {
+  unsigned long long *table;
+  uint32_t mask;
+  int32_t *owner;
+};
+// Launch kernel<<<grid, block, smem, s>>>(args...) as a programmatic dependent of the
+// previous kernel on s (the kernel must call grid_dependency_wait before it reads
+// anything that kernel wrote).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+int gather_units_per_row(const RowGeom &g);
 int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offsets,
                   uint64_t packed_bytes, int64_t n_rows, const RowGeom &g, uint32_t dtype,
                   const uint32_t *d_bitmask, const ibp_meta *d_meta, const int64_t *d_idx,
@@ -74,7 +105,8 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   bool slots_in_device_memory, cudaStream_t s,
                   const uint32_t *d_row_bits = nullptr, bool skip_negative = false,
                   bool pos_in_index = false,
-                  const unsigned long long *d_idx_count = nullptr);
+                  const unsigned long long *d_idx_count = nullptr,
+                  const ClaimTable *claim = nullptr);
 // De-duplicated slotted gather: every distinct row of d_idx is read and decoded
 // once (into d_scratch), then copied to each output position that asks for it.
 size_t dedup_scratch_bytes(int64_t n_idx, const RowGeom &g);

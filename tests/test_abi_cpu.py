@@ -45,6 +45,9 @@ def test_testing_wait_limit_hook(lib):
     assert ibp.testing_set_wait_limit_ns(5) == 0
     assert ibp.testing_set_wait_limit_ns(0) == 5
     assert ibp.testing_set_wait_limit_ns(0) == 0
+    assert ibp.testing_withhold_plans(True) is False
+    assert ibp.testing_withhold_plans(False) is True
+    assert ibp.testing_withhold_plans(False) is False
 
 
 def test_size_queries(lib):

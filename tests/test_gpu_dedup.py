@@ -107,6 +107,24 @@ def test_all_distinct_and_one_row():
     full_check(words, FP32, 0.9, 32, np.array([7], dtype=np.int64), "device")
 
 
+def test_few_hot_rows_across_many_blocks():
+    # 50,003 positions over 40 rows: every row repeats inside each 1024-position block
+    # of the hash pass and across all of them; bad indices are scattered in between
+    words = words_of(gen.tiny_fp32(4096))
+    g = np.random.default_rng(5)
+    idx = g.integers(0, 40, size=50_003).astype(np.int64) * 97
+    bad = g.choice(idx.size, size=300, replace=False)
+    idx[bad[:150]] = -3
+    idx[bad[150:]] = 4096
+    store, meta = build(words, FP32, 0.9, 32, "device")
+    out, st = dedup_gather(store, meta, idx, fill=7)
+    assert st == ibp.ERR_INDEX
+    got = from_torch(out, np.uint32)
+    good = np.setdiff1d(np.arange(idx.size), bad)
+    assert np.array_equal(got[good], words[idx[good]])
+    assert np.all(got[bad] == 7)
+
+
 def test_bad_indices_leave_rows_untouched():
     words = words_of(gen.tiny_fp32(1000))
     store, meta = build(words, FP32, 0.9, 32, "device")

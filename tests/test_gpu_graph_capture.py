@@ -1,7 +1,8 @@
 """Every compute call of the C ABI captured in one CUDA graph and replayed (needs a GPU).
 
 The header states that the calls may be captured once their argument checks pass;
-this builds metadata (threshold, saving-aware, per-position), compresses, gathers,
+this builds metadata (threshold, saving-aware, per-position), compresses, gathers
+(plain, packed, per-position and de-duplicated, the last for short and long rows),
 packs and streams a range inside one capture, replays the graph on fresh inputs and
 checks every output against the oracle."""
 from __future__ import annotations
@@ -49,6 +50,20 @@ def test_whole_api_in_one_graph():
     packed = torch.zeros(n * sb, dtype=torch.uint8, device=dev)
     kbm = torch.zeros_like(bm)
     kout = torch.zeros_like(out)
+    dout = torch.zeros_like(out)
+    dscr = torch.empty(ibp.gather_dedup_scratch_bytes(1000, L, FP32, B), dtype=torch.uint8,
+                       device=dev)
+    # long rows (several gather units each): the de-duplicated gather's hash-pass path
+    Ll = 2048
+    lrows = torch.zeros((300, Ll), dtype=torch.int32, device=dev)
+    lmeta = torch.zeros(4, dtype=torch.int32, device=dev)
+    lsb = ibp.slot_bytes(Ll, FP32)
+    lslots = torch.zeros((300, lsb), dtype=torch.uint8, device=dev)
+    lbm = torch.zeros(((300 + 31) // 32,), dtype=torch.int32, device=dev)
+    lidx = torch.zeros(500, dtype=torch.int64, device=dev)
+    lout = torch.zeros((500, Ll), dtype=torch.int32, device=dev)
+    lscr = torch.empty(ibp.gather_dedup_scratch_bytes(500, Ll, FP32, B), dtype=torch.uint8,
+                       device=dev)
 
     def calls(stream):
         ibp.build_meta(rows, T, B, meta, scr, dtype=FP32, stream=stream)
@@ -64,6 +79,12 @@ def test_whole_api_in_one_graph():
         ibp.compress_positions(rows, B, pm, pb, pslots, pbm, prb, dtype=FP32, stream=stream)
         ibp.decompress_gather_positions(pslots, n, L, FP32, B, pbm, pm, pb, idx, pout, status,
                                         stream=stream)
+        ibp.decompress_gather_dedup(slots, n, L, FP32, B, bm, meta, idx, dout, dscr, status,
+                                    stream=stream)
+        ibp.build_meta(lrows, T, B, lmeta, scr, dtype=FP32, stream=stream)
+        ibp.compress(lrows, B, lmeta, lslots, lbm, None, status, dtype=FP32, stream=stream)
+        ibp.decompress_gather_dedup(lslots, 300, Ll, FP32, B, lbm, lmeta, lidx, lout, lscr,
+                                    status, stream=stream)
 
     s = torch.cuda.Stream()
     calls(s)  # first calls outside the capture (per-device lookups happen once)
@@ -76,6 +97,10 @@ def test_whole_api_in_one_graph():
         ix = np.random.default_rng(k).integers(0, n, size=1000)
         rows.copy_(torch.from_numpy(words.view(np.int32)))
         idx.copy_(torch.from_numpy(ix))
+        lwords = words_of(gen.gnn_dense(300 * 16)).reshape(300, Ll)
+        lix = np.random.default_rng(10 + k).zipf(1.2, size=500).astype(np.int64) % 300
+        lrows.copy_(torch.from_numpy(lwords.view(np.int32)))
+        lidx.copy_(torch.from_numpy(lix))
         status.zero_()
         g.replay()
         torch.cuda.synchronize()
@@ -87,8 +112,9 @@ def test_whole_api_in_one_graph():
         o_pm, o_pb = oracle.build_meta_positions(words, T)
         assert np.array_equal(pm.cpu().numpy().view(np.uint32), o_pm)
         assert np.array_equal(pb.cpu().numpy().view(np.uint32), o_pb)
-        for t in (out, kout, pout):
+        for t in (out, kout, pout, dout):
             assert np.array_equal(t.cpu().numpy().view(np.uint32), words[ix])
+        assert np.array_equal(lout.cpu().numpy().view(np.uint32), lwords[lix])
         assert np.array_equal(rout.cpu().numpy().view(np.uint32), words)
         _, o_bm, o_rb = oracle.compress(words, B, mask, bitval)
         assert np.array_equal(bm.cpu().numpy().view(np.uint32), o_bm)

@@ -5,11 +5,12 @@ The warp-specialised decompress-gather (slots in device memory, rows over 1 KiB)
 passes work from planner warps to decoder warps through shared-memory barriers;
 every wait on them is bounded ("Reducing the GPU Memory Bottleneck with Lossless
 Compression for ML -- Extended", technical summary, "Core algorithm", decompression,
-is the stage; the bound is this library's). With the limit lowered to 1 ns through
-the testing hook (include/ibp_testing.h) a wait runs out: the call must record
-IBP_ERR_TIMEOUT, the stream must complete, and the next gather with the default
-limit on the same stream must be bit-exact against the oracle. No GPU fault, trap
-or endless wait is involved: the kernel gives up and returns."""
+is the stage; the bound is this library's). The testing hooks (include/ibp_testing.h)
+make the planners keep their plans to themselves -- a barrier that nothing completes
+-- and lower the limit to 1 ms: the decoders' waits run out, the call must record
+IBP_ERR_TIMEOUT, the stream must complete, and the next gather with the hooks cleared
+on the same stream must be bit-exact against the oracle. No GPU fault, trap or endless
+wait is involved: every warp gives up within the limit and returns."""
 from __future__ import annotations
 
 import numpy as np
@@ -41,11 +42,13 @@ def test_wait_runs_out_then_the_stream_recovers():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
-    prev = ibp.testing_set_wait_limit_ns(1)
+    prev = ibp.testing_set_wait_limit_ns(1_000_000)
+    prev_w = ibp.testing_withhold_plans(True)
     try:
         ibp.decompress_gather(store.slots, n, L, ibp.FP32, B, store.bitmask, meta, it, out,
                               status, stream=stream)
     finally:
+        ibp.testing_withhold_plans(prev_w)
         ibp.testing_set_wait_limit_ns(prev)
     stream.synchronize()  # the call ends: no wait is left without a bound
     assert int(status.item()) == ibp.ERR_TIMEOUT
