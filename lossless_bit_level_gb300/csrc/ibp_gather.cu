@@ -446,9 +446,11 @@ struct __align__(16) StagedMeta {
   uint32_t lsb, segp, nvec, bmw, nchunk, lead;  // nchunk, lead: Unit.echunk, Unit.lead
 };
 
-template <int TL, bool PACKED>
+// CLAIM (slotted stores only): the de-duplicated gather's claiming mode.
+template <int TL, bool PACKED, bool CLAIM = false>
 __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedRuns &sruns,
                             uint8_t *warp_smem, StagedMeta *warp_meta) {
+  static_assert(!(PACKED && CLAIM), "claims are made on slotted stores only");
   constexpr int TPW = 32 / TL;  // teams per warp
   const uint32_t nr = sruns.n;
   const int lane = threadIdx.x & 31;
@@ -485,7 +487,7 @@ __device__ void gather_body(const GatherArgs &a, const Code &code, const SharedR
     } else {
       r_after = load_index(a, u_plan + stride, n_units);  // prefetch
     }
-    if (!PACKED && a.claim_table) {  // the team's leader claims, the team follows
+    if (CLAIM) {  // the team's leader claims, the team follows
       const int64_t rc = leader ? claim_row(a, u_plan, n_units, r_plan) : 0;
       r_plan = __shfl_sync(FULL, rc, lane & ~(TL - 1));
     }
@@ -552,7 +554,7 @@ __host__ __device__ inline size_t team_warp_bytes(int tl, int unit_bytes) {
 
 // MINB: resident CTAs per SM the register budget is sized for (4 for slots in
 // device memory, 3 for host memory; measured best for each).
-template <int TL, bool PACKED>
+template <int TL, bool PACKED, bool CLAIM = false>
 __device__ __forceinline__ void team_gather(const GatherArgs &a, uint8_t *smem,
                                             SharedRuns &sruns) {
   const ibp_meta m = load_meta(a.meta);
@@ -566,16 +568,16 @@ __device__ __forceinline__ void team_gather(const GatherArgs &a, uint8_t *smem,
   uint8_t *warp_smem = smem + (threadIdx.x >> 5) * team_warp_bytes(TL, a.unit_bytes);
   StagedMeta *warp_meta = reinterpret_cast<StagedMeta *>(
       warp_smem + (size_t)GATHER_NBUF * (32 / TL) * a.unit_bytes);
-  gather_body<TL, PACKED>(a, code, sruns, warp_smem, warp_meta);
+  gather_body<TL, PACKED, CLAIM>(a, code, sruns, warp_smem, warp_meta);
 }
 
-template <int TL, int MINB, bool PACKED>
+template <int TL, int MINB, bool PACKED, bool CLAIM = false>
 __global__ void __launch_bounds__(GATHER_WARPS * 32, MINB) gather_kernel(GatherArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ SharedRuns sruns;
   // a de-duplicated gather is launched as a dependent of the kernel clearing its table
-  if (a.claim_table) grid_dependency_wait();
-  team_gather<TL, PACKED>(a, smem, sruns);
+  if (CLAIM) grid_dependency_wait();
+  team_gather<TL, PACKED, CLAIM>(a, smem, sruns);
 }
 
 // Several gathers with one row geometry in one launch (e.g. one lookup batch per
@@ -849,18 +851,19 @@ int ilog2(int x) {
   return s;
 }
 
-template <int TL, int MINB, bool PACKED>
+template <int TL, int MINB, bool PACKED, bool CLAIM = false>
 int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   const size_t smem = (size_t)GATHER_WARPS * team_warp_bytes(TL, a.unit_bytes);
   static std::atomic<int> configured[64];  // the attribute is set once per device
   if (dev.device >= 64 || !configured[dev.device].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(gather_kernel<TL, MINB, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gather_kernel<TL, MINB, PACKED, CLAIM>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dev.max_smem_optin - (int)sizeof(SharedRuns) - 1024) != cudaSuccess)
       return IBP_ERR_CUDA;
     if (dev.device < 64) configured[dev.device].store(1, std::memory_order_release);
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL, MINB, PACKED>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<TL, MINB, PACKED, CLAIM>,
                                                     GATHER_WARPS * 32, smem) != cudaSuccess ||
       per_sm < 1)
     return IBP_ERR_CUDA;
@@ -874,9 +877,9 @@ int launch_tl(const GatherArgs &a, const DeviceInfo &dev, cudaStream_t s) {
   GatherArgs g = a;
   g.cta0 = 0;
   g.ncta = grid;
-  if (g.claim_table) {
-    if (launch_dependent(gather_kernel<TL, MINB, PACKED>, dim3(grid), dim3(GATHER_WARPS * 32),
-                         smem, s, g) != cudaSuccess)
+  if (CLAIM) {
+    if (launch_dependent(gather_kernel<TL, MINB, PACKED, CLAIM>, dim3(grid),
+                         dim3(GATHER_WARPS * 32), smem, s, g) != cudaSuccess)
       return IBP_ERR_CUDA;
     return IBP_OK;
   }
@@ -931,7 +934,7 @@ int launch_ws(GatherArgs a, const RowGeom &g, const DeviceInfo &dev, cudaStream_
   }
 }
 
-template <bool PACKED>
+template <bool PACKED, bool CLAIM = false>
 int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const DeviceInfo &dev,
                 cudaStream_t s) {
   // units of at most 1 KiB in device memory: team size 4 or 8, 4 CTAs per SM (for
@@ -939,14 +942,14 @@ int launch_team(const GatherArgs &a, int tl, bool slots_in_device_memory, const 
   // store in HBM).
   if (slots_in_device_memory) {
     constexpr int MINB = 4;
-    if (tl == 4) return launch_tl<4, MINB, PACKED>(a, dev, s);
-    return launch_tl<8, MINB, PACKED>(a, dev, s);
+    if (tl == 4) return launch_tl<4, MINB, PACKED, CLAIM>(a, dev, s);
+    return launch_tl<8, MINB, PACKED, CLAIM>(a, dev, s);
   }
   switch (tl) {
-    case 4: return launch_tl<4, 3, PACKED>(a, dev, s);
-    case 8: return launch_tl<8, 3, PACKED>(a, dev, s);
-    case 16: return launch_tl<16, 3, PACKED>(a, dev, s);
-    default: return launch_tl<32, 3, PACKED>(a, dev, s);
+    case 4: return launch_tl<4, 3, PACKED, CLAIM>(a, dev, s);
+    case 8: return launch_tl<8, 3, PACKED, CLAIM>(a, dev, s);
+    case 16: return launch_tl<16, 3, PACKED, CLAIM>(a, dev, s);
+    default: return launch_tl<32, 3, PACKED, CLAIM>(a, dev, s);
   }
 }
 
@@ -1032,6 +1035,7 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
   int tl = 4;
   while (tl < 32 && tl * 4 < nvec) tl *= 2;
   if (d_offsets || a.row_bits) return launch_team<true>(a, tl, slots_in_device_memory, dev, s);
+  if (a.claim_table) return launch_team<false, true>(a, tl, slots_in_device_memory, dev, s);
   return launch_team<false>(a, tl, slots_in_device_memory, dev, s);
 }
 
