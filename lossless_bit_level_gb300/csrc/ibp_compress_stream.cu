@@ -247,6 +247,66 @@ __device__ __forceinline__ void pack_full(const Code &code, const Runs4 &runs,
   sp.pb = (wq - (uint32_t)lane - (uint32_t)qh) << 5;
 }
 
+// Match bits of a full step from the 16-byte view (lane l holds lane words 4l..4l+3):
+// a block is LWB / 4 consecutive lanes, and matches when all of their words do.
+template <int LWB>
+__device__ __forceinline__ uint32_t vec_frag(const uint4 &v, const Code &code) {
+  constexpr int LPB = LWB / 4;  // lanes per block
+  constexpr int BPS = 128 / LWB;
+  const uint32_t bv = code.bitval32, m = code.mask32;
+  const bool ok = (((v.x ^ bv) & m) | ((v.y ^ bv) & m) | ((v.z ^ bv) & m) | ((v.w ^ bv) & m)) == 0u;
+  uint32_t A = __ballot_sync(FULL, ok);
+#pragma unroll
+  for (int sft = 1; sft < LPB; sft <<= 1) A &= A >> sft;
+  if (LPB == 8) return ((A & 0x01010101u) * 0x01020408u) >> 24;  // bits 0, 8, 16, 24
+  uint32_t frag = 0;
+#pragma unroll
+  for (int b = 0; b < BPS; ++b) frag |= ((A >> (b * LPB)) & 1u) << b;
+  return frag;
+}
+
+// A full step packed from the 16-byte view, for fields of FC = 8, 16 or 24 bits: four
+// consecutive lane words give four fields that fill FC / 8 whole payload words, so
+// each lane writes its own words (no shuffles). A raw block's lane writes its four
+// lane words.
+template <int LWB, int FC>
+__device__ __forceinline__ void pack_vec(const Runs4 &runs, WarpRing &w, const uint4 &v,
+                                         uint32_t frag, StreamPos &sp, int qh) {
+  static_assert(FC == 8 || FC == 16 || FC == 24, "whole words per four fields");
+  constexpr int LPB = LWB / 4;
+  constexpr int BPS = 128 / LWB;
+  constexpr uint32_t MW = (uint32_t)LWB * FC / 32;  // payload words of a matching block
+  const int lane = threadIdx.x & 31;
+  const uint32_t blk = (uint32_t)lane / LPB, pos = (uint32_t)lane % LPB;
+  const uint32_t p = (frag >> blk) & 1u;
+  const uint32_t nm = __popc(frag & low_mask(blk));  // matching blocks before this one
+  uint32_t wq = (uint32_t)qh + (sp.pb >> 5) + nm * MW + (blk - nm) * (uint32_t)LWB;
+  uint32_t *ring = w.ring();
+  if (p) {
+    const uint32_t f0 = extract4_mul(v.x, runs), f1 = extract4_mul(v.y, runs);
+    const uint32_t f2 = extract4_mul(v.z, runs), f3 = extract4_mul(v.w, runs);
+    wq += pos * (FC / 8);
+    if (FC == 8) {
+      ring[wq & (RING_WORDS - 1)] = f0 | (f1 << 8) | (f2 << 16) | (f3 << 24);
+    } else if (FC == 16) {
+      ring[wq & (RING_WORDS - 1)] = f0 | (f1 << 16);
+      ring[(wq + 1) & (RING_WORDS - 1)] = f2 | (f3 << 16);
+    } else {
+      ring[wq & (RING_WORDS - 1)] = f0 | (f1 << 24);
+      ring[(wq + 1) & (RING_WORDS - 1)] = (f1 >> 8) | (f2 << 16);
+      ring[(wq + 2) & (RING_WORDS - 1)] = (f2 >> 16) | (f3 << 8);
+    }
+  } else {
+    wq += pos * 4;
+    ring[wq & (RING_WORDS - 1)] = v.x;
+    ring[(wq + 1) & (RING_WORDS - 1)] = v.y;
+    ring[(wq + 2) & (RING_WORDS - 1)] = v.z;
+    ring[(wq + 3) & (RING_WORDS - 1)] = v.w;
+  }
+  const uint32_t nmatch = __popc(frag);
+  sp.pb += (nmatch * MW + ((uint32_t)BPS - nmatch) * (uint32_t)LWB) << 5;
+}
+
 // Any other step (the row's last one, or blocks of 8 or 16 lane words).
 template <int LWB>
 __device__ __forceinline__ void pack_step(const Code &code, const Runs4 &runs,
@@ -313,29 +373,28 @@ __device__ __forceinline__ void flush(WarpRing &w, uint4 *dst, StreamPos &sp, in
   if (fe > sp.fv) sp.fv = fe;
 }
 
-// flush for the vectors a step completes: at most 33 (a step adds at most 128
-// payload words, and up to three words before them were complete already), so at
-// most two per lane.
+// flush for the vectors a step completes: at most 32, one per lane. sp.fv is the
+// vector of stream word qh + pb/32 rounded down (all complete vectors before it are
+// out), and a step adds at most 128 payload words, so fe - sp.fv <= 32.
 __device__ __forceinline__ void flush_step(WarpRing &w, uint4 *dst, StreamPos &sp, int fe,
                                            uint32_t s0, int hv, int nvec, int lane) {
   const uint4 *ring4 = reinterpret_cast<const uint4 *>(w.ring());
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int v = sp.fv + lane + 32 * i;
-    if (v < fe) {
-      const uint4 cur = ring4[v & (RING_VECS - 1)];
-      const uint32_t prev = w.ring()[(4 * v - 1) & (RING_WORDS - 1)];
-      const uint4 val =
-          make_uint4(__funnelshift_l(prev, cur.x, s0), __funnelshift_l(cur.x, cur.y, s0),
-                     __funnelshift_l(cur.y, cur.z, s0), __funnelshift_l(cur.z, cur.w, s0));
-      if (v < hv) *w.head() = val;
-      else if (v < nvec) dst[v] = val;
-    }
+  const int v = sp.fv + lane;
+  if (v < fe) {
+    const uint4 cur = ring4[v & (RING_VECS - 1)];
+    const uint32_t prev = w.ring()[(4 * v - 1) & (RING_WORDS - 1)];
+    const uint4 val =
+        make_uint4(__funnelshift_l(prev, cur.x, s0), __funnelshift_l(cur.x, cur.y, s0),
+                   __funnelshift_l(cur.y, cur.z, s0), __funnelshift_l(cur.z, cur.w, s0));
+    if (v < hv) *w.head() = val;
+    else if (v < nvec) dst[v] = val;
   }
   if (fe > sp.fv) sp.fv = fe;
 }
 
-template <int LWB, bool FAST>
+// FC8 (8, 16 or 24; 0: off): with FAST, full steps are matched and packed from the
+// 16-byte view (pack_vec); other steps as below.
+template <int LWB, bool FAST, int FC8 = 0>
 __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedRuns &sruns,
                             WarpRing &w) {
   constexpr int BPS = 128 / LWB;  // blocks per step
@@ -401,15 +460,23 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
         const int nw_step = min(128, a.raw_words - 128 * k);
         uint32_t *S = reinterpret_cast<uint32_t *>(&w.stage()[k % PF][0]);
         uint32_t xg[4];
-        if (nw_step == 128) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) xg[g] = S[32 * g + lane];
-        } else {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) xg[g] = 32 * g + lane < nw_step ? S[32 * g + lane] : 0u;
-        }
+        uint4 v4;
+        const bool vec = FC8 != 0 && nw_step == 128;  // a full step (no partial block)
         const int b0 = k * BPS;
-        const uint32_t frag = group_frag<LWB>(xg, nw_step, min(BPS, a.nb - b0), code);
+        uint32_t frag;
+        if (vec) {
+          v4 = w.stage()[k % PF][lane];
+          frag = vec_frag<LWB>(v4, code);
+        } else {
+          if (nw_step == 128) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) xg[g] = S[32 * g + lane];
+          } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) xg[g] = 32 * g + lane < nw_step ? S[32 * g + lane] : 0u;
+          }
+          frag = group_frag<LWB>(xg, nw_step, min(BPS, a.nb - b0), code);
+        }
         if (k >= k_seen) {
           hcur |= frag << (b0 & 31);
           if (((b0 + BPS) & 31) == 0 || k == nsteps - 1) {
@@ -431,10 +498,17 @@ __device__ void stream_rows(const StreamArgs &a, const Code &code, const SharedR
           __syncwarp();
           break;
         }
-        if (LWB >= 32 && nw_step == 128)
+        if constexpr (FC8 != 0) {
+          if (vec) {
+            pack_vec<LWB, (FC8 ? FC8 : 8)>(runs, w, v4, frag, sp, qh);
+          } else {
+            pack_step<LWB>(code, runs, sruns, w, xg, nw_step, frag, sp, qh, pl);
+          }
+        } else if (LWB >= 32 && nw_step == 128) {
           pack_full<LWB, FAST>(code, runs, sruns, w, xg, frag, sp, qh, pl);
-        else
+        } else {
           pack_step<LWB>(code, runs, sruns, w, xg, nw_step, frag, sp, qh, pl);
+        }
         __syncwarp();
         flush_step(w, dst, sp, (int)(((uint32_t)qh + (sp.pb >> 5)) >> 2), s0, hv, nvec, lane);
         __syncwarp();
@@ -492,9 +566,17 @@ __global__ void __launch_bounds__(SW_THREADS, 3) compress_stream_kernel(StreamAr
   __syncthreads();
   WarpRing w;
   w.base = smem_stream + (threadIdx.x >> 5) * warp_ring_bytes(a.hdr_words);
-  // the common masks (fields of at least 16 bits, at most four runs of kept bits, bit
-  // 0 kept) get their own copy of the row loop; only one copy runs in a launch
-  if (code.fc >= 16 && sruns.n <= 4 && sruns.n > 0 && sruns.sh[0] == 0u)
+  // the common masks (at most four runs of kept bits, bit 0 kept) get their own copies
+  // of the row loop: fields of 8, 16 or 24 bits (whole words per four fields), other
+  // fields of at least 16 bits; only one copy runs in a launch
+  const bool fast_runs = sruns.n <= 4 && sruns.n > 0 && sruns.sh[0] == 0u;
+  if (fast_runs && code.fc == 24)
+    stream_rows<LWB, true, 24>(a, code, sruns, w);
+  else if (fast_runs && code.fc == 16)
+    stream_rows<LWB, true, 16>(a, code, sruns, w);
+  else if (fast_runs && code.fc == 8)
+    stream_rows<LWB, true, 8>(a, code, sruns, w);
+  else if (fast_runs && code.fc >= 16)
     stream_rows<LWB, true>(a, code, sruns, w);
   else
     stream_rows<LWB, false>(a, code, sruns, w);

@@ -185,6 +185,49 @@ def test_forced_masks_bf16(mask16):
     assert np.array_equal(from_torch(out, np.uint16), words[idx])
 
 
+# masks whose matching lane words keep 8, 16 or 24 bits, in at most four runs with bit
+# 0 kept: long rows take the compressor's 16-byte path for them
+WHOLE_WORD_FIELDS = [
+    (FP32, np.uint32, 0xFFFFFF00, 1000), (FP32, np.uint32, 0xFFFF0000, 1000),
+    (FP32, np.uint32, 0x7F800000, 1000),
+    (BF16, np.uint16, 0x7FF8, 2056), (BF16, np.uint16, 0x7F80, 2056),
+    (BF16, np.uint16, 0x7800, 2056),
+    (W8, np.uint8, 0xFC, 4112), (W8, np.uint8, 0xF0, 4112), (W8, np.uint8, 0xC0, 4112),
+]
+
+
+@pytest.mark.parametrize("B", [32, 64])
+@pytest.mark.parametrize("dtype_code,np_dt,mask,L", WHOLE_WORD_FIELDS)
+def test_whole_word_fields_long_rows(dtype_code, np_dt, mask, L, B):
+    """Rows over 2 KiB (a ragged last block, a partial last step) with fields of 8, 16
+    or 24 bits per lane word: blocks matching and not within a step, rows that never
+    match, rows that match but save nothing; slots, bitmask and row sizes vs the
+    oracle, then the gather."""
+    g = np.random.default_rng(mask * 7 + B)
+    n = 96
+    bits = np.dtype(np_dt).itemsize * 8
+    bitval = (0x5A5A5A5A & mask) & ((1 << bits) - 1)
+    rnd = g.integers(0, 1 << bits, size=(n, L), dtype=np.uint64).astype(np_dt)
+    keep = g.random(size=(n, L)) < 0.997
+    words = np.where(keep, (rnd & ~np_dt(mask)) | np_dt(bitval), rnd).astype(np_dt)
+    words[: n // 8] = rnd[: n // 8]  # no match at all
+    lw = L // 8
+    words[n // 8: n // 4, :lw] = rnd[n // 8: n // 4, :lw]  # a raw first stretch
+    o_slots, o_bitmask, o_row_bits = oracle.compress(words, B, mask, bitval)
+    meta = meta_tensor(mask, bitval, dtype_code, B)
+    store = GpuStore(n, L, dtype_code, B, "device")
+    gpu_compress(to_torch(words, "device"), meta, store)
+    torch.cuda.synchronize()
+    assert int(store.status.item()) == 0
+    assert np.array_equal(bitmask_np(store), o_bitmask)
+    assert np.array_equal(row_bits_np(store), o_row_bits)
+    compare_slots(slots_np(store), o_slots, o_bitmask, o_row_bits, L * np.dtype(np_dt).itemsize)
+    idx = g.integers(0, n, size=300)
+    out, st = gpu_gather(store, meta, idx)
+    assert st == 0
+    assert np.array_equal(from_torch(out, np_dt), words[idx])
+
+
 @pytest.mark.parametrize("w", [32, 16, 8])
 def test_special_values_round_trip(w):
     g = np.random.default_rng(w)
