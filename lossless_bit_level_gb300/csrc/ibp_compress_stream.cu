@@ -27,10 +27,13 @@
 //     are its lane words; a matching block's lane words give fields of fc bits, and
 //     lane k assembles payload word k from the (at most three for fc >= 16) fields
 //     that overlap it, fetched with shuffles (which fields, and the shifts, depend
-//     only on k and fc). The payload words go into a 256-word ring per warp, at the
-//     index of the stream word they start;
-//   * the complete 16-byte stream vectors go out to the slot, each lane's words
-//     funnel-shifted from two payload words. The vectors that hold participation
+//     only on k and fc). For fields of 8, 16 or 24 bits a full step is taken from
+//     the 16-byte view instead (lane l holds lane words 4l..4l+3): its four fields
+//     fill fc/8 whole payload words, which the lane writes itself, no shuffles. The
+//     payload words go into a 256-word ring per warp, at the index of the stream word
+//     they start;
+//   * the complete 16-byte stream vectors (at most one per lane per step) go out to
+//     the slot, each lane's words funnel-shifted from two payload words. The vectors that hold participation
 //     bits are written last: those below the first payload word from the warp's copy
 //     of the bits, the one shared with the payload (at most one) kept back from the
 //     flush and written with the bits ORed in.

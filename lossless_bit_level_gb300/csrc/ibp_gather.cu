@@ -29,6 +29,9 @@
 // The loop is software-pipelined two deep: the next unit's plan and staging are
 // issued before the current unit is decoded, and the index two units ahead is
 // prefetched, so header and body round trips overlap with decode.
+// De-duplicated gathers of rows that are one unit each use a claiming instantiation
+// (CLAIM): before a unit is planned its leader claims the row in a hash table, and
+// only the first claimant stages and decodes it (ibp_dedup.cu copies the rest).
 #include <algorithm>
 #include <atomic>
 
