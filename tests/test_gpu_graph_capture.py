@@ -1,7 +1,7 @@
 """Every compute call of the C ABI captured in one CUDA graph and replayed (needs a GPU).
 
 The header states that the calls may be captured once their argument checks pass;
-this builds metadata (threshold, saving-aware, per-position), compresses, gathers
+the test builds metadata (threshold, saving-aware, per-position), compresses, gathers
 (plain, packed, per-position and de-duplicated, the last for short and long rows),
 packs and streams a range inside one capture, replays the graph on fresh inputs and
 checks every output against the oracle."""
