@@ -986,8 +986,10 @@ def configs_leg(dev, flush, hbm_peak, link, main):
       DLRM: table 0 (65,536 Zipf(1.05) lookups, host and HBM) and all 26 tables in
         HBM, one lookup batch per table per step, 26 separate calls vs one batched call;
       LLM BF16: layer 0's seven weights and its K and V caches (8 x 4096 tokens), each
-        tensor streamed in order through ibp_decompress_range from host and from HBM;
-        summed over the layer (the other 31 layers have the same shapes and
+        tensor streamed in order through ibp_decompress_range from host and from HBM
+        (the weights also with one launch per row geometry: a batched call for the six
+        with 4096-element rows, a range call for the down-projection); summed over the
+        layer (the other 31 layers have the same shapes and
         distributions, so a layer's time scales by 32 for the model).
     Every gather's output is checked against the original rows on the device."""
     import concurrent.futures as cf
@@ -1104,6 +1106,7 @@ def configs_leg(dev, flush, hbm_peak, link, main):
     # LLM: one decoder layer, every row of each tensor streamed in order
     parts = {"weights": [*gen.LLM_MATRICES], "kv": ["K", "V"]}
     acc = {}
+    kept = []  # the weights' HBM stores, for the one-launch-per-row-geometry decode
     for part, names in parts.items():
         a = dict(raw=0, stored=0, t_comp=0.0, comp_alg=0.0, host=0.0, device=0.0)
         for name in names:
@@ -1116,10 +1119,55 @@ def configs_leg(dev, flush, hbm_peak, link, main):
             a["comp_alg"] += tb.comp_alg
             for where in ("host", "device"):
                 a[where] += tb.gather(where, None, steps=6)
+            if part == "weights":
+                tb.host_slots = None
+                kept.append(tb)
             del tb, words
             torch.cuda.empty_cache()
         acc[part] = a
     pool.shutdown()
+
+    # the same weights decoded with one launch per row geometry: the tensors with
+    # 4096-element rows in one batched call (their rows in order as index lists), the
+    # down-projection (11008-element rows) in one range call
+    geo = {}
+    for tb in kept:
+        geo.setdefault(tb.st.L, []).append(tb)
+    calls, alg_b = [], 0.0
+    for L_g, tbs in geo.items():
+        if len(tbs) == 1:
+            st = tbs[0].st
+            out = torch.empty_like(st.rows)
+            calls.append(lambda k, st=st, out=out, L_g=L_g: ibp.decompress_range(
+                st.slots, st.n, L_g, ibp.BF16, 64, st.bitmask, st.meta, 0, st.n, out))
+            alg_b += float(tbs[0].stored.sum()) + tbs[0].raw
+            checks = [(out, st.rows)]
+        else:
+            jobs_w = []
+            for tb in tbs:
+                st = tb.st
+                out = torch.empty_like(st.rows)
+                jobs_w.append((st.slots, st.n, st.bitmask, st.meta,
+                               torch.arange(st.n, dtype=torch.int64, device=dev), out))
+                alg_b += float(tb.stored.sum()) + tb.raw + 8 * st.n
+            calls.append(lambda k, jobs_w=jobs_w, L_g=L_g: ibp.decompress_gather_batched(
+                jobs_w, L_g, ibp.BF16, 64))
+            checks = [(j[5], tb.st.rows) for j, tb in zip(jobs_w, tbs)]
+        geo[L_g] = checks
+
+    def per_geometry(k):
+        for c in calls:
+            c(k)
+
+    t_b = time_steps(per_geometry, 6, 3, flush)
+    torch.cuda.synchronize()
+    for checks in geo.values():
+        for out, rows in checks:
+            assert torch.equal(out, rows), "decoded weights differ from the originals"
+    weights_batched = {"ms": _sig(t_b * 1e3), "GBs": _sig(acc["weights"]["raw"] / t_b / 1e9),
+                       "frac": _sig(alg_b / t_b / 1e9 / hbm_peak), "launches": len(calls)}
+    del kept, geo, calls
+    torch.cuda.empty_cache()
 
     def llm_entry(a):
         e = {"save_pct": _sig(100.0 * (1.0 - a["stored"] / a["raw"])),
@@ -1135,6 +1183,7 @@ def configs_leg(dev, flush, hbm_peak, link, main):
     res["llm_layer0"] = {"all": llm_entry(layer), "weights": llm_entry(acc["weights"]),
                          "kv": llm_entry(acc["kv"]),
                          "note": "ms per layer; 32 layers of the same shapes: x32"}
+    res["llm_layer0"]["weights"]["hbm_per_geometry"] = weights_batched
     return res
 
 
