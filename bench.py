@@ -1353,6 +1353,9 @@ def main():
     args.steps, args.warmup = steps, warmup
     if warmup < 3 and args.impl == "ibp":
         raise SystemExit("at least 3 warm-up steps are required")
+    legs = None if args.legs is None else set(args.legs.split(","))
+    if legs is not None and not legs <= set(LEGS):
+        raise SystemExit(f"unknown legs: {sorted(legs - set(LEGS))}")
     wl = workload_table(args.workload)
     if args.residency:
         wl["residency"] = args.residency
@@ -1457,10 +1460,6 @@ def main():
                     "frac": achieved / hbm_peak, "traffic": traffic,
                     "peak_source": f"{hbm_peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                     "algorithmic_bytes_per_launch": alg}
-
-    legs = None if args.legs is None else set(args.legs.split(","))
-    if legs is not None and not legs <= set(LEGS):
-        raise SystemExit(f"unknown legs: {sorted(legs - set(LEGS))}")
 
     def want(leg):
         return (not args.quick) if legs is None else leg in legs

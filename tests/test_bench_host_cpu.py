@@ -69,3 +69,12 @@ def test_oracle_baselines_single_and_all_cores():
     for d in (one, every):
         assert d["kind"] == "oracle" and d["unit"] == "GB/s" and d["value"] > 0
         assert d["batches"] >= 1
+
+
+def test_unknown_legs_are_refused_before_any_work():
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, bench.__file__, "--legs", "dedup,nonsense"],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "unknown legs" in r.stderr and "nonsense" in r.stderr
