@@ -107,8 +107,9 @@ int launch_gather(const void *slots, int64_t slot_bytes, const uint64_t *d_offse
                   bool pos_in_index = false,
                   const unsigned long long *d_idx_count = nullptr,
                   const ClaimTable *claim = nullptr);
-// De-duplicated slotted gather: every distinct row of d_idx is read and decoded
-// once (into d_scratch), then copied to each output position that asks for it.
+// De-duplicated slotted gather: every distinct row of d_idx is read and decoded once,
+// into the output row of the position that claimed it, then copied to each other
+// output position that asks for it (d_scratch holds the claim table and lists).
 size_t dedup_scratch_bytes(int64_t n_idx, const RowGeom &g);
 int64_t dedup_max_indices();  // index positions share a 64-bit word with the row
 int launch_gather_dedup(const void *slots, int64_t slot_bytes, int64_t n_rows, const RowGeom &g,
